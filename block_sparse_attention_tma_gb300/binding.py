@@ -1,0 +1,237 @@
+"""Thin ctypes binding of libgbattn.so (argument marshalling only).
+
+Every entry point has the name of its C counterpart in include/gbattn.h and
+passes device pointers, sizes and the current CUDA stream straight through;
+PyTorch only allocates the output / workspace tensors. There is no fallback:
+if the library cannot be loaded, or a call returns an error status, a
+GbattnError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+
+NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK = range(6)
+BF16, FP32 = 0, 1
+_DT = {torch.bfloat16: BF16, torch.float32: FP32}
+
+OK = 0
+ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_BLOCKS, ERR_CUDA, ERR_TIMEOUT = -1, -2, -3, -4, -5, -6, -7
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {code} ({strerror(code)})")
+
+
+class _Mask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("window_left", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("prefix_len", ctypes.c_int), ("topk", ctypes.c_int), ("rel_bias_slope", ctypes.c_float),
+                ("softcap", ctypes.c_float), ("key_bias", ctypes.c_void_p)]
+
+
+class _Blocks(ctypes.Structure):
+    _fields_ = [("sparse_m", ctypes.c_int), ("sparse_n", ctypes.c_int)] + [
+        (n, ctypes.c_void_p) for n in ("q_mask_cnt", "q_mask_idx", "q_full_cnt", "q_full_idx",
+                                       "k_mask_cnt", "k_mask_idx", "k_full_cnt", "k_full_idx", "keep_bits")]
+
+
+_lib = None
+
+# (name, restype, argtypes)
+_SIGS = [
+    ("gbattn_version", ctypes.c_int, []),
+    ("gbattn_strerror", ctypes.c_char_p, [ctypes.c_int]),
+    ("gbattn_block_mask_sizes", ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)] * 5),
+    ("build_block_mask", ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(_Mask), ctypes.POINTER(_Blocks),
+                                                              ctypes.c_void_p]),
+    ("attn_fwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.POINTER(_Mask),
+                                                                              ctypes.POINTER(_Blocks),
+                                                                              ctypes.c_void_p, ctypes.c_void_p,
+                                                                              ctypes.c_void_p]),
+    ("attn_bwd_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 7),
+    ("attn_bwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.POINTER(_Mask),
+                                                                              ctypes.POINTER(_Blocks), ctypes.c_int]
+     + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
+    ("attn_fwd_splitkv_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 5),
+    ("attn_fwd_splitkv", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float,
+                                                                                      ctypes.POINTER(_Mask),
+                                                                                      ctypes.c_int]
+     + [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
+    ("gbattn_last_device_error", ctypes.c_int, [ctypes.c_void_p]),
+]
+
+EXPORTS = [s[0] for s in _SIGS]
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libgbattn.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise GbattnError(ERR_CUDA, f"libgbattn.so not found at {path}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, res, args in _SIGS:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load_library().gbattn_strerror(code).decode()
+    except Exception:  # the library itself may be what is missing
+        return "unknown"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise GbattnError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+@dataclass
+class MaskSpec:
+    kind: int = NONE
+    window_left: int = -1
+    block_size: int = 0
+    prefix_len: int = 0
+    topk: int = 0
+    rel_bias_slope: float = 0.0
+    softcap: float = 0.0
+    key_bias: Optional[torch.Tensor] = None  # [B, H, Sk] fp32 on the GPU
+
+    def c(self) -> _Mask:
+        return _Mask(self.kind, self.window_left, self.block_size, self.prefix_len, self.topk,
+                     float(self.rel_bias_slope), float(self.softcap),
+                     None if self.key_bias is None else self.key_bias.data_ptr())
+
+
+@dataclass
+class BlockLists:
+    sparse_m: int
+    sparse_n: int
+    tensors: dict = field(default_factory=dict)  # name -> int32 / uint32-as-int32 tensor
+
+    def c(self) -> _Blocks:
+        b = _Blocks(self.sparse_m, self.sparse_n)
+        for name, t in self.tensors.items():
+            setattr(b, name, t.data_ptr())
+        return b
+
+
+def alloc_block_lists(B, H, Sq, Sk, sparse_m, sparse_n, device="cuda") -> BlockLists:
+    lib = load_library()
+    sz = [ctypes.c_size_t() for _ in range(5)]
+    _check(lib.gbattn_block_mask_sizes(B, H, Sq, Sk, sparse_m, sparse_n, *[ctypes.byref(s) for s in sz]),
+           "gbattn_block_mask_sizes")
+    qc, qi, kc, ki, kw = (s.value // 4 for s in sz)
+    mk = lambda n: torch.empty(max(n, 1), dtype=torch.int32, device=device)  # noqa: E731
+    t = {"q_mask_cnt": mk(qc), "q_mask_idx": mk(qi), "q_full_cnt": mk(qc), "q_full_idx": mk(qi),
+         "k_mask_cnt": mk(kc), "k_mask_idx": mk(ki), "k_full_cnt": mk(kc), "k_full_idx": mk(ki),
+         "keep_bits": mk(kw)}
+    return BlockLists(sparse_m, sparse_n, t)
+
+
+def build_block_mask(B, H, Sq, Sk, mask: MaskSpec, lists: BlockLists, stream=None) -> BlockLists:
+    lib = load_library()
+    cm, cb = mask.c(), lists.c()
+    _check(lib.build_block_mask(B, H, Sq, Sk, ctypes.byref(cm), ctypes.byref(cb), _stream(stream)),
+           "build_block_mask")
+    return lists
+
+
+def attn_fwd(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, lists: Optional[BlockLists] = None,
+             o=None, lse=None, stream=None):
+    lib = load_library()
+    B, H, Sq, Dqk = q.shape
+    Sk, Dv = k.shape[2], v.shape[3]
+    if o is None:
+        o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    mask = mask or MaskSpec()
+    cm = mask.c()
+    cb = lists.c() if lists is not None else None
+    _check(lib.attn_fwd(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), float(scale),
+                        ctypes.byref(cm), ctypes.byref(cb) if cb is not None else None, _ptr(o), _ptr(lse),
+                        _stream(stream)), "attn_fwd")
+    return o, lse
+
+
+def attn_bwd_workspace_bytes(dtype, B, H, Sq, Sk, Dqk, Dv) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(_DT.get(dtype, -1), B, H, Sq, Sk, Dqk, Dv))
+
+
+def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
+             lists: Optional[BlockLists] = None, deterministic=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    lib = load_library()
+    B, H, Sq, Dqk = q.shape
+    Sk, Dv = k.shape[2], v.shape[3]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = attn_bwd_workspace_bytes(q.dtype, B, H, Sq, Sk, Dqk, Dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    mask = mask or MaskSpec()
+    cm = mask.c()
+    cb = lists.c() if lists is not None else None
+    _check(lib.attn_bwd(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                        _ptr(lse), float(scale), ctypes.byref(cm), ctypes.byref(cb) if cb is not None else None,
+                        int(bool(deterministic)), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream)), "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits) -> int:
+    return int(load_library().attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits))
+
+
+def attn_fwd_splitkv(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_splits=1, o=None, lse=None,
+                     workspace=None, stream=None):
+    lib = load_library()
+    B, H, Sq, Dqk = q.shape
+    Sk, Dv = k.shape[2], v.shape[3]
+    if o is None:
+        o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    need = attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    mask = mask or MaskSpec()
+    cm = mask.c()
+    _check(lib.attn_fwd_splitkv(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), float(scale),
+                                ctypes.byref(cm), int(num_splits), _ptr(o), _ptr(lse), _ptr(workspace),
+                                0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                _stream(stream)), "attn_fwd_splitkv")
+    return o, lse
+
+
+def last_device_error(stream=None) -> int:
+    return int(load_library().gbattn_last_device_error(_stream(stream)))

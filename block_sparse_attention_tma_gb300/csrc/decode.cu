@@ -1,0 +1,301 @@
+// decode.cu - split-KV forward for decode shapes, and the split combine.
+//
+// "Optimize Flash Dynamic Mask Attention Kernel Configurations" simplifies the
+// split-KV forward path and tests 1/2/4/8/16 splits; it also notes that
+// Q = 1 / very long K is memory-bound. Here each CTA = (b, h, query row,
+// split) streams its contiguous K/V key range once from HBM with 1-D bulk
+// copies (cp.async.bulk) into a 4-stage shared-memory ring; 8 compute warps
+// read 16-byte vectors from it. Each warp keeps its own running max / sum /
+// output over its keys (online softmax); the warps are merged at the end and
+// the split partials are merged by a combine kernel using the rule of the
+// POPCORNBENCH "Kimi-K2.6 l1_p97" trace: m = max_s m_s, weights exp(m_s - m).
+#include "kernels.h"
+#include "mask.cuh"
+
+namespace gb {
+
+constexpr int kDecWarps = 8;                 // compute warps
+constexpr int kDecThreads = 32 * (kDecWarps + 1);
+constexpr int kDecChunk = 64;                // keys per stage
+constexpr int kDecStages = 4;
+
+struct DecParams {
+  const __nv_bfloat16 *q, *k, *v;
+  __nv_bfloat16* o;
+  float* lse;
+  float* o_part;     // [n][BH][Sq][D]
+  float* lse_part;   // [n][BH][Sq]
+  int BH, Sq, Sk, nsplit, per, causal;
+  float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams p) {
+  constexpr int ROWB = D * 2;                       // bytes per key row
+  constexpr int CHB = kDecChunk * ROWB;             // bytes per K (or V) chunk
+  constexpr int EPL = D / 32;                       // V elements per lane (PV phase)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* sK = base;
+  uint8_t* sV = sK + kDecStages * CHB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sV + kDecStages * CHB);
+  uint64_t* empty = full + kDecStages;
+  float* red = reinterpret_cast<float*>(empty + kDecStages);  // [kDecWarps][D + 2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kDecWarps * (D + 2));
+
+  const int split = blockIdx.x % p.nsplit;
+  const int rowid = blockIdx.x / p.nsplit;  // bh * Sq + i
+  const int bh = rowid / p.Sq, i = rowid % p.Sq;
+  int kb = split * p.per;
+  int ke = min(kb + p.per, p.Sk);
+  if (p.causal) ke = min(ke, i + (p.Sk - p.Sq) + 1);
+  const int nkeys = max(0, ke - kb);
+  const int nchunks = (nkeys + kDecChunk - 1) / kDecChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kDecWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const __nv_bfloat16* Kg = p.k + ((size_t)bh * p.Sk + kb) * D;
+  const __nv_bfloat16* Vg = p.v + ((size_t)bh * p.Sk + kb) * D;
+
+  if (warp == kDecWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kDecStages;
+        if (c >= kDecStages && !mbar_wait(empty + s, ((c / kDecStages) + 1) & 1, abort_flag)) break;
+        const int rows = min(kDecChunk, nkeys - c * kDecChunk);
+        const uint32_t bytes = (uint32_t)rows * ROWB;
+        mbar_expect_tx(full + s, 2 * bytes);
+        bulk_load(sK + s * CHB, Kg + (size_t)c * kDecChunk * D, bytes, full + s);
+        bulk_load(sV + s * CHB, Vg + (size_t)c * kDecChunk * D, bytes, full + s);
+        ++issued;
+      }
+      if (*abort_flag)
+        for (int c = (issued > kDecStages ? issued - kDecStages : 0); c < issued; ++c)
+          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int g = lane >> 3, sub = lane & 7;  // 4 groups of 8 lanes, one key per group
+    // q slice of this lane for the score phase: elements [64 h + 8 sub, +8)
+    float qv[D / 8];
+    const __nv_bfloat16* qrow = p.q + ((size_t)bh * p.Sq + i) * D;
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(qrow + h * 64 + sub * 8);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(b2[e]);
+        qv[h * 8 + 2 * e] = f.x * p.scale_log2;
+        qv[h * 8 + 2 * e + 1] = f.y * p.scale_log2;
+      }
+    }
+    float m = -INFINITY, l = 0.f;
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kDecStages;
+      ok = mbar_wait(full + s, (c / kDecStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const int rows = min(kDecChunk, nkeys - c * kDecChunk);
+      const uint8_t* kc = sK + s * CHB;
+      const uint8_t* vc = sV + s * CHB;
+      // scores of this warp's 8 keys: key (warp * 8 + it * 4 + g)
+      float sc[2];
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int key = warp * 8 + it * 4 + g;
+        float dot = 0.f;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(kc + key * ROWB + h * 128 + sub * 16);
+          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(b2[e]);
+            dot = fmaf(f.x, qv[h * 8 + 2 * e], dot);
+            dot = fmaf(f.y, qv[h * 8 + 2 * e + 1], dot);
+          }
+        }
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        sc[it] = (key < rows) ? dot : -INFINITY;
+      }
+      float mc = fmaxf(sc[0], sc[1]);
+      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
+      mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+      const float mn = fmaxf(m, mc);
+      const float msafe = (mn == -INFINITY) ? 0.f : mn;
+      const float alpha = ex2(m - msafe);  // m = -inf -> 0
+      float pr[2];
+      pr[0] = ex2(sc[0] - msafe);
+      pr[1] = ex2(sc[1] - msafe);
+      float ls = pr[0] + pr[1];
+      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+      l = l * alpha + ls;
+      m = mn;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] *= alpha;
+      // O += sum over the 8 keys of p_key * v_key; lane owns EPL dims
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const float pk = __shfl_sync(0xffffffffu, pr[it], gg * 8);
+          const int key = warp * 8 + it * 4 + gg;
+          if (key >= rows) continue;  // stale smem beyond the chunk end
+          if constexpr (EPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(vc + key * ROWB + lane * 8);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+            acc[0] = fmaf(pk, f0.x, acc[0]);
+            acc[1] = fmaf(pk, f0.y, acc[1]);
+            acc[2] = fmaf(pk, f1.x, acc[2]);
+            acc[3] = fmaf(pk, f1.y, acc[3]);
+          } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(vc + key * ROWB + lane * 4);
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw));
+            acc[0] = fmaf(pk, f0.x, acc[0]);
+            acc[1] = fmaf(pk, f0.y, acc[1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+    // publish this warp's (m, l, acc) for the merge
+    float* rw = red + warp * (D + 2);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) rw[lane * EPL + e] = acc[e];
+    if (lane == 0) {
+      rw[D] = m;
+      rw[D + 1] = l;
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) return;
+  // merge the warps (threads 0..D-1, one output element each)
+  if (threadIdx.x < D) {
+    const int d = threadIdx.x;
+    float mx = -INFINITY;
+    for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, red[w * (D + 2) + D]);
+    float lt = 0.f, ot = 0.f;
+    if (mx != -INFINITY) {
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float wgt = ex2(red[w * (D + 2) + D] - mx);
+        lt += wgt * red[w * (D + 2) + D + 1];
+        ot += wgt * red[w * (D + 2) + d];
+      }
+    }
+    const bool live = lt > 0.f;
+    const float val = live ? ot / lt : 0.f;
+    const float lse_nat = live ? (mx + __log2f(lt)) * kLn2 : -INFINITY;
+    if (p.nsplit == 1) {
+      p.o[(size_t)rowid * D + d] = __float2bfloat16_rn(val);
+      if (d == 0 && p.lse) p.lse[rowid] = lse_nat;
+    } else {
+      const size_t prow = (size_t)split * p.BH * p.Sq + rowid;
+      p.o_part[prow * D + d] = val;
+      if (d == 0) p.lse_part[prow] = lse_nat;
+    }
+  }
+}
+
+// One warp per (b, h, query row): merge the split partials.
+template <int D>
+__global__ void combine_kernel(const DecParams p) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)p.BH * p.Sq;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < p.nsplit; ++s) mx = fmaxf(mx, p.lse_part[s * rows + row]);
+  float acc[D / 32];
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
+  float tot = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < p.nsplit; ++s) {
+      const float ls = p.lse_part[s * rows + row];
+      const float w = (ls == -INFINITY) ? 0.f : __expf(ls - mx);
+      tot += w;
+      const float* op = p.o_part + (s * rows + row) * D;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) acc[e] = fmaf(w, op[lane + 32 * e], acc[e]);
+    }
+  }
+  const bool live = tot > 0.f;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e)
+    p.o[row * D + lane + 32 * e] = __float2bfloat16_rn(live ? acc[e] / tot : 0.f);
+  if (lane == 0 && p.lse) p.lse[row] = live ? mx + __logf(tot) : -INFINITY;
+}
+
+template <int D>
+static int launch_dec(const DecParams& prm, cudaStream_t st) {
+  constexpr int CHB = kDecChunk * D * 2;
+  constexpr int SMEM = 128 + 2 * kDecStages * CHB + 2 * kDecStages * 8 + kDecWarps * (D + 2) * 4 + 16;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+      return GBATTN_ERR_CUDA;
+    attr = true;
+  }
+  const long long grid = (long long)prm.BH * prm.Sq * prm.nsplit;
+  if (grid >= (1ll << 31)) return GBATTN_ERR_ARG;
+  splitkv_kernel<D><<<(unsigned)grid, kDecThreads, SMEM, st>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  if (prm.nsplit > 1) {
+    const long long rows = (long long)prm.BH * prm.Sq;
+    combine_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  }
+  return GBATTN_OK;
+}
+
+int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st) {
+  DecParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.k = static_cast<const __nv_bfloat16*>(k);
+  prm.v = static_cast<const __nv_bfloat16*>(v);
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.BH = s.B * s.H;
+  prm.Sq = s.Sq;
+  prm.Sk = s.Sk;
+  prm.nsplit = num_splits;
+  int per = (s.Sk + num_splits - 1) / num_splits;
+  per = (per + 127) / 128 * 128;
+  prm.per = per;
+  prm.causal = causal;
+  prm.scale_log2 = scale * kLog2e;
+  if (num_splits > 1) {
+    const size_t rows = (size_t)num_splits * prm.BH * s.Sq;
+    prm.o_part = static_cast<float*>(ws);
+    prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(rows * s.Dv * sizeof(float), 256));
+  }
+  if (s.Dqk == 128) return launch_dec<128>(prm, st);
+  if (s.Dqk == 64) return launch_dec<64>(prm, st);
+  return GBATTN_ERR_UNSUPPORTED;
+}
+
+GB_DEFINE_ERROR_READER(decode_take_error)
+
+}  // namespace gb

@@ -1,0 +1,447 @@
+// fwd_sm103.cu - fused attention forward on the 5th-generation tensor cores.
+//
+// Method: "Optimize Flash Dynamic Mask Attention Kernel Configurations"
+// (forward kernel; masks, softcap) and "Enable 2CTA for SM100 block-sparse
+// backward" (forward driven by block-sparse lists, q/kv sub-tiling of a
+// sparse block into 128 x 128 kernel tiles, QK/V head dims 192/128). The
+// running max / sum update is the online-softmax merge of the POPCORNBENCH
+// "Kimi-K2.6 l1_p97" trace (m_new = max, rescale by exp(m_old - m_new)).
+//
+// One CTA = one (b, h, 128-row query tile); 6 warps:
+//   warp 0      TMA producer: Q once, then K and V tiles into a ring.
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (two buffers),
+//               O += P V with P read from TMEM (A operand) and V from smem.
+//   warps 2..5  softmax: thread = query row = TMEM lane. Loads its S row,
+//               masks, exp2 with the scale folded in, writes P (bf16) back
+//               over the S buffer, rescales O only when the row max grows by
+//               more than 2^8 ("lazy" rescale), final O / l and LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv).
+#include "kernels.h"
+#include "mask.cuh"
+
+namespace gb {
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;
+  int B, H, Sq, Sk;
+  int nqt;             // query tiles per head
+  float scale_log2;    // scale * log2(e)
+  float cap_pre;       // scale / softcap (softcap on), else 0
+  float cap_post;      // softcap * log2(e)
+  int has_colterm;     // key bias or rel-bias slope present
+  MaskParams mask;
+  int has_lists;
+  int sub;             // sparse_n / 128
+  int nqb, nkb, sparse_m;
+  const int32_t *mcnt, *midx, *fcnt, *fidx;  // forward lists
+  __nv_bfloat16* o;
+  float* lse;
+};
+
+template <int DQK, int DV>
+struct FwdCfg {
+  static constexpr int SWQ = DQK >= 64 ? 128 : 64;  // swizzle span of Q/K rows
+  static constexpr int SWV = DV >= 64 ? 128 : 64;
+  static constexpr int QSLAB = 128 * SWQ;           // bytes of one 128-row slab
+  static constexpr int NQSLAB = DQK * 2 / SWQ;
+  static constexpr int QTILE = 128 * DQK * 2;
+  static constexpr int VSLAB = 128 * SWV;
+  static constexpr int NVSLAB = DV * 2 / SWV;
+  static constexpr int VTILE = 128 * DV * 2;
+  static constexpr int KST = DQK >= 192 ? 2 : 3;
+  static constexpr int VST = DQK >= 128 ? 2 : 3;
+  // barriers: q_full, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
+  // s_full[2], p_full[2], o_done, drain
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
+  // TMEM columns are the whole TMEM)
+  static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sK = sQ + C::QTILE;
+  uint8_t* sV = sK + C::KST * C::QTILE;
+  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 warps][2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + C::KST;
+  uint64_t* v_full = k_empty + C::KST;
+  uint64_t* v_empty = v_full + C::VST;
+  uint64_t* s_full = v_empty + C::VST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int L = blockIdx.x;
+  const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
+  const int bh = L % BH;
+  const int q0 = qt * 128;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128); }
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Tile walk of this CTA (identical in every role).
+  TileWalk walk;
+  int nslots;
+  if (p.has_lists) {
+    const int r = q0 / p.sparse_m;
+    walk = make_walk(p.mcnt, p.midx, p.fcnt, p.fidx, bh * p.nqb + r, p.nkb, p.sub, p.Sk);
+    nslots = walk.nslots;
+  } else {
+    nslots = (p.Sk + 127) / 128;
+  }
+  auto slot = [&](int s, int* kv0, bool* masked) -> bool {
+    return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
+                       : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      int n = 0, nk = 0, nv = 0;
+      bool ok = true;
+      for (int s = 0; s < nslots && ok; ++s) {
+        int kv0;
+        bool masked;
+        if (!slot(s, &kv0, &masked)) continue;
+        if (n == 0) {
+          mbar_expect_tx(q_full, C::QTILE);
+          for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+        }
+        const int ks = n % C::KST;
+        if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(k_full + ks, C::QTILE);
+        for (int j = 0; j < C::NQSLAB; ++j)
+          tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bh);
+        ++nk;
+        const int vs = n % C::VST;
+        if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(v_full + vs, C::VTILE);
+        for (int j = 0; j < C::NVSLAB; ++j)
+          tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bh);
+        ++nv;
+        ++n;
+      }
+      if (*abort_flag) {
+        // let every copy this thread started land before the CTA exits
+        if (nk > 0) mbar_drain(q_full, 0);
+        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
+        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+      auto issue_pv = [&](int j) -> bool {
+        const int sb = j & 1;
+        if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
+        const int vs = j % C::VST;
+        if (!mbar_wait(v_full + vs, (j / C::VST) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows
+          const uint64_t bd = sdesc(va + vs * C::VTILE + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV));
+          umma_ts(tmem + 256, tmem + sb * 128 + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(v_empty + vs);
+        umma_commit(o_done);
+        return true;
+      };
+      int n = 0;
+      bool ok = true;
+      for (int s = 0; s < nslots && ok; ++s) {
+        int kv0;
+        bool masked;
+        if (!slot(s, &kv0, &masked)) continue;
+        if (n == 0 && !(ok = mbar_wait(q_full, 0, abort_flag))) break;
+        const int ks = n % C::KST;
+        if (!(ok = mbar_wait(k_full + ks, (n / C::KST) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (n & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const int slab = (kk * 16) / (C::SWQ / 2);
+          const int off = (kk * 32) % C::SWQ;
+          const uint64_t ad = sdesc(qa + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ));
+          const uint64_t bd = sdesc(ka + ks * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ));
+          umma_ss(d, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(k_empty + ks);
+        umma_commit(s_full + (n & 1));
+        if (n >= 1 && !(ok = issue_pv(n - 1))) break;
+        ++n;
+      }
+      if (ok && n >= 1) issue_pv(n - 1);
+      if (*abort_flag) {
+        umma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int i = q0 + row;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    int lo, hi;
+    row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
+    const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
+    const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
+    const float slope_log2 = p.mask.slope * kLog2e;
+    float m_run = -INFINITY, l_run = 0.f;
+    int n = 0;
+    bool ok = true;
+    for (int s = 0; s < nslots && ok; ++s) {
+      int kv0;
+      bool masked;
+      if (!slot(s, &kv0, &masked)) continue;
+      const int sb = n & 1;
+      // per-key score term (key bias - slope * j) * log2(e); each warp keeps
+      // its own copy (4 keys per lane), so only a warp-level sync is needed
+      float* ctw = colterm + (quarter * 2 + sb) * 128;
+      if (p.has_colterm) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = kv0 + e * 32 + lane;
+          float c = 0.f;
+          if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
+          ctw[e * 32 + lane] = c;
+        }
+        __syncwarp();
+      }
+      ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[128];
+      tmem_ld32(tl + sb * 128 + 0, r);
+      tmem_ld32(tl + sb * 128 + 32, r + 32);
+      tmem_ld32(tl + sb * 128 + 64, r + 64);
+      tmem_ld32(tl + sb * 128 + 96, r + 96);
+      tmem_wait_ld32(r);
+      reg_fence32(r + 32);
+      reg_fence32(r + 64);
+      reg_fence32(r + 96);
+      float t[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float x = __uint_as_float(r[c]);
+        x = (p.cap_pre != 0.f) ? p.cap_post * tanh_fast(x * p.cap_pre) : x * p.scale_log2;
+        t[c] = x;
+      }
+      if (p.has_colterm) {
+        const float4* ct = reinterpret_cast<const float4*>(ctw);
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4) {
+          const float4 v4 = ct[c4];
+          t[4 * c4 + 0] += v4.x;
+          t[4 * c4 + 1] += v4.y;
+          t[4 * c4 + 2] += v4.z;
+          t[4 * c4 + 3] += v4.w;
+        }
+      }
+      if (masked) {
+        const int clo = lo - kv0;
+        const int chi = min(hi, p.Sk - 1) - kv0;
+        if (keep) {
+          uint32_t kw[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int wi = (kv0 >> 5) + w;
+            kw[w] = wi < p.mask.nkw ? __ldg(keep + wi) : 0u;
+          }
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const bool okc = (c >= clo) && (c <= chi) && ((kw[c >> 5] >> (c & 31)) & 1u);
+            t[c] = okc ? t[c] : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
+        }
+      }
+      float mt = t[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, t[c]);
+      float m_use = m_run, alpha = 1.f;
+      bool resc = false;
+      if (mt > m_run + 8.0f) {
+        if (m_run != -INFINITY) {
+          resc = true;
+          alpha = ex2(m_run - mt);
+        }
+        m_use = mt;
+      }
+      const float msafe = (m_use == -INFINITY) ? 0.f : m_use;
+      float lsum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float a0 = ex2(t[2 * c] - msafe);
+        const float a1 = ex2(t[2 * c + 1] - msafe);
+        lsum += a0 + a1;
+        pk[c] = pack_bf16(a0, a1);
+      }
+      l_run = (resc ? l_run * alpha : l_run) + lsum;
+      m_run = m_use;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must not be in flight: PV of the previous tile has completed
+        ok = mbar_wait(o_done, (n - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t orr[32];
+          tmem_ld32(tl + 256 + c0, orr);
+          tmem_wait_ld32(orr);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+          tmem_st32(tl + 256 + c0, orr);
+        }
+      }
+      tmem_st32(tl + sb * 128 + 0, pk);
+      tmem_st32(tl + sb * 128 + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + sb);
+      ++n;
+    }
+    // ---- epilogue
+    if (ok && i < p.Sq) {
+      __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
+      if (n == 0 || l_run == 0.f) {
+#pragma unroll
+        for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        if (p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
+      }
+    }
+    if (ok && n > 0) {
+      if (__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t orr[32];
+          tmem_ld32(tl + 256 + c0, orr);
+          tmem_wait_ld32(orr);
+          if (i < p.Sq && l_run > 0.f) {
+            uint32_t pkd[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              pkd[c] = pack_bf16(__uint_as_float(orr[2 * c]) * inv, __uint_as_float(orr[2 * c + 1]) * inv);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(orow + c0 + 8 * c) =
+                  make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+          }
+        }
+        if (i < p.Sq && l_run > 0.f && p.lse)
+          p.lse[(size_t)bh * p.Sq + i] = (m_run + __log2f(l_run)) * kLn2 + p.mask.slope * (float)i;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int DQK, int DV>
+static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
+  using C = FwdCfg<DQK, DV>;
+  auto kern = fwd_bf16_kernel<DQK, DV>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return GBATTN_ERR_CUDA;
+    attr_set = true;
+  }
+  kern<<<grid, 192, C::SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, const HostMask& m,
+                    void* o, float* lse, cudaStream_t st) {
+  FwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int BH = s.B * s.H;
+  const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
+  if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
+  if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
+  if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+  prm.B = s.B;
+  prm.H = s.H;
+  prm.Sq = s.Sq;
+  prm.Sk = s.Sk;
+  prm.nqt = (s.Sq + 127) / 128;
+  prm.scale_log2 = scale * kLog2e;
+  if (m.softcap > 0.f) {
+    prm.cap_pre = scale / m.softcap;
+    prm.cap_post = m.softcap * kLog2e;
+  }
+  prm.has_colterm = (m.key_bias != nullptr) || (m.slope != 0.f);
+  prm.mask.kind = m.kind;
+  prm.mask.window_left = m.window_left;
+  prm.mask.block_size = m.block_size;
+  prm.mask.prefix_len = m.prefix_len;
+  prm.mask.slope = m.slope;
+  prm.mask.key_bias = m.key_bias;
+  prm.mask.keep = m.kind == GBATTN_MASK_DYNAMIC_TOPK ? m.keep : nullptr;
+  prm.mask.nkw = (s.Sk + 31) / 32;
+  prm.has_lists = m.has_lists;
+  if (m.has_lists) {
+    prm.sub = m.sparse_n / 128;
+    prm.nqb = m.nqb;
+    prm.nkb = m.nkb;
+    prm.sparse_m = m.sparse_m;
+    prm.mcnt = m.q_mask_cnt;
+    prm.midx = m.q_mask_idx;
+    prm.fcnt = m.q_full_cnt;
+    prm.fidx = m.q_full_idx;
+  }
+  prm.o = reinterpret_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  const int grid = prm.nqt * BH;
+  if (s.Dqk == 32 && s.Dv == 32) return launch_fwd<32, 32>(prm, grid, st);
+  if (s.Dqk == 64 && s.Dv == 64) return launch_fwd<64, 64>(prm, grid, st);
+  if (s.Dqk == 128 && s.Dv == 128) return launch_fwd<128, 128>(prm, grid, st);
+  if (s.Dqk == 192 && s.Dv == 128) return launch_fwd<192, 128>(prm, grid, st);
+  return GBATTN_ERR_UNSUPPORTED;
+}
+
+GB_DEFINE_ERROR_READER(fwd_take_error)
+
+}  // namespace gb

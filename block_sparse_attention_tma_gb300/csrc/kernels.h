@@ -1,0 +1,61 @@
+// kernels.h - host-side interface between the C ABI (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gbattn.h"
+
+namespace gb {
+
+struct Shape {
+  int B, H, Sq, Sk, Dqk, Dv;
+};
+
+// Validated, device-ready view of the mask and lists of one call.
+struct HostMask {
+  int kind, window_left, block_size, prefix_len, topk;
+  float slope, softcap;
+  const float* key_bias;
+  const uint32_t* keep;
+  int has_lists;
+  int sparse_m, sparse_n, nqb, nkb;
+  const int32_t *q_mask_cnt, *q_mask_idx, *q_full_cnt, *q_full_idx;
+  const int32_t *k_mask_cnt, *k_mask_idx, *k_full_cnt, *k_full_idx;
+};
+
+// Encodes a 3-D bf16 tensor map over [BH, S, D] (D innermost) with a box of
+// (swizzle_bytes/2) x 128 x 1 and the given swizzle (64 or 128 bytes).
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes);
+
+// Kernel launchers: return GBATTN_OK or GBATTN_ERR_CUDA.
+int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale,
+                    const HostMask& m, void* o, float* lse, cudaStream_t st);
+int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, float scale,
+                    const HostMask& m, float* o, float* lse, cudaStream_t st);
+int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o,
+                    const void* dout, const float* lse, float scale, const HostMask& m, int deterministic,
+                    void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
+int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
+                    const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
+                    float* dv, void* ws, cudaStream_t st);
+int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st);
+int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbattn_blocks* out,
+                     cudaStream_t st);
+
+// Device error words, one per translation unit (read and cleared).
+int fwd_take_error();
+int bwd_take_error();
+int simt_take_error();
+int decode_take_error();
+int blockmask_take_error();
+
+// Workspace layout of attn_bwd: [dq_accum fp32 BHxSqxDqk][delta fp32 BHxSq][pad]
+size_t bwd_workspace_bytes(const Shape& s);
+size_t align_up(size_t x, size_t a);
+
+}  // namespace gb

@@ -1,0 +1,183 @@
+// mask.cuh - element masks as per-row (or per-key) index intervals, the
+// classification of a 128 x 128 kernel tile, and the walk over block-sparse
+// lists shared by every attention kernel.
+//
+// Mask kinds follow "Enable 2CTA for SM100 block-sparse backward" (fuzz
+// tester mask names: causal, sliding_window, block_diagonal, prefix_lm) and
+// the dynamic (bias-ranked) mask of "Optimize Flash Dynamic Mask Attention
+// Kernel Configurations". With the diagonal aligned bottom-right
+// (a = i + Sk - Sq), every closed-form kind allows, for query i, one interval
+// of keys [lo_i, hi_i]; lo_i and hi_i never decrease with i. The dynamic kind
+// is the causal interval intersected with a per-(b,h) keep bitmask.
+#pragma once
+
+#include "common.cuh"
+
+namespace gb {
+
+struct MaskParams {
+  int kind;
+  int window_left;
+  int block_size;
+  int prefix_len;
+  float slope;             // rel-bias slope (score += slope * (i - j))
+  const float* key_bias;   // [B*H, Sk] or nullptr
+  const uint32_t* keep;    // [B*H, nkw] (dynamic) or nullptr
+  int nkw;                 // words per (b,h) in keep
+};
+
+// Allowed keys of query i: [lo, hi] (inclusive, clipped to [0, Sk-1]);
+// empty when lo > hi.
+__device__ __forceinline__ void row_interval(const MaskParams& m, int i, int Sq, int Sk, int& lo, int& hi) {
+  const int a = i + (Sk - Sq);
+  lo = 0;
+  hi = Sk - 1;
+  switch (m.kind) {
+    case GBATTN_MASK_CAUSAL:
+    case GBATTN_MASK_DYNAMIC_TOPK:
+      hi = min(a, Sk - 1);
+      break;
+    case GBATTN_MASK_SLIDING:
+      hi = min(a, Sk - 1);
+      if (m.window_left >= 0) lo = max(0, a - m.window_left);
+      break;
+    case GBATTN_MASK_BLOCK_DIAG: {
+      const int blk = floor_div(a, m.block_size) * m.block_size;
+      lo = max(0, blk);
+      hi = min(Sk - 1, blk + m.block_size - 1);
+      break;
+    }
+    case GBATTN_MASK_PREFIX_LM:
+      hi = min(max(m.prefix_len - 1, a), Sk - 1);
+      break;
+    default:
+      break;
+  }
+}
+
+// Queries that may see key j: [lo, hi] (inclusive, clipped to [0, Sq-1]);
+// the transpose of row_interval (ignores the dynamic keep bit, which the
+// caller tests separately).
+__device__ __forceinline__ void col_interval(const MaskParams& m, int j, int Sq, int Sk, int& lo, int& hi) {
+  const int d = Sk - Sq;  // a = i + d
+  lo = 0;
+  hi = Sq - 1;
+  switch (m.kind) {
+    case GBATTN_MASK_CAUSAL:
+    case GBATTN_MASK_DYNAMIC_TOPK:
+      lo = max(0, j - d);
+      break;
+    case GBATTN_MASK_SLIDING:
+      lo = max(0, j - d);
+      if (m.window_left >= 0) hi = min(Sq - 1, j - d + m.window_left);
+      break;
+    case GBATTN_MASK_BLOCK_DIAG: {
+      const int blk = floor_div(j, m.block_size) * m.block_size;
+      lo = max(0, blk - d);
+      hi = min(Sq - 1, blk + m.block_size - 1 - d);
+      break;
+    }
+    case GBATTN_MASK_PREFIX_LM:
+      if (j >= m.prefix_len) lo = max(0, j - d);
+      break;
+    default:
+      break;
+  }
+}
+
+enum { TILE_EMPTY = 0, TILE_PARTIAL = 1, TILE_FULL = 2 };
+
+// Class of the tile rows [q0, q0+128) x keys [k0, k0+128), rows clipped to
+// Sq and keys to Sk. EMPTY is exact when returned (no allowed pair); FULL
+// is exact when returned (every pair allowed, nothing clipped, and - when
+// rows_whole - no padding row); otherwise PARTIAL (element masks applied).
+__device__ __forceinline__ int tile_class(const MaskParams& m, int q0, int k0, int Sq, int Sk,
+                                          bool rows_whole) {
+  const int q1 = min(q0 + 128, Sq);
+  const int k1 = min(k0 + 128, Sk);
+  if (q1 <= q0 || k1 <= k0) return TILE_EMPTY;
+  int lo_f, hi_f, lo_l, hi_l;
+  row_interval(m, q0, Sq, Sk, lo_f, hi_f);
+  row_interval(m, q1 - 1, Sq, Sk, lo_l, hi_l);
+  if (hi_l < k0 || lo_f > k1 - 1) return TILE_EMPTY;
+  if (m.kind == GBATTN_MASK_DYNAMIC_TOPK) return TILE_PARTIAL;
+  const bool whole = (k1 - k0 == 128) && (!rows_whole || q1 - q0 == 128);
+  if (whole && lo_l <= k0 && hi_f >= k1 - 1) return TILE_FULL;
+  return TILE_PARTIAL;
+}
+
+// Walk over the 128-wide tiles a CTA streams. The CTA owns a fixed 128-range
+// of the other dimension; the lists (mask list first, then full list) name
+// sparse blocks of `span` = (sub * 128) positions along the streamed
+// dimension. Slot s = (list entry) * sub + (sub-tile). Every role of a CTA
+// walks the same slots and keeps the same ones, so they agree on the order.
+struct TileWalk {
+  const int32_t* mlist;  // mask-list entries of this CTA's block row
+  const int32_t* flist;  // full-list entries
+  int mcnt, fcnt;
+  int sub;               // sub-tiles per sparse block
+  int nblk;              // number of sparse blocks along the streamed dim
+  int limit;             // Sk (forward) or Sq (backward)
+  int nslots;
+};
+
+// Returns false for a slot that is skipped (beyond the sequence end, empty
+// sub-tile, or a corrupt list entry, which also raises GBATTN_ERR_BLOCKS).
+// On true, *start is the first streamed index and *masked says whether the
+// element mask must be applied.
+__device__ __forceinline__ bool walk_slot(const TileWalk& w, int s, const MaskParams& m, bool forward,
+                                          int fixed0, int Sq, int Sk, int* start, bool* masked) {
+  const int e = s / w.sub;
+  const int u = s - e * w.sub;
+  const bool from_mask = e < w.mcnt;
+  const int blk = from_mask ? __ldg(w.mlist + e) : __ldg(w.flist + (e - w.mcnt));
+  if (blk < 0 || blk >= w.nblk) {
+    if (u == 0) raise_dev_error(GBATTN_ERR_BLOCKS);
+    return false;
+  }
+  const int st = (blk * w.sub + u) * 128;
+  if (st >= w.limit) return false;
+  *start = st;
+  if (!from_mask) {
+    *masked = false;
+    return true;
+  }
+  const int cls = forward ? tile_class(m, fixed0, st, Sq, Sk, false) : tile_class(m, st, fixed0, Sq, Sk, true);
+  if (cls == TILE_EMPTY) return false;
+  *masked = (cls != TILE_FULL);
+  return true;
+}
+
+__device__ __forceinline__ TileWalk make_walk(const int32_t* mcnt, const int32_t* midx, const int32_t* fcnt,
+                                              const int32_t* fidx, int row, int nblk, int sub, int limit) {
+  TileWalk w;
+  int mc = __ldg(mcnt + row);
+  int fc = __ldg(fcnt + row);
+  if (mc < 0 || mc > nblk || fc < 0 || fc > nblk || mc + fc > nblk) {
+    raise_dev_error(GBATTN_ERR_BLOCKS);
+    mc = 0;
+    fc = 0;
+  }
+  w.mlist = midx + (size_t)row * nblk;
+  w.flist = fidx + (size_t)row * nblk;
+  w.mcnt = mc;
+  w.fcnt = fc;
+  w.sub = sub;
+  w.nblk = nblk;
+  w.limit = limit;
+  w.nslots = (mc + fc) * sub;
+  return w;
+}
+
+// Dense walk (no lists, mask kind NONE): every 128-tile of [0, limit).
+__device__ __forceinline__ bool dense_slot(int s, const MaskParams& m, bool forward, int fixed0, int Sq,
+                                           int Sk, int* start, bool* masked) {
+  const int st = s * 128;
+  const int cls = forward ? tile_class(m, fixed0, st, Sq, Sk, false) : tile_class(m, st, fixed0, Sq, Sk, true);
+  if (cls == TILE_EMPTY) return false;
+  *start = st;
+  *masked = (cls != TILE_FULL);
+  return true;
+}
+
+}  // namespace gb

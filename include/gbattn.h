@@ -1,0 +1,206 @@
+/*
+ * gbattn.h - C ABI of libgbattn.so: fused, block-sparse scaled-dot-product
+ * attention for one GB300 GPU (compute capability 10.3, sm_103a).
+ *
+ * What the operations compute is taken from these pages:
+ *   [FSA]  "Optimize Flash Dynamic Mask Attention Kernel Configurations"
+ *          (flash-sparse-attention PR #148): forward, split-KV forward,
+ *          backward with an optional deterministic path; masks and softcap.
+ *   [FA2C] "Enable 2CTA for SM100 block-sparse backward" (flash-attention
+ *          PR #2661): block-sparse forward/backward driven by per-block index
+ *          lists, sparse tiles that are multiples of the kernel tile (q and kv
+ *          sub-tiling), mask kinds, QK/V head dims 192/128, rel-bias score_mod.
+ *   [PCB]  POPCORNBENCH trace "Kimi-K2.6 l1_p97": scaled-dot-product
+ *          attention and the online-softmax merge of partial results.
+ *
+ * Conventions shared by every entry point
+ *   - Layout: Q [B,H,Sq,Dqk], K [B,H,Sk,Dqk], V [B,H,Sk,Dv], O/dO [B,H,Sq,Dv],
+ *     each contiguous with the head dim innermost; LSE [B,H,Sq] fp32.
+ *   - Every pointer is a DEVICE pointer of the current CUDA device, owned by
+ *     the caller. The library allocates nothing, frees nothing and keeps no
+ *     pointer after the call returns. Tensor pointers must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). Inputs must stay valid until the stream reaches the
+ *     end of the work.
+ *   - Return value: GBATTN_OK (0) or a negative GBATTN_ERR_* code. Argument
+ *     checks run on the host before any CUDA call; nothing is launched when a
+ *     check fails. No C++ exception crosses the ABI.
+ *   - Mask alignment for Sq != Sk is bottom-right: query i is aligned with key
+ *     i + (Sk - Sq).
+ *   - Rows with no allowed key produce O = 0, LSE = -inf and zero gradients.
+ *   - scale <= 0 selects 1/sqrt(Dqk), the pages' default softmax scale.
+ *   - Supported head dims: bf16 (Dqk,Dv) in {(32,32),(64,64),(128,128),
+ *     (192,128)} on the tensor-core path; fp32 any 1 <= Dqk,Dv <= 128 on the
+ *     exact CUDA-core path. Any Sq, Sk >= 1; ragged tile edges are masked.
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* gbattn_stream; /* a cudaStream_t */
+
+/* element types */
+enum { GBATTN_BF16 = 0, GBATTN_FP32 = 1 };
+
+/* mask kinds ([FA2C] fuzz tester mask names; [FSA] dynamic mask) */
+enum {
+  GBATTN_MASK_NONE = 0,
+  GBATTN_MASK_CAUSAL = 1,       /* key j allowed iff j <= i + (Sk - Sq)                      */
+  GBATTN_MASK_SLIDING = 2,      /* 0 <= (i + Sk - Sq) - j <= window_left (window_left < 0:   */
+                                /* unbounded, i.e. causal)                                    */
+  GBATTN_MASK_BLOCK_DIAG = 3,   /* floor((i + Sk - Sq) / block_size) == floor(j / block_size) */
+  GBATTN_MASK_PREFIX_LM = 4,    /* j < prefix_len, or causal                                  */
+  GBATTN_MASK_DYNAMIC_TOPK = 5  /* j among the topk keys of (b,h) ranked by key_bias          */
+                                /* (descending, ties: lower index first), and causal          */
+};
+
+/* status codes */
+enum {
+  GBATTN_OK = 0,
+  GBATTN_ERR_ARG = -1,         /* null pointer, non-positive or too large dimension     */
+  GBATTN_ERR_ALIGN = -2,       /* a tensor pointer is not 16-byte aligned               */
+  GBATTN_ERR_UNSUPPORTED = -3, /* dtype / head-dim combination, or device is not CC 10.3 */
+  GBATTN_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the query function says */
+  GBATTN_ERR_BLOCKS = -5,      /* block lists missing, or inconsistent with the shape    */
+  GBATTN_ERR_CUDA = -6,        /* a CUDA runtime call or a kernel launch failed          */
+  GBATTN_ERR_TIMEOUT = -7      /* a kernel gave up a bounded wait (see last_device_error) */
+};
+
+/*
+ * Element-level mask and score modifiers, shared by every call.
+ * Score of pair (i,j): s = scale * q_i.k_j; if softcap > 0, s = softcap *
+ * tanh(s / softcap); then s += rel_bias_slope * (i - j) + key_bias[b,h,j].
+ * The biases are constants (no gradient flows to them): the rel-bias
+ * score_mod backward of [FA2C] returns the incoming gradient unchanged.
+ */
+typedef struct {
+  int kind;             /* GBATTN_MASK_*                                        */
+  int window_left;      /* SLIDING                                               */
+  int block_size;       /* BLOCK_DIAG, > 0                                       */
+  int prefix_len;       /* PREFIX_LM, >= 0                                       */
+  int topk;             /* DYNAMIC_TOPK, >= 0                                    */
+  float rel_bias_slope; /* 0 = off                                               */
+  float softcap;        /* 0 = off                                               */
+  const float* key_bias;/* device [B,H,Sk] fp32 additive key bias, or NULL; required */
+                        /* for DYNAMIC_TOPK (it is also the ranking key)          */
+} gbattn_mask;
+
+/*
+ * Block-sparse lists ([FA2C]: forward lists per q-block of kv-blocks, backward
+ * lists per kv-block of q-blocks, split into blocks that need the element mask
+ * ("mask" lists) and blocks whose every pair is allowed ("full" lists); blocks
+ * with no allowed pair are absent and never loaded). Sparse blocks are
+ * sparse_m x sparse_n with both multiples of the 128 x 128 kernel tile; the
+ * kernels walk each listed block as (sparse_m/128) x (sparse_n/128) tiles.
+ * nQB = ceil(Sq/sparse_m), nKB = ceil(Sk/sparse_n). Lists ascend; unused tail
+ * entries are 0; a block cut by the end of the sequence is never "full".
+ * All arrays are caller-owned device memory (sizes: gbattn_block_mask_sizes).
+ */
+typedef struct {
+  int sparse_m, sparse_n;
+  int32_t* q_mask_cnt;  /* [B,H,nQB]     */
+  int32_t* q_mask_idx;  /* [B,H,nQB,nKB] */
+  int32_t* q_full_cnt;  /* [B,H,nQB]     */
+  int32_t* q_full_idx;  /* [B,H,nQB,nKB] */
+  int32_t* k_mask_cnt;  /* [B,H,nKB]     */
+  int32_t* k_mask_idx;  /* [B,H,nKB,nQB] */
+  int32_t* k_full_cnt;  /* [B,H,nKB]     */
+  int32_t* k_full_idx;  /* [B,H,nKB,nQB] */
+  uint32_t* keep_bits;  /* [B,H,ceil(Sk/32)]: DYNAMIC_TOPK keep set, bit j%32 of word
+                           j/32; written by build_block_mask, read by the kernels.
+                           NULL allowed for the other kinds.                      */
+} gbattn_blocks;
+
+/* Byte sizes of the block-list arrays for this shape (any of the out pointers
+ * may be NULL). Returns GBATTN_ERR_ARG for bad dims or tiles. */
+int gbattn_block_mask_sizes(int B, int H, int Sq, int Sk, int sparse_m, int sparse_n,
+                            size_t* q_cnt_bytes, size_t* q_idx_bytes,
+                            size_t* k_cnt_bytes, size_t* k_idx_bytes,
+                            size_t* keep_bits_bytes);
+
+/*
+ * build_block_mask - classify every sparse block as absent / mask / full and
+ * write the forward and backward lists into `out` ([FA2C]
+ * `_build_block_sparse_masks_for_bwd`, restated for C). For DYNAMIC_TOPK it
+ * first selects the keep set per (b,h) on the GPU and writes out->keep_bits.
+ * The result is exact (integer work; the top-k compares fp32 biases).
+ */
+int build_block_mask(int B, int H, int Sq, int Sk, const gbattn_mask* mask,
+                     gbattn_blocks* out, gbattn_stream stream);
+
+/*
+ * attn_fwd - O = softmax(mask(scores)) V and LSE = ln sum_j exp(s_ij), fused:
+ * per 128-row query tile the kernel streams the 128-key tiles of the listed
+ * blocks, keeps a running max/sum (online softmax, [PCB]) and never writes the
+ * score matrix to memory ([FSA] forward; [FA2C] `_flash_attn_fwd` with
+ * block_sparse_tensors and return_lse). `blocks` may be NULL only for
+ * GBATTN_MASK_NONE. o has the dtype of q; lse may be NULL.
+ */
+int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+             const void* q, const void* k, const void* v, float scale,
+             const gbattn_mask* mask, const gbattn_blocks* blocks,
+             void* o, float* lse, gbattn_stream stream);
+
+/* Workspace bytes attn_bwd needs for this shape (fp32 dQ accumulator and two
+ * per-row fp32 vectors). Returns 0 for invalid dims. */
+size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv);
+
+/*
+ * attn_bwd - gradients of O for the loss <dO, O> ([FSA] backward, "seq-k
+ * parallel" path with an optional deterministic mode; [FA2C] `_flash_attn_bwd`
+ * with the backward block lists). Steps: D_i = sum_d dO_id O_id; per kv tile,
+ * recompute P from LSE, dV += P^T dO, dP = dO V^T, dS = P (dP - D),
+ * dK += scale dS^T Q, dQ += scale dS K. deterministic = 0 accumulates dQ
+ * with fp32 atomics across kv tiles; deterministic = 1 computes dQ in a
+ * separate query-parallel pass so that dQ is bitwise reproducible. o and lse
+ * must be the outputs of attn_fwd for the same inputs. workspace is device
+ * memory of at least attn_bwd_workspace_bytes(); its contents on entry do not
+ * matter.
+ */
+int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+             const void* q, const void* k, const void* v, const void* o,
+             const void* dout, const float* lse, float scale,
+             const gbattn_mask* mask, const gbattn_blocks* blocks, int deterministic,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+             gbattn_stream stream);
+
+/* Workspace bytes attn_fwd_splitkv needs: num_splits partial outputs
+ * [n,B,H,Sq,Dv] fp32 and partial LSEs [n,B,H,Sq] fp32 (0 when num_splits == 1). */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Dv, int num_splits);
+
+/*
+ * attn_fwd_splitkv - decode-shaped forward ([FSA] split-KV forward, splits
+ * 1/2/4/8/16 tested). The keys are cut into num_splits ranges of
+ * L = ceil(Sk/num_splits) rounded up to 128 keys; each (b,h,split) streams
+ * its K/V range once with 16-byte vector loads and writes a partial output and
+ * LSE; a combine kernel merges them with the LSE-weighted rule of [PCB]
+ * (num_splits == 1 writes O directly). bf16 only; mask kind NONE or CAUSAL,
+ * no softcap or biases. 1 <= num_splits <= 64.
+ */
+int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+                     const void* q, const void* k, const void* v, float scale,
+                     const gbattn_mask* mask, int num_splits, void* o, float* lse,
+                     void* workspace, size_t workspace_bytes, gbattn_stream stream);
+
+/* Synchronises `stream`, then returns and clears the device-side error word
+ * of the current device: GBATTN_OK, GBATTN_ERR_TIMEOUT (a bounded wait inside
+ * a kernel ran out; the kernel returned early and its outputs are invalid) or
+ * GBATTN_ERR_BLOCKS (a kernel met an out-of-range list entry and skipped it). */
+int gbattn_last_device_error(gbattn_stream stream);
+
+/* Static, human-readable text for a status code. */
+const char* gbattn_strerror(int status);
+
+/* ABI version: 100 * major + minor. */
+int gbattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBATTN_H */

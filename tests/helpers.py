@@ -1,0 +1,112 @@
+"""Shared test helpers: run one case through the C ABI and through the oracle
+on the same seeded inputs, and compare with the stated tolerances.
+
+Tolerances (bf16): O elementwise |g - r| <= 2e-2 + 2e-2 |r|; LSE |g - r| <=
+2e-2 (-inf must match); dQ/dK/dV max|g - r| / max|r| <= 5e-2. fp32 path:
+atol = rtol = 1e-4 (the fp32 tolerance of the POPCORNBENCH "Kimi-K2.6
+l1_p97" SDPA task).
+"""
+import numpy as np
+import torch
+
+import block_sparse_attention_tma_gb300 as ga
+from block_sparse_attention_tma_gb300.synth import make_inputs
+from oracle import attention as orc
+
+KIND = {"none": orc.NONE, "causal": orc.CAUSAL, "sliding": orc.SLIDING, "sliding_window": orc.SLIDING,
+        "block_diag": orc.BLOCK_DIAG, "block_diagonal": orc.BLOCK_DIAG, "prefix_lm": orc.PREFIX_LM,
+        "dynamic": orc.DYNAMIC_TOPK}
+
+
+def spec_dicts(kind, Sq, Sk, window=None, block_size=256, prefix_len=64, topk=None, slope=0.0, softcap=0.0,
+               key_bias=None):
+    k = KIND[kind]
+    d = dict(kind=k, rel_bias_slope=slope, softcap=softcap)
+    if k == orc.SLIDING:
+        d["window_left"] = max(64, min(Sq, Sk) // 3) if window is None else window
+    if k == orc.BLOCK_DIAG:
+        d["block_size"] = block_size
+    if k == orc.PREFIX_LM:
+        d["prefix_len"] = prefix_len
+    if k == orc.DYNAMIC_TOPK:
+        d["topk"] = max(1, Sk // 4) if topk is None else topk
+    return d
+
+
+def to_gpu_spec(d, key_bias_gpu=None):
+    return ga.MaskSpec(kind=d["kind"], window_left=d.get("window_left", -1), block_size=d.get("block_size", 0),
+                       prefix_len=d.get("prefix_len", 0), topk=d.get("topk", 0),
+                       rel_bias_slope=d.get("rel_bias_slope", 0.0), softcap=d.get("softcap", 0.0),
+                       key_bias=key_bias_gpu)
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+class Case:
+    """Inputs on host and device, the GPU spec and lists, and the oracle spec."""
+
+    def __init__(self, B, H, Sq, Sk, Dqk, Dv, kind="none", dtype="bf16", seed=42, sparse=(256, 512),
+                 use_bias=False, lists=True, **kw):
+        need_bias = use_bias or KIND[kind] == orc.DYNAMIC_TOPK
+        self.shape = (B, H, Sq, Sk, Dqk, Dv)
+        self.x = make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype, seed=seed, bias=need_bias)
+        self.dev = {n: t.cuda() for n, t in self.x.items()}
+        self.d = spec_dicts(kind, Sq, Sk, **kw)
+        self.spec = to_gpu_spec(self.d, self.dev.get("key_bias"))
+        self.lists = None
+        if lists and (self.d["kind"] != orc.NONE or sparse is not None):
+            sm, sn = sparse
+            self.lists = ga.alloc_block_lists(B, H, Sq, Sk, sm, sn)
+            ga.build_block_mask(B, H, Sq, Sk, self.spec, self.lists)
+        od = dict(self.d)
+        if need_bias:
+            od["key_bias"] = self.x["key_bias"].double().numpy()
+        self.od = od
+        self.h = {n: f64(t) for n, t in self.x.items() if n != "key_bias"}
+
+    def fwd(self):
+        return ga.attn_fwd(self.dev["q"], self.dev["k"], self.dev["v"], 0.0, self.spec, self.lists)
+
+    def bwd(self, o, lse, deterministic=False):
+        return ga.attn_bwd(self.dev["q"], self.dev["k"], self.dev["v"], o, self.dev["do"], lse, 0.0, self.spec,
+                           self.lists, deterministic=deterministic)
+
+    def problem(self, b, h):
+        kb = self.od.get("key_bias")
+        return orc.Problem(self.h["q"][b, h], self.h["k"][b, h], self.h["v"][b, h], kind=self.od["kind"],
+                           window_left=self.od.get("window_left", -1), block_size=self.od.get("block_size", 0),
+                           prefix_len=self.od.get("prefix_len", 0), topk=self.od.get("topk", 0),
+                           rel_bias_slope=self.od.get("rel_bias_slope", 0.0), softcap=self.od.get("softcap", 0.0),
+                           key_bias=None if kb is None else kb[b, h])
+
+
+def check_out(og, o_ref, fp32=False):
+    if fp32:
+        assert np.allclose(og, o_ref, rtol=1e-4, atol=1e-4), np.max(np.abs(og - o_ref))
+    else:
+        bad = np.abs(og - o_ref) > 2e-2 + 2e-2 * np.abs(o_ref)
+        assert not bad.any(), f"O mismatch: {bad.sum()} elements, max abs {np.max(np.abs(og - o_ref)):.3e}"
+
+
+def check_lse(lg, l_ref, fp32=False):
+    inf_r = np.isinf(l_ref)
+    assert np.array_equal(np.isinf(lg) & (lg < 0), inf_r), "-inf rows differ"
+    if (~inf_r).any():
+        err = np.max(np.abs(lg[~inf_r] - l_ref[~inf_r]))
+        assert err <= (1e-4 if fp32 else 2e-2), f"LSE err {err:.3e}"
+
+
+def check_grad(g, r, name, fp32=False):
+    if fp32:
+        assert np.allclose(g, r, rtol=1e-4, atol=1e-4), f"{name}: {np.max(np.abs(g - r)):.3e}"
+        return 0.0
+    den = np.max(np.abs(r))
+    err = np.max(np.abs(g - r)) / den if den > 0 else np.max(np.abs(g))
+    assert err <= 5e-2, f"{name} rel-to-max err {err:.3e}"
+    return err
+
+
+def assert_no_device_error():
+    assert ga.load_library().gbattn_last_device_error(None) == 0

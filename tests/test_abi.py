@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/gbattn.h declares, and rejects bad arguments on the host (before any
+CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import block_sparse_attention_tma_gb300 as ga
+from block_sparse_attention_tma_gb300 import binding as bd
+
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_fwd_splitkv", "build_block_mask", "gbattn_strerror",
+              "gbattn_last_device_error", "gbattn_block_mask_sizes", "attn_bwd_workspace_bytes",
+              "attn_fwd_splitkv_workspace_bytes", "gbattn_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ga.load_library()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(bd.EXPORTS) >= set(declared_functions())
+    assert lib.gbattn_version() == 100
+
+
+def test_strerror_covers_codes():
+    lib = ga.load_library()
+    for c in range(0, -8, -1):
+        assert lib.gbattn_strerror(c) not in (None, b"unknown status")
+
+
+def test_block_mask_sizes():
+    lib = ga.load_library()
+    sz = [ctypes.c_size_t() for _ in range(5)]
+    rc = lib.gbattn_block_mask_sizes(1, 16, 16384, 16384, 256, 512, *[ctypes.byref(s) for s in sz])
+    assert rc == 0
+    assert [s.value for s in sz] == [16 * 64 * 4, 16 * 64 * 32 * 4, 16 * 32 * 4, 16 * 32 * 64 * 4, 16 * 512 * 4]
+    assert lib.gbattn_block_mask_sizes(1, 1, 100, 100, 100, 128, *[None] * 5) == bd.ERR_ARG
+    assert lib.gbattn_block_mask_sizes(0, 1, 100, 100, 128, 128, *[None] * 5) == bd.ERR_ARG
+
+
+def test_workspace_queries():
+    lib = ga.load_library()
+    # dq accumulator fp32 [2,8,2048,64] + 2 row vectors of [2,8,2048]
+    assert lib.attn_bwd_workspace_bytes(0, 2, 8, 2048, 2048, 64, 64) == 2 * 8 * 2048 * 64 * 4 + 2 * 2 * 8 * 2048 * 4
+    assert lib.attn_bwd_workspace_bytes(0, 0, 8, 2048, 2048, 64, 64) == 0
+    assert lib.attn_fwd_splitkv_workspace_bytes(32, 32, 1, 128, 1) == 0
+    assert lib.attn_fwd_splitkv_workspace_bytes(32, 32, 1, 128, 4) == 4 * 1024 * 128 * 4 + 4 * 1024 * 4
+    assert lib.attn_fwd_splitkv_workspace_bytes(32, 32, 1, 128, 65) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def _fwd(dtype=0, B=1, H=1, Sq=128, Sk=128, Dqk=64, Dv=64, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE,
+         mask=None, blocks=None):
+    lib = ga.load_library()
+    m = mask.c() if mask is not None else None
+    return lib.attn_fwd(dtype, B, H, Sq, Sk, Dqk, Dv, q, k, v, 0.0, ctypes.byref(m) if m else None,
+                        ctypes.byref(blocks) if blocks else None, o, lse, None)
+
+
+def test_fwd_argument_checks():
+    assert _fwd(B=0) == bd.ERR_ARG
+    assert _fwd(Sk=-1) == bd.ERR_ARG
+    assert _fwd(q=0) == bd.ERR_ARG
+    assert _fwd(q=FAKE + 8) == bd.ERR_ALIGN
+    assert _fwd(Dqk=96, Dv=96) == bd.ERR_UNSUPPORTED      # bf16 head dims
+    assert _fwd(Dqk=128, Dv=64) == bd.ERR_UNSUPPORTED
+    assert _fwd(dtype=7) == bd.ERR_UNSUPPORTED
+    assert _fwd(dtype=1, Dqk=200, Dv=8) == bd.ERR_UNSUPPORTED  # fp32 path: <= 128
+    assert _fwd(mask=bd.MaskSpec(kind=9)) == bd.ERR_ARG
+    assert _fwd(mask=bd.MaskSpec(kind=bd.BLOCK_DIAG, block_size=0)) == bd.ERR_ARG
+    assert _fwd(mask=bd.MaskSpec(kind=bd.CAUSAL, softcap=-1.0)) == bd.ERR_ARG
+    # a masked call needs block lists
+    assert _fwd(mask=bd.MaskSpec(kind=bd.CAUSAL)) == bd.ERR_BLOCKS
+    blk = bd._Blocks(256, 100)
+    assert _fwd(mask=bd.MaskSpec(kind=bd.CAUSAL), blocks=blk) == bd.ERR_BLOCKS
+    blk = bd._Blocks(256, 512)  # right tiles, but no list pointers
+    assert _fwd(mask=bd.MaskSpec(kind=bd.CAUSAL), blocks=blk) == bd.ERR_BLOCKS
+
+
+def test_valid_call_without_gpu_reports_unsupported_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd() == bd.ERR_UNSUPPORTED
+
+
+def test_bwd_and_splitkv_argument_checks():
+    lib = ga.load_library()
+    args = [0, 1, 1, 128, 128, 64, 64] + [FAKE] * 6 + [0.0, None, None]
+    assert lib.attn_bwd(*args, 2, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == bd.ERR_ARG   # deterministic flag
+    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, 1 << 30, None) == bd.ERR_WORKSPACE
+    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE, 16, None) == bd.ERR_WORKSPACE
+    sk = [0, 32, 32, 1, 65536, 128, 128, FAKE, FAKE, FAKE, 0.0, None]
+    assert lib.attn_fwd_splitkv(*sk, 0, FAKE, FAKE, None, 0, None) == bd.ERR_ARG          # 0 splits
+    assert lib.attn_fwd_splitkv(*sk, 4, FAKE, FAKE, None, 0, None) == bd.ERR_WORKSPACE
+    m = bd.MaskSpec(kind=bd.SLIDING, window_left=3).c()
+    sk2 = sk[:11] + [ctypes.byref(m)]
+    assert lib.attn_fwd_splitkv(*sk2, 1, FAKE, FAKE, None, 0, None) == bd.ERR_UNSUPPORTED
+    sk3 = list(sk)
+    sk3[0] = 1
+    assert lib.attn_fwd_splitkv(*sk3, 1, FAKE, FAKE, None, 0, None) == bd.ERR_UNSUPPORTED  # fp32 decode
+
+
+def test_build_block_mask_argument_checks():
+    lib = ga.load_library()
+    m = bd.MaskSpec(kind=bd.DYNAMIC_TOPK, topk=4).c()  # no key bias
+    b = bd._Blocks(128, 128, *[FAKE] * 9)
+    assert lib.build_block_mask(1, 1, 128, 128, ctypes.byref(m), ctypes.byref(b), None) == bd.ERR_ARG
+    m = bd.MaskSpec(kind=bd.CAUSAL).c()
+    b = bd._Blocks(128, 128, *[FAKE] * 8, None)
+    assert lib.build_block_mask(1, 1, 128, 128, ctypes.byref(m), None, None) == bd.ERR_ARG
+    b2 = bd._Blocks(64, 128, *[FAKE] * 9)
+    assert lib.build_block_mask(1, 1, 128, 128, ctypes.byref(m), ctypes.byref(b2), None) == bd.ERR_BLOCKS

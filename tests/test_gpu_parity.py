@@ -1,0 +1,204 @@
+"""GPU parity: every step of the hot path through the C ABI against the fp64
+oracle on the same seeded inputs (element by element at sizes the oracle
+finishes in seconds, spanning several 128-tiles and a ragged tail)."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_tma_gb300 as ga
+from conftest import read_golden
+from helpers import Case, check_grad, check_lse, check_out, f64, assert_no_device_error
+from oracle import attention as orc
+
+pytestmark = pytest.mark.gpu
+
+LIST_NAMES = ["q_mask_cnt", "q_mask_idx", "q_full_cnt", "q_full_idx",
+              "k_mask_cnt", "k_mask_idx", "k_full_cnt", "k_full_idx"]
+
+
+def lists_equal(c, B, H, Sq, Sk, sm, sn):
+    ref = orc.block_lists(B, H, Sq, Sk, c.od, sm, sn)
+    for n in LIST_NAMES:
+        g = c.lists.tensors[n].cpu().numpy().reshape(ref[n].shape)
+        assert np.array_equal(g, ref[n]), n
+    if c.od["kind"] == orc.DYNAMIC_TOPK:
+        bits = orc.keep_bits(c.od["key_bias"], c.od["topk"])
+        g = c.lists.tensors["keep_bits"].cpu().numpy().view(np.uint32).reshape(bits.shape)
+        assert np.array_equal(g, bits)
+
+
+# ------------------------------------------------------------------ a1 build_block_mask
+@pytest.mark.parametrize("kind", ["causal", "sliding", "block_diag", "prefix_lm", "dynamic", "none"])
+@pytest.mark.parametrize("Sq,Sk,sm,sn", [(1000, 1000, 256, 512), (383, 769, 256, 256), (1025, 511, 128, 128),
+                                         (640, 512, 256, 512), (129, 257, 128, 256)])
+def test_block_mask_bit_exact(kind, Sq, Sk, sm, sn):
+    c = Case(1, 2, Sq, Sk, 64, 64, kind, sparse=(sm, sn), prefix_len=100, block_size=192)
+    torch.cuda.synchronize()
+    lists_equal(c, 1, 2, Sq, Sk, sm, sn)
+    assert_no_device_error()
+
+
+def test_topk_ties_and_signed_zeros():
+    B, H, Sk = 1, 3, 700
+    c = Case(B, H, 64, Sk, 64, 64, "dynamic", topk=100)
+    kb = torch.randn(B, H, Sk, generator=torch.Generator().manual_seed(5))
+    kb = torch.round(kb * 2) / 2  # many ties
+    kb[0, 1, :50] = 0.0
+    kb[0, 1, 50:100] = -0.0
+    kb[0, 2] = 1.0  # all equal: lowest indices win
+    c.dev["key_bias"].copy_(kb)
+    c.od["key_bias"] = kb.double().numpy()
+    ga.build_block_mask(B, H, 64, Sk, c.spec, c.lists)
+    torch.cuda.synchronize()
+    lists_equal(c, B, H, 64, Sk, 256, 512)
+
+
+# ------------------------------------------------------------------ a2 forward (bf16, tensor cores)
+FWD_CASES = [
+    # B, H, Sq, Sk, Dqk, Dv, kind, extras
+    (1, 2, 300, 300, 64, 64, "none", {}),
+    (1, 2, 1000, 1000, 64, 64, "causal", {}),
+    (2, 1, 640, 700, 128, 128, "causal", dict(slope=0.01)),
+    (1, 2, 513, 769, 192, 128, "sliding", dict(slope=0.01)),
+    (1, 1, 1024, 1024, 192, 128, "block_diag", dict(block_size=256)),
+    (1, 2, 700, 700, 32, 32, "prefix_lm", dict(prefix_len=300)),
+    (1, 2, 900, 900, 64, 64, "dynamic", dict(topk=200)),
+    (1, 1, 256, 384, 128, 128, "causal", dict(softcap=2.0, use_bias=True)),
+    (1, 1, 1025, 511, 128, 128, "sliding", {}),
+]
+
+
+@pytest.mark.parametrize("case", FWD_CASES, ids=lambda c: f"{c[6]}-{c[2]}x{c[3]}-d{c[4]}")
+def test_forward_bf16(case):
+    B, H, Sq, Sk, Dqk, Dv, kind, ex = case
+    c = Case(B, H, Sq, Sk, Dqk, Dv, kind, **ex)
+    o, lse = c.fwd()
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for b in range(B):
+        for h in range(H):
+            o_ref, l_ref = c.problem(b, h).forward()
+            check_out(f64(o[b, h]), o_ref)
+            check_lse(f64(lse[b, h]), l_ref)
+
+
+@pytest.mark.parametrize("row", read_golden("fa_pr2661_fuzz_cases.txt"), ids=lambda r: r[0])
+def test_forward_fuzz_shapes(row):
+    seed, sq, sk, dqk, dv, stm, stn, name = row
+    if name == "mini_causal":
+        pytest.skip("mini_causal is out of scope")
+    c = Case(1, 1, int(sq), int(sk), int(dqk), int(dv), name, seed=int(seed), sparse=(int(stm), int(stn)),
+             slope=0.01, block_size=256)
+    o, lse = c.fwd()
+    torch.cuda.synchronize()
+    o_ref, l_ref = c.problem(0, 0).forward()
+    check_out(f64(o[0, 0]), o_ref)
+    check_lse(f64(lse[0, 0]), l_ref)
+    assert_no_device_error()
+
+
+# ------------------------------------------------------------------ a3-a5 backward (bf16)
+BWD_CASES = [
+    (1, 2, 400, 400, 64, 64, "causal", {}),
+    (1, 1, 513, 769, 192, 128, "sliding", dict(slope=0.01)),
+    (1, 2, 384, 384, 128, 128, "none", {}),
+    (1, 1, 600, 600, 32, 32, "prefix_lm", dict(prefix_len=200)),
+    (1, 1, 700, 700, 64, 64, "dynamic", dict(topk=150)),
+    (1, 1, 512, 512, 192, 128, "block_diag", dict(block_size=256)),
+    (1, 1, 300, 260, 128, 128, "causal", dict(softcap=2.0, use_bias=True)),
+]
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"{c[6]}-{c[2]}x{c[3]}-d{c[4]}")
+def test_backward_bf16(case, deterministic):
+    B, H, Sq, Sk, Dqk, Dv, kind, ex = case
+    c = Case(B, H, Sq, Sk, Dqk, Dv, kind, **ex)
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse, deterministic)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for b in range(B):
+        for h in range(H):
+            dq_r, dk_r, dv_r, _ = c.problem(b, h).backward(c.h["do"][b, h])
+            check_grad(f64(dq[b, h]), dq_r, "dQ")
+            check_grad(f64(dk[b, h]), dk_r, "dK")
+            check_grad(f64(dv[b, h]), dv_r, "dV")
+
+
+def test_deterministic_dq_is_bitwise_reproducible():
+    c = Case(1, 2, 640, 640, 128, 128, "causal")
+    o, lse = c.fwd()
+    a = c.bwd(o, lse, True)
+    b = c.bwd(o, lse, True)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+# ------------------------------------------------------------------ fp32 path
+@pytest.mark.parametrize("case", [(1, 1, 128, 128, 64, 64, "causal", {}),
+                                  (1, 2, 200, 333, 48, 24, "sliding", dict(window=50, slope=0.02)),
+                                  (1, 1, 150, 150, 64, 64, "dynamic", dict(topk=40)),
+                                  (1, 1, 130, 100, 16, 16, "block_diag", dict(block_size=64, softcap=1.5))],
+                         ids=lambda c: c[6])
+def test_fp32_forward_backward(case):
+    B, H, Sq, Sk, Dqk, Dv, kind, ex = case
+    c = Case(B, H, Sq, Sk, Dqk, Dv, kind, dtype="fp32", sparse=(128, 128), **ex)
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for h in range(H):
+        p = c.problem(0, h)
+        o_ref, l_ref = p.forward()
+        check_out(f64(o[0, h]), o_ref, fp32=True)
+        check_lse(f64(lse[0, h]), l_ref, fp32=True)
+        dq_r, dk_r, dv_r, _ = p.backward(c.h["do"][0, h])
+        check_grad(f64(dq[0, h]), dq_r, "dQ", fp32=True)
+        check_grad(f64(dk[0, h]), dk_r, "dK", fp32=True)
+        check_grad(f64(dv[0, h]), dv_r, "dV", fp32=True)
+
+
+# ------------------------------------------------------------------ a6-a7 split-KV decode
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("D,Sq,Sk,kind", [(128, 1, 3000, "none"), (64, 3, 1100, "causal"), (128, 2, 77, "none")])
+def test_splitkv_decode(n, D, Sq, Sk, kind):
+    c = Case(2, 3, Sq, Sk, D, D, kind, lists=False, sparse=None)
+    o, lse = ga.attn_fwd_splitkv(c.dev["q"], c.dev["k"], c.dev["v"], 0.0, c.spec, n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for b in range(2):
+        for h in range(3):
+            o_ref, l_ref = c.problem(b, h).forward()
+            check_out(f64(o[b, h]), o_ref)
+            check_lse(f64(lse[b, h]), l_ref)
+
+
+# ------------------------------------------------------------------ edge cases
+def test_fully_masked_rows_and_empty_lists():
+    # block-diagonal with Sq > Sk: the first Sq - Sk rows see no key at all
+    c = Case(1, 1, 400, 150, 64, 64, "block_diag", block_size=64, sparse=(128, 128))
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse)
+    torch.cuda.synchronize()
+    p = c.problem(0, 0)
+    o_ref, l_ref = p.forward()
+    check_out(f64(o[0, 0]), o_ref)
+    check_lse(f64(lse[0, 0]), l_ref)
+    assert np.all(f64(o[0, 0])[:250] == 0.0)
+    dq_r, dk_r, dv_r, _ = p.backward(c.h["do"][0, 0])
+    assert np.all(f64(dq[0, 0])[:250] == 0.0)
+    check_grad(f64(dk[0, 0]), dk_r, "dK")
+    check_grad(f64(dv[0, 0]), dv_r, "dV")
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 1), (1, 300), (300, 1), (129, 1)])
+def test_tiny_and_single_key_shapes(Sq, Sk):
+    c = Case(1, 2, Sq, Sk, 64, 64, "none", lists=False, sparse=None)
+    o, lse = c.fwd()
+    torch.cuda.synchronize()
+    for h in range(2):
+        o_ref, l_ref = c.problem(0, h).forward()
+        check_out(f64(o[0, h]), o_ref)
+        check_lse(f64(lse[0, h]), l_ref)

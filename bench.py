@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention hot path on one GB300 (or N, one process each).
+
+One step = every row of the path on its workload:
+  * 16K block-sparse causal MLA prefill: B=1, H=16, Sq=Sk=16384, Dqk=192,
+    Dv=128, bf16, 256 x 512 sparse tiles, rel bias 0.01 (q - kv):
+    build_block_mask -> attn_fwd -> attn_bwd (preprocess, dK/dV with atomic
+    dQ, dQ convert).
+  * split-KV decode: B=32, H=32, Sq=1, Sk=65536, D=128, bf16, once per split
+    count in {1, 2, 4, 8, 16} (partial + combine).
+`value` is the prefill forward+backward throughput in TFLOP/s counting only
+unmasked FLOPs (fwd 2N(Dqk+Dv), bwd 2N(3Dqk+2Dv)); decode is reported as
+HBM GB/s of K+V bytes. Inputs are resident in HBM (0.34 GB prefill + 34.4 GB
+decode per step, all larger than the 129 MB L2, so no flush is needed).
+
+--impl reference times the fp64 CPU oracle (the only reference this path
+has) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd/bwd TFLOP/s (unmasked FLOPs) & % BF16 peak; decode HBM GB/s"
+PREFILL = dict(B=1, H=16, S=16384, Dqk=192, Dv=128, sparse_m=256, sparse_n=512, slope=0.01)
+DECODE = dict(B=32, H=32, Sq=1, Sk=65536, D=128, splits=(1, 2, 4, 8, 16))
+
+
+def causal_pairs(S):
+    return S * (S + 1) // 2
+
+
+def prefill_flops():
+    P = PREFILL
+    n = P["B"] * P["H"] * causal_pairs(P["S"])
+    return 2 * n * (P["Dqk"] + P["Dv"]), 2 * n * (3 * P["Dqk"] + 2 * P["Dv"]), n
+
+
+def decode_bytes():
+    D = DECODE
+    return D["B"] * D["H"] * D["Sk"] * D["D"] * 2 * 2  # K and V, bf16
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def file_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of each kernel from the committed ncu summary, kept
+    only while the kernel source still hashes to what was profiled."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        tr = json.load(f)
+    out = {}
+    for name, rec in tr.items():
+        try:
+            if file_hash(*rec["sources"]) == rec["source_hash"]:
+                out[name] = rec["bytes_per_launch"]
+        except (OSError, KeyError):
+            pass
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        load = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import block_sparse_attention_tma_gb300 as ga
+    from block_sparse_attention_tma_gb300.synth import make_inputs, make_device_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = ga.load_library()
+    P, D = PREFILL, DECODE
+    B, H, S, Dqk, Dv = P["B"], P["H"], P["S"], P["Dqk"], P["Dv"]
+    x = make_inputs(B, H, S, S, Dqk, Dv, "bf16", seed=42 + rank)
+    g = {n: t.to(dev) for n, t in x.items()}
+    spec = ga.MaskSpec(kind=ga.CAUSAL, rel_bias_slope=P["slope"])
+    lists = ga.alloc_block_lists(B, H, S, S, P["sparse_m"], P["sparse_n"], device=dev)
+    o = torch.empty(B, H, S, Dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    ws = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, H, S, S, Dqk, Dv), dtype=torch.uint8,
+                     device=dev)
+    D = dict(DECODE, Sk=args.decode_sk)
+    dx = make_device_inputs(D["B"], D["H"], D["Sq"], D["Sk"] if args.only != "prefill" else 128, D["D"], D["D"],
+                            "bf16", seed=42 + rank, device=dev, dout=False)
+    do_ = torch.empty(D["B"], D["H"], D["Sq"], D["D"], dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty(D["B"], D["H"], D["Sq"], dtype=torch.float32, device=dev)
+    dws = torch.empty(max(ga.attn_fwd_splitkv_workspace_bytes(D["B"], D["H"], D["Sq"], D["D"], n)
+                          for n in D["splits"]), dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    do_prefill = args.only in ("all", "prefill")
+    do_decode = args.only in ("all", "decode")
+    names = (["mask", "fwd", "bwd"] if do_prefill else []) + ([f"dec{n}" for n in D["splits"]] if do_decode else [])
+    ev = {n: [] for n in names}
+    ev_marks = []
+
+    def step(record):
+        marks = []
+        if record:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(st)
+            marks.append(e)
+
+        def mark():
+            if record:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(st)
+                marks.append(e)
+
+        if do_prefill:
+            ga.build_block_mask(B, H, S, S, spec, lists)
+            mark()
+            ga.attn_fwd(g["q"], g["k"], g["v"], 0.0, spec, lists, o=o, lse=lse)
+            mark()
+            ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists, dq=dq, dk=dk, dv=dv,
+                        workspace=ws)
+            mark()
+        if do_decode:
+            for n in D["splits"]:
+                ga.attn_fwd_splitkv(dx["q"], dx["k"], dx["v"], 0.0, None, n, o=do_, lse=dlse, workspace=dws)
+                mark()
+        if record:
+            ev_marks.append(marks)
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    rc = lib.gbattn_last_device_error(None)
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} during warm-up")
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(vis.split(",")[local_rank] if vis else str(local_rank))
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(st)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+    rc = lib.gbattn_last_device_error(None)
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} in the timed region")
+    for marks in ev_marks:
+        for i, n in enumerate(names):
+            ev[n].append(marks[i].elapsed_time(marks[i + 1]))
+    per = {n: statistics.mean(v) for n, v in ev.items()}
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e and args.only == "all":
+        e2e = run_e2e(args, ga, torch, dev, x, dx, spec, lists, st)
+    if args.only != "all":
+        print(json.dumps({"only": args.only, "ms": {n: round(statistics.mean(v), 4) for n, v in ev.items()},
+                          "total_ms": round(total_ms, 3)}), flush=True)
+        return None
+
+    fwd_f, bwd_f, npairs = prefill_flops()
+    peaks = load_peaks()
+    ms_step = total_ms / args.steps
+    prefill_ms = per["mask"] + per["fwd"] + per["bwd"]
+    value = world * (fwd_f + bwd_f) / (prefill_ms * 1e-3) / 1e12
+    dec = {f"n={n}": round(decode_bytes() / (per[f"dec{n}"] * 1e-3) / 1e9, 1) for n in D["splits"]}
+    traffic = load_traffic()
+    tpeak = peaks["bf16_tflops_sustained"]
+    kern = {
+        "attn_fwd": {"bound": "tensor", "achieved": fwd_f / (per["fwd"] * 1e-3) / 1e12, "peak": tpeak,
+                     "unit": "TFLOP/s", "ms": per["fwd"], "traffic": traffic.get("attn_fwd")},
+        "attn_bwd": {"bound": "tensor", "achieved": bwd_f / (per["bwd"] * 1e-3) / 1e12, "peak": tpeak,
+                     "unit": "TFLOP/s", "ms": per["bwd"], "traffic": traffic.get("attn_bwd")},
+    }
+    best_n = min(D["splits"], key=lambda n: per[f"dec{n}"])
+    kern["attn_fwd_splitkv"] = {"bound": "hbm", "achieved": decode_bytes() / (per[f"dec{best_n}"] * 1e-3) / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s", "ms": per[f"dec{best_n}"],
+                                "splits": best_n, "traffic": traffic.get("attn_fwd_splitkv")}
+    for k in kern.values():
+        k["frac"] = round(k["achieved"] / k["peak"], 4)
+        k["achieved"] = round(k["achieved"], 2)
+        k["ms"] = round(k["ms"], 4)
+    # dominant kernel = largest share of the step's time (decode runs once per split count)
+    share = {"attn_fwd": per["fwd"], "attn_bwd": per["bwd"],
+             "attn_fwd_splitkv": sum(per[f"dec{n}"] for n in D["splits"])}
+    dom = max(share, key=share.get)
+    roof = dict(kern[dom])
+    roof["kernel"] = dom
+    roof["share_of_step"] = round(share[dom] / sum(per.values()), 4)
+    roof["peak_source"] = f"{peaks['source']} ({'sustained bf16' if roof['unit'] == 'TFLOP/s' else 'hbm copy'})"
+    launches_per_step = 2 + 1 + 3 + sum(1 if n == 1 else 2 for n in D["splits"])
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "16K block-sparse causal MLA prefill fwd+bwd + 64K split-KV decode",
+                   "prefill": "B=1 H=16 Sq=Sk=16384 Dqk=192 Dv=128 bf16 causal, sparse tiles 256x512, "
+                              "kernel tiles 128x128, rel bias 0.01(q-kv)",
+                   "decode": "B=32 H=32 Sq=1 Sk=65536 D=128 bf16, splits 1,2,4,8,16",
+                   "parallelism": f"replicas x{world} (independent heads per rank, no collective)",
+                   "l2": "inputs larger than L2 (0.34 GB prefill + 34.4 GB decode per step); no flush"},
+        "fwd_tflops": round(fwd_f / (per["fwd"] * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(bwd_f / (per["bwd"] * 1e-3) / 1e12, 2),
+        "fwd_frac_of_peak": round(fwd_f / (per["fwd"] * 1e-3) / 1e12 / tpeak, 4),
+        "bwd_frac_of_peak": round(bwd_f / (per["bwd"] * 1e-3) / 1e12 / tpeak, 4),
+        "decode_gbs": dec, "decode_frac_of_hbm": round(max(dec.values()) / peaks["hbm_gbs"], 4),
+        "ms": {n: round(v, 4) for n, v in per.items()},
+        "roofline": roof, "rooflines": kern,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(quick=args.quick_cpu)
+    return out
+
+
+def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
+    """Same step through the C ABI with host buffers: pinned host inputs are
+    copied in and the step's results copied out inside the timed region."""
+    P, D = PREFILL, DECODE
+    B, H, S, Dqk, Dv = P["B"], P["H"], P["S"], P["Dqk"], P["Dv"]
+    h_in = {n: t.pin_memory() for n, t in x.items()}
+    d_in = {n: torch.empty_like(t, device=dev) for n, t in x.items()}
+    outs = {"o": (B, H, S, Dv), "dq": (B, H, S, Dqk), "dk": (B, H, S, Dqk), "dv": (B, H, S, Dv)}
+    h_out = {n: torch.empty(s, dtype=torch.bfloat16).pin_memory() for n, s in outs.items()}
+    h_lse = torch.empty(B, H, S, dtype=torch.float32).pin_memory()
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    o = torch.empty(B, H, S, Dv, dtype=torch.bfloat16, device=dev)
+    dq, dk, dv = (torch.empty(s, dtype=torch.bfloat16, device=dev) for s in (outs["dq"], outs["dk"], outs["dv"]))
+    ws = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, H, S, S, Dqk, Dv), dtype=torch.uint8, device=dev)
+    # decode: host copies of the KV cache (34 GB pinned) are what a host caller holds
+    dh = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in dx.items()}
+    for n, t in dx.items():
+        dh[n].copy_(t)
+    dd = {n: torch.empty_like(t) for n, t in dx.items()}
+    d_o = torch.empty(D["B"], D["H"], D["Sq"], D["D"], dtype=torch.bfloat16, device=dev)
+    d_lse = torch.empty(D["B"], D["H"], D["Sq"], dtype=torch.float32, device=dev)
+    h_do = torch.empty(d_o.shape, dtype=torch.bfloat16).pin_memory()
+    nmax = max(D["splits"])
+    dws = torch.empty(ga.attn_fwd_splitkv_workspace_bytes(D["B"], D["H"], D["Sq"], D["D"], nmax), dtype=torch.uint8,
+                      device=dev)
+
+    def prefill():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        ga.build_block_mask(B, H, S, S, spec, lists)
+        ga.attn_fwd(d_in["q"], d_in["k"], d_in["v"], 0.0, spec, lists, o=o, lse=lse)
+        ga.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse, 0.0, spec, lists, dq=dq, dk=dk, dv=dv,
+                    workspace=ws)
+        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            h_out[n].copy_(t, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    def decode():
+        for n in dh:
+            dd[n].copy_(dh[n], non_blocking=True)
+        ga.attn_fwd_splitkv(dd["q"], dd["k"], dd["v"], 0.0, None, nmax, o=d_o, lse=d_lse, workspace=dws)
+        h_do.copy_(d_o, non_blocking=True)
+
+    steps = max(2, min(args.steps, 5))
+    res = {}
+    for name, fn in (("prefill", prefill), ("decode", decode)):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            fn()
+        torch.cuda.synchronize()
+        res[name] = (time.perf_counter() - t0) / steps
+    fwd_f, bwd_f, _ = prefill_flops()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values()) + h_lse.numel() * 4
+    dh2d = sum(t.numel() * t.element_size() for t in dh.values())
+    return {"value": round((fwd_f + bwd_f) / res["prefill"] / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(res["prefill"] * 1e3, 3),
+            "decode": {"value": round(decode_bytes() / res["decode"] / 1e9, 1), "unit": "GB/s",
+                       "splits": nmax, "h2d_bytes_per_step": dh2d,
+                       "d2h_bytes_per_step": h_do.numel() * 2, "ms_per_step": round(res["decode"] * 1e3, 3)},
+            "steps": steps}
+
+
+def cpu_baseline(quick=False):
+    """The fp64 oracle on a bounded sample: one (b, h) head of the prefill
+    workload (forward + backward) and one head of the decode workload."""
+    import numpy as np
+    import torch
+
+    from block_sparse_attention_tma_gb300.synth import make_inputs
+    from oracle import attention as orc
+
+    P = PREFILL
+    S = 4096 if quick else P["S"]
+    x = make_inputs(1, 1, S, S, P["Dqk"], P["Dv"], "bf16", seed=42)
+    f = {n: t.float().double().numpy()[0, 0] for n, t in x.items()}
+    prob = orc.Problem(f["q"], f["k"], f["v"], kind=orc.CAUSAL, rel_bias_slope=P["slope"])
+    t0 = time.perf_counter()
+    prob.forward()
+    t1 = time.perf_counter()
+    prob.backward(f["do"])
+    t2 = time.perf_counter()
+    n = causal_pairs(S)
+    flops = 2 * n * (P["Dqk"] + P["Dv"]) + 2 * n * (3 * P["Dqk"] + 2 * P["Dv"])
+    D = DECODE
+    g = torch.Generator().manual_seed(42)
+    q = torch.randn(1, D["D"], generator=g).bfloat16().double().numpy()
+    k = torch.randn(D["Sk"], D["D"], generator=g).bfloat16().double().numpy()
+    v = torch.randn(D["Sk"], D["D"], generator=g).bfloat16().double().numpy()
+    t3 = time.perf_counter()
+    orc.Problem(q, k, v).forward()
+    t4 = time.perf_counter()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(flops / (t2 - t0) / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"prefill: one (b,h) head, Sq=Sk={S}, causal, rel bias, fwd+bwd in fp64 "
+                      f"({(t2 - t0):.1f} s); decode: one head, Sk={D['Sk']} ({(t4 - t3) * 1e3:.0f} ms)",
+            "fwd_s": round(t1 - t0, 2), "bwd_s": round(t2 - t1, 2),
+            "decode_gbs": round(D["Sk"] * D["D"] * 2 * 2 / (t4 - t3) / 1e9, 3)}
+
+
+def run_reference(args):
+    """The fp64 oracle, as it stands, on the host cores; each step is one
+    bounded sample of the prefill workload (one head, forward + backward)."""
+    import numpy as np  # noqa: F401
+
+    from block_sparse_attention_tma_gb300.synth import make_inputs
+    from oracle import attention as orc
+
+    P = PREFILL
+    S = args.ref_seq
+    x = make_inputs(1, 1, S, S, P["Dqk"], P["Dv"], "bf16", seed=42)
+    f = {n: t.float().double().numpy()[0, 0] for n, t in x.items()}
+    prob = orc.Problem(f["q"], f["k"], f["v"], kind=orc.CAUSAL, rel_bias_slope=P["slope"])
+    n = causal_pairs(S)
+    flops = 2 * n * (P["Dqk"] + P["Dv"]) + 2 * n * (3 * P["Dqk"] + 2 * P["Dv"])
+    for _ in range(args.warmup):
+        prob.forward()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        prob.forward()
+        prob.backward(f["do"])
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms * 1e-3) / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"one (b,h) head of the 16K causal MLA prefill at Sq=Sk={S}, fwd+bwd, fp64"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "16K block-sparse causal MLA prefill fwd+bwd (oracle sample)", "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
+    ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="time one part only (profiling runs); prints a short line, not the bench line")
+    ap.add_argument("--decode-sk", type=int, default=DECODE["Sk"], help="decode keys (profiling runs only)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.only == "all" and args.decode_sk != DECODE["Sk"]:
+        ap.error("--decode-sk is for profiling runs with --only")
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -66,6 +66,8 @@ _SIGS = [
                                                                                       ctypes.POINTER(_Mask),
                                                                                       ctypes.c_int]
      + [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
+    ("attn_fwd_splitkv_noalloc", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3
+     + [ctypes.c_float, ctypes.POINTER(_Mask), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("gbattn_last_device_error", ctypes.c_int, [ctypes.c_void_p]),
 ]
 
@@ -235,3 +237,25 @@ def attn_fwd_splitkv(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_sp
 
 def last_device_error(stream=None) -> int:
     return int(load_library().gbattn_last_device_error(_stream(stream)))
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_splits=1, o=None, lse=None,
+                             stream=None):
+    """attn_fwd_splitkv without a workspace argument, for callers that may not
+    allocate device memory: the split partials go to the library's own static
+    scratch array (limit GBATTN_NOALLOC_SCRATCH_BYTES, 16 MiB). Calls whose GPU
+    work overlaps race on that array. Pass preallocated o / lse to allocate
+    nothing here either."""
+    lib = load_library()
+    B, H, Sq, Dqk = q.shape
+    Sk, Dv = k.shape[2], v.shape[3]
+    if o is None:
+        o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    mask = mask or MaskSpec()
+    cm = mask.c()
+    _check(lib.attn_fwd_splitkv_noalloc(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v),
+                                        float(scale), ctypes.byref(cm), int(num_splits), _ptr(o), _ptr(lse),
+                                        _stream(stream)), "attn_fwd_splitkv_noalloc")
+    return o, lse

@@ -321,6 +321,30 @@ int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, c
                         workspace, static_cast<cudaStream_t>(stream));
 }
 
+int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k,
+                             const void* v, float scale, const gbattn_mask* mask, int num_splits, void* o, float* lse,
+                             gbattn_stream stream) {
+  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
+  if (!q || !k || !v || !o) return GBATTN_ERR_ARG;
+  if (num_splits < 1 || num_splits > 64) return GBATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
+    return GBATTN_ERR_ALIGN;
+  if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+  if (!(Dqk == Dv && (Dqk == 64 || Dqk == 128))) return GBATTN_ERR_UNSUPPORTED;
+  HostMask hm;
+  int rc = check_mask(mask, &hm);
+  if (rc) return rc;
+  if (hm.kind != GBATTN_MASK_NONE && hm.kind != GBATTN_MASK_CAUSAL) return GBATTN_ERR_UNSUPPORTED;
+  if (hm.softcap != 0.f || hm.slope != 0.f || hm.key_bias) return GBATTN_ERR_UNSUPPORTED;
+  const size_t need = attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits);
+  if (need > (size_t)GBATTN_NOALLOC_SCRATCH_BYTES) return GBATTN_ERR_WORKSPACE;
+  rc = device_check();
+  if (rc) return rc;
+  const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  return splitkv_noalloc_launch(s, q, k, v, resolve_scale(scale, Dqk), hm.kind == GBATTN_MASK_CAUSAL, num_splits,
+                                need, o, lse, static_cast<cudaStream_t>(stream));
+}
+
 int gbattn_last_device_error(gbattn_stream stream) {
   if (device_check() != GBATTN_OK) return GBATTN_ERR_UNSUPPORTED;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GBATTN_ERR_CUDA;

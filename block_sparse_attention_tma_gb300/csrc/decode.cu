@@ -9,6 +9,8 @@
 // output over its keys (online softmax); the warps are merged at the end and
 // the split partials are merged by a combine kernel using the rule of the
 // POPCORNBENCH "Kimi-K2.6 l1_p97" trace: m = max_s m_s, weights exp(m_s - m).
+#include <mutex>
+
 #include "kernels.h"
 #include "mask.cuh"
 
@@ -294,6 +296,45 @@ int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, 
   if (s.Dqk == 128) return launch_dec<128>(prm, st);
   if (s.Dqk == 64) return launch_dec<64>(prm, st);
   return GBATTN_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free split-KV: the split partials live in this file-scope array
+// (GBATTN_NOALLOC_SCRATCH_BYTES), for callers that may not allocate device
+// memory. Host code cannot use the array's name as a device address; the
+// address is looked up once per device with that device current. Nothing in
+// the array needs to start at zero: every split writes its whole partial
+// (empty splits write LSE = -inf and zeros). Calls that overlap on the GPU
+// share the array and race.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GBATTN_NOALLOC_SCRATCH_BYTES];
+
+static void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+int splitkv_noalloc_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                           int num_splits, size_t workspace_bytes, void* o, float* lse, cudaStream_t st) {
+  if (workspace_bytes > (size_t)GBATTN_NOALLOC_SCRATCH_BYTES) return GBATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (num_splits > 1) {
+    scratch = noalloc_scratch_address();
+    if (!scratch) return GBATTN_ERR_CUDA;
+  }
+  return splitkv_launch(s, q, k, v, scale, causal, num_splits, o, lse, scratch, st);
 }
 
 GB_DEFINE_ERROR_READER(decode_take_error)

@@ -44,6 +44,10 @@ int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
                     float* dv, void* ws, cudaStream_t st);
 int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
                    int num_splits, void* o, float* lse, void* ws, cudaStream_t st);
+// Split-KV forward with its split partials in the library's static scratch
+// array (no allocation); workspace_bytes is what attn_fwd_splitkv would need.
+int splitkv_noalloc_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                           int num_splits, size_t workspace_bytes, void* o, float* lse, cudaStream_t st);
 int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbattn_blocks* out,
                      cudaStream_t st);
 

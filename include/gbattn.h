@@ -188,6 +188,40 @@ int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
                      const gbattn_mask* mask, int num_splits, void* o, float* lse,
                      void* workspace, size_t workspace_bytes, gbattn_stream stream);
 
+/*
+ * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is a
+ * convenience of this library, not a step of the method.
+ *
+ * Some callers only ever hold the buffers they are handed: a plug-in inside an
+ * inference engine whose device memory all belongs to the engine's own
+ * allocator, or a latency-critical decode loop that must not call cudaMalloc
+ * once it runs (cudaMalloc can synchronise the device and stall other work).
+ * They cannot provide the split workspace attn_fwd_splitkv asks for. This
+ * entry point takes the same arguments minus the workspace and keeps the split
+ * partials in a scratch array that the library holds in device memory: a
+ * file-scope array of GBATTN_NOALLOC_SCRATCH_BYTES bytes, reserved on every GPU
+ * that loads the library until the process exits. It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   - Limit: attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits) must
+ *     not exceed GBATTN_NOALLOC_SCRATCH_BYTES; larger problems are rejected
+ *     with GBATTN_ERR_WORKSPACE (use attn_fwd_splitkv with your own workspace).
+ *     num_splits == 1 needs no scratch.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind. Calls
+ *     whose GPU work overlaps (different streams, or several host threads)
+ *     race on it and give wrong results: order them on one stream or
+ *     synchronise between them.
+ * Arguments, layouts, supported shapes and the other status codes are those of
+ * attn_fwd_splitkv.
+ */
+#define GBATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+                             const void* q, const void* k, const void* v, float scale,
+                             const gbattn_mask* mask, int num_splits, void* o, float* lse,
+                             gbattn_stream stream);
+
 /* Synchronises `stream`, then returns and clears the device-side error word
  * of the current device: GBATTN_OK, GBATTN_ERR_TIMEOUT (a bounded wait inside
  * a kernel ran out; the kernel returned early and its outputs are invalid) or

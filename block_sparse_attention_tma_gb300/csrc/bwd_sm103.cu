@@ -442,34 +442,371 @@ __global__ void __launch_bounds__(192, 1) dkdv_kernel(const __grid_constant__ Bw
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// ------------------------------------------------------------------ dQ (deterministic)
+// ------------------------------------------------------------------ dK / dV, TMEM-resident (no dQ)
+// CTA = (b, h, 128-key tile). Per listed query tile n (thread = key row):
+//   S^T_n = K Q_n^T -> R;   P^T_n = exp2(...) -> X (bf16);
+//   dP^T_n = V dO_n^T -> R; dV += P^T_n dO_n (A = X);
+//   dS^T_n = P^T (dP^T - delta) -> X (bf16);  dK += dS^T_n Q_n (A = X).
+// dK of tile n is issued after S^T of tile n+1, so the tensor pipe runs
+// S^T_{n+1} / dK_n / dP^T_{n+1} / dV_{n+1} back to back while the dS warps
+// work. TMEM: R [0,128), X [128,192), dV [192,192+Dv), dK [192+Dv, +Dqk).
 template <int DQK, int DV>
-struct DqCfg {
+struct Dkdv2Cfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
   static constexpr int SWV = DV >= 64 ? 128 : 64;
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
   static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
-  static constexpr int DSTILE = 128 * 128 * 2;
-  static constexpr int T_S = 0, T_DP = 128, T_DQ = 256;
-  static_assert(256 + DQK <= 512, "TMEM budget");
-  enum { B_QG, B_KF, B_KE, B_VF, B_VE, B_S, B_DS, B_DQD, B_DRAIN, NBAR };
-  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + QTILE + VTILE + DSTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
+  static constexpr int QST = 2;
+  static constexpr int GST = DQK >= 192 ? 1 : 2;
+  static constexpr int T_R = 0, T_X = 128, T_DV = 192, T_DK = 192 + DV;
+  static_assert(192 + DV + DQK <= 512, "TMEM budget");
+  enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_P, B_DP, B_DVD,
+         B_DS, B_DKD, B_DONE, B_DRAIN, NBAR };
+  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + NBAR * 8 + 16 + 4096;
+  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
+  static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
+  static constexpr uint32_t ID_DV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
+  static constexpr uint32_t ID_DK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
+};
+
+template <int DQK, int DV, bool CAP>
+__global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dkdv2Cfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = base;
+  uint8_t* sV = sK + C::QTILE;
+  uint8_t* sQ = sV + C::VTILE;                  // [QST]
+  uint8_t* sG = sQ + C::QST * C::QTILE;         // [GST]
+  float* sLD = reinterpret_cast<float*>(sG + C::GST * C::VTILE);  // [QST][lse2 128 | delta 128]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sLD + C::QST * 256);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int bh = blockIdx.x % BH;
+  const int k0 = (blockIdx.x / BH) * 128;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 128 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  TileWalk walk;
+  int nslots;
+  if (p.has_lists) {
+    walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
+    nslots = walk.nslots;
+  } else {
+    nslots = (p.Sq + 127) / 128;
+  }
+  auto slot = [&](int s, int* q0, bool* masked) -> bool {
+    return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, q0, masked)
+                       : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, q0, masked);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int n = 0, nq = 0, ng = 0;
+      bool ok = true;
+      for (int s = 0; s < nslots && ok; ++s) {
+        int q0;
+        bool masked;
+        if (!slot(s, &q0, &masked)) continue;
+        if (n == 0) {
+          mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
+          for (int j = 0; j < C::NQSLAB; ++j)
+            tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bh);
+          for (int j = 0; j < C::NVSLAB; ++j)
+            tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bh);
+        }
+        const int qs = n % C::QST;
+        if (n >= C::QST && !(ok = mbar_wait(bar + C::B_QE + qs, ((n / C::QST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
+        for (int j = 0; j < C::NQSLAB; ++j)
+          tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
+        bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+        bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+        ++nq;
+        const int gs = n % C::GST;
+        if (n >= C::GST && !(ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
+        for (int j = 0; j < C::NVSLAB; ++j)
+          tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bh);
+        ++ng;
+        ++n;
+      }
+      if (*abort_flag) {
+        if (nq > 0) mbar_drain(bar + C::B_KV, 0);
+        for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t) mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
+        for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t) mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), qa = smem_u32(sQ), ga = smem_u32(sG);
+      auto issue_dk = [&](int j) {
+        const int qs = j % C::QST;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + C::T_DK, tmem + C::T_X + kk * 8,
+                  sdesc(qa + qs * C::QTILE + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DK,
+                  (j > 0 || kk > 0));
+        umma_commit(bar + C::B_DKD);
+        umma_commit(bar + C::B_QE + qs);
+      };
+      int n = 0;
+      bool ok = true;
+      for (int s = 0; s < nslots && ok; ++s) {
+        int q0;
+        bool masked;
+        if (!slot(s, &q0, &masked)) continue;
+        if (n == 0 && !(ok = mbar_wait(bar + C::B_KV, 0, abort_flag))) break;
+        const int qs = n % C::QST;
+        if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
+        // R is free once the dS warps have read dP^T of the previous tile
+        if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const int slab = (kk * 16) / (C::SWQ / 2), off = (kk * 32) % C::SWQ;
+          umma_ss(tmem + C::T_R, sdesc(ka + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)),
+                  sdesc(qa + qs * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_ST,
+                  kk > 0);
+        }
+        umma_commit(bar + C::B_S);
+        if (n >= 1) issue_dk(n - 1);
+        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;
+        const int gs = n % C::GST;
+        if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const int slab = (kk * 16) / (C::SWV / 2), off = (kk * 32) % C::SWV;
+          umma_ss(tmem + C::T_R, sdesc(va + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)),
+                  sdesc(ga + gs * C::VTILE + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_ST,
+                  kk > 0);
+        }
+        umma_commit(bar + C::B_DP);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + C::T_DV, tmem + C::T_X + kk * 8,
+                  sdesc(ga + gs * C::VTILE + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV)), C::ID_DV,
+                  (n > 0 || kk > 0));
+        umma_commit(bar + C::B_DVD);
+        umma_commit(bar + C::B_GE + gs);
+        ++n;
+      }
+      if (ok && n >= 1) {
+        if ((ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) {
+          tc_fence_after();
+          issue_dk(n - 1);
+        }
+      }
+      umma_commit(bar + C::B_DONE);
+      if (*abort_flag) {
+        umma_commit(bar + C::B_DRAIN);
+        mbar_drain(bar + C::B_DRAIN, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ P / dS warps
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row
+    const int j = k0 + row;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    int ilo, ihi;
+    col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
+    bool kept = j < p.Sk;
+    if (kept && p.mask.keep) kept = (__ldg(p.mask.keep + (size_t)bh * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
+    const float kb = (j < p.Sk && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bh * p.Sk + j) : 0.f;
+    const float kt = (kb - p.mask.slope * (float)j) * kLog2e;  // per-key score term, log2 units
+    int n = 0;
+    bool ok = true;
+    for (int s = 0; s < nslots && ok; ++s) {
+      int q0;
+      bool masked;
+      if (!slot(s, &q0, &masked)) continue;
+      const int qs = n % C::QST;
+      ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag);  // lse2 / delta landed
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* sl = sLD + qs * 256;
+      const float* sd = sl + 128;
+      const int clo = masked ? (kept ? ilo - q0 : 128) : 0;
+      const int chi = masked ? ihi - q0 : 127;
+      uint32_t pk[64], dc[CAP ? 64 : 1];
+#pragma unroll
+      for (int qtr = 0; qtr < 4; ++qtr) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::T_R + qtr * 32, r);
+        tmem_wait_ld32(r);
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          float pr[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cl = 2 * c2 + e, c = qtr * 32 + cl;
+            const float x = __uint_as_float(r[cl]);
+            float t;
+            dd[e] = 1.f;
+            if constexpr (CAP) {
+              const float th = tanh_fast(x * p.cap_pre);
+              t = p.cap_post * th;
+              dd[e] = 1.f - th * th;
+            } else {
+              t = x * p.scale_log2;
+            }
+            const float v = ex2(t + kt - sl[c]);
+            pr[e] = (c >= clo && c <= chi) ? v : 0.f;
+          }
+          pk[qtr * 16 + c2] = pack_bf16(pr[0], pr[1]);
+          if constexpr (CAP) dc[qtr * 16 + c2] = pack_bf16(dd[0], dd[1]);
+        }
+      }
+      // X still holds dS^T of the previous tile until its dK MMA completes
+      if (n >= 1) {
+        ok = mbar_wait(bar + C::B_DKD, (n - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tl + C::T_X, pk);
+      tmem_st32(tl + C::T_X + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar + C::B_P);
+      // dP^T -> dS^T
+      ok = mbar_wait(bar + C::B_DP, n & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t ds[64];
+#pragma unroll
+      for (int qtr = 0; qtr < 4; ++qtr) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::T_R + qtr * 32, r);
+        tmem_wait_ld32(r);
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const int c = qtr * 32 + 2 * c2;
+          const uint32_t pw = pk[qtr * 16 + c2];
+          float d0 = bf_lo(pw) * (__uint_as_float(r[2 * c2]) - sd[c]);
+          float d1 = bf_hi(pw) * (__uint_as_float(r[2 * c2 + 1]) - sd[c + 1]);
+          if constexpr (CAP) {
+            d0 *= bf_lo(dc[qtr * 16 + c2]);
+            d1 *= bf_hi(dc[qtr * 16 + c2]);
+          }
+          ds[qtr * 16 + c2] = pack_bf16(d0, d1);
+        }
+      }
+      // X holds P^T until the dV MMA completes
+      ok = mbar_wait(bar + C::B_DVD, n & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tl + C::T_X, ds);
+      tmem_st32(tl + C::T_X + 32, ds + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar + C::B_DS);
+      ++n;
+    }
+    // ---- epilogue: dV, dK rows of this thread's key
+    if (ok) {
+      const bool wrote = n > 0;
+      if (wrote) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar + C::B_DONE, 0, abort_flag));
+        tc_fence_after();
+      }
+      if (ok) {
+        __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + j) * DV;
+        __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + j) * DQK;
+#pragma unroll 1
+        for (int c0 = 0; c0 < DV + DQK; c0 += 32) {
+          const bool isv = c0 < DV;
+          uint32_t a[32];
+          if (wrote) {
+            tmem_ld32(tl + (isv ? C::T_DV + c0 : C::T_DK + c0 - DV), a);
+            tmem_wait_ld32(a);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) a[c] = 0u;
+          }
+          const float sc = isv ? 1.f : p.scale;
+          __nv_bfloat16* dst = isv ? dvrow + c0 : dkrow + (c0 - DV);
+          if (j < p.Sk) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8)
+              *reinterpret_cast<uint4*>(dst + c) =
+                  make_uint4(pack_bf16(sc * __uint_as_float(a[c]), sc * __uint_as_float(a[c + 1])),
+                             pack_bf16(sc * __uint_as_float(a[c + 2]), sc * __uint_as_float(a[c + 3])),
+                             pack_bf16(sc * __uint_as_float(a[c + 4]), sc * __uint_as_float(a[c + 5])),
+                             pack_bf16(sc * __uint_as_float(a[c + 6]), sc * __uint_as_float(a[c + 7])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ dQ, query-parallel (no atomics)
+// CTA = (b, h, 128-row query tile), walking the forward lists (thread = query
+// row). Per kv tile n: S_n = Q K_n^T -> [0,128), dP_n = dO V_n^T -> [128,256);
+// dS_n = P (dP - delta) -> [448,512) (bf16); dQ += dS_n K_n -> [256,256+Dqk).
+// dQ of tile n is issued after S / dP of tile n+1.
+template <int DQK, int DV>
+struct Dq2Cfg {
+  static constexpr int SWQ = DQK >= 64 ? 128 : 64;
+  static constexpr int SWV = DV >= 64 ? 128 : 64;
+  static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
+  static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
+  static constexpr int KST = 2;
+  static constexpr int VST = DQK >= 192 ? 1 : 2;
+  static constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 448;
+  static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
+  enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DS, B_DQD, B_DONE,
+         B_DRAIN, NBAR };
+  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t ID_DQ = idesc_bf16(128, DQK, false, true);
 };
 
-template <int DQK, int DV>
-__global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdParams p) {
-  using C = DqCfg<DQK, DV>;
+template <int DQK, int DV, bool CAP>
+__global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ BwdParams p) {
+  using C = Dq2Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sG = sQ + C::QTILE;
-  uint8_t* sK = sG + C::VTILE;
-  uint8_t* sV = sK + C::QTILE;
-  uint8_t* sS = sV + C::VTILE;
-  float* colterm = reinterpret_cast<float*>(sS + C::DSTILE);  // [4 warps][2][128]
+  uint8_t* sK = sG + C::VTILE;             // [KST]
+  uint8_t* sV = sK + C::KST * C::QTILE;    // [VST]
+  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 warps][2][128]
   uint64_t* bar = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -519,27 +856,39 @@ __global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdP
           for (int j = 0; j < C::NVSLAB; ++j)
             tma_load_3d(sG + j * C::VSLAB, &p.tm_do, bar + C::B_QG, j * (C::SWV / 2), q0, bh);
         }
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_KE, (n - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_KF, C::QTILE);
+        const int ks = n % C::KST;
+        if (n >= C::KST && !(ok = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
         for (int j = 0; j < C::NQSLAB; ++j)
-          tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KF, j * (C::SWQ / 2), kv0, bh);
+          tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bh);
         ++nk;
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_VE, (n - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_VF, C::VTILE);
+        const int vs = n % C::VST;
+        if (n >= C::VST && !(ok = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
+        mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
         for (int j = 0; j < C::NVSLAB; ++j)
-          tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_VF, j * (C::SWV / 2), kv0, bh);
+          tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, bar + C::B_VF + vs, j * (C::SWV / 2), kv0, bh);
         ++nv;
         ++n;
       }
       if (*abort_flag) {
         if (nk > 0) mbar_drain(bar + C::B_QG, 0);
-        if (nk > 0) mbar_drain(bar + C::B_KF, (nk - 1) & 1);
-        if (nv > 0) mbar_drain(bar + C::B_VF, (nv - 1) & 1);
+        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
+        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t qa = smem_u32(sQ), ga = smem_u32(sG), ka = smem_u32(sK), va = smem_u32(sV), sa = smem_u32(sS);
+      const uint32_t qa = smem_u32(sQ), ga = smem_u32(sG), ka = smem_u32(sK), va = smem_u32(sV);
+      auto issue_dq = [&](int jt) {
+        const int ks = jt % C::KST;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + C::T_DQ, tmem + C::T_DS + kk * 8,
+                  sdesc(ka + ks * C::QTILE + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DQ,
+                  (jt > 0 || kk > 0));
+        umma_commit(bar + C::B_DQD);
+        umma_commit(bar + C::B_KE + ks);
+      };
       int n = 0;
       bool ok = true;
       for (int s = 0; s < nslots && ok; ++s) {
@@ -547,39 +896,36 @@ __global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdP
         bool masked;
         if (!slot(s, &kv0, &masked)) continue;
         if (n == 0 && !(ok = mbar_wait(bar + C::B_QG, 0, abort_flag))) break;
-        if (!(ok = mbar_wait(bar + C::B_KF, n & 1, abort_flag))) break;
-        // S and dP buffers are free once the dS of the previous tile is ready
+        const int ks = n % C::KST, vs = n % C::VST;
+        if (!(ok = mbar_wait(bar + C::B_KF + ks, (n / C::KST) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar + C::B_VF + vs, (n / C::VST) & 1, abort_flag))) break;
+        // S / dP buffers are free once the dS warps have read the previous tile
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const int slab = (kk * 16) / (C::SWQ / 2), off = (kk * 32) % C::SWQ;
           umma_ss(tmem + C::T_S, sdesc(qa + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)),
-                  sdesc(ka + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_S, kk > 0);
+                  sdesc(ka + ks * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_S, kk > 0);
         }
-        if (!(ok = mbar_wait(bar + C::B_VF, n & 1, abort_flag))) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const int slab = (kk * 16) / (C::SWV / 2), off = (kk * 32) % C::SWV;
           umma_ss(tmem + C::T_DP, sdesc(ga + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)),
-                  sdesc(va + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_S, kk > 0);
+                  sdesc(va + vs * C::VTILE + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_S, kk > 0);
         }
-        umma_commit(bar + C::B_VE);
         umma_commit(bar + C::B_S);
-        if (!(ok = mbar_wait(bar + C::B_DS, n & 1, abort_flag))) break;
-        tc_fence_after();
-        // dQ += dS K : A = dS (K-major, rows = queries), B = K MN-major (N = DQK)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int slab = kk >> 2, off = (kk & 3) * 32;
-          umma_ss(tmem + C::T_DQ, sdesc(sa + slab * 16384 + off, 16, 1024, 2),
-                  sdesc(ka + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DQ, (n > 0 || kk > 0));
-        }
-        umma_commit(bar + C::B_KE);
-        umma_commit(bar + C::B_DQD);
+        umma_commit(bar + C::B_VE + vs);
+        if (n >= 1) issue_dq(n - 1);
         ++n;
       }
+      if (ok && n >= 1) {
+        if ((ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) {
+          tc_fence_after();
+          issue_dq(n - 1);
+        }
+      }
+      umma_commit(bar + C::B_DONE);
       if (*abort_flag) {
         umma_commit(bar + C::B_DRAIN);
         mbar_drain(bar + C::B_DRAIN, 0);
@@ -596,7 +942,6 @@ __global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdP
     const float dl = p.delta[(size_t)bh * p.sq_pad + i];
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
     const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
-    const bool cap = p.cap_pre != 0.f;
     int n = 0;
     bool ok = true;
     for (int s = 0; s < nslots && ok; ++s) {
@@ -606,15 +951,17 @@ __global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdP
       float* ctw = colterm + (quarter * 2 + (n & 1)) * 128;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int j = kv0 + e * 32 + lane;
+        const int jj = kv0 + e * 32 + lane;
         float c = 0.f;
-        if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
+        if (jj < p.Sk) c = ((kb ? __ldg(kb + jj) : 0.f) - p.mask.slope * (float)jj) * kLog2e;
         ctw[e * 32 + lane] = c;
       }
       __syncwarp();
       ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
-      if (ok && n >= 1) ok = mbar_wait(bar + C::B_DQD, (n - 1) & 1, abort_flag);  // dS tile free
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (keep) {
@@ -628,55 +975,61 @@ __global__ void __launch_bounds__(192, 1) dq_kernel(const __grid_constant__ BwdP
       const int chi = masked ? min(hi, p.Sk - 1) - kv0 : 127;
       uint32_t ds[64];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t rs[64], rp[64];
-        tmem_ld32(tl + C::T_S + half * 64, rs);
-        tmem_ld32(tl + C::T_S + half * 64 + 32, rs + 32);
-        tmem_ld32(tl + C::T_DP + half * 64, rp);
-        tmem_ld32(tl + C::T_DP + half * 64 + 32, rp + 32);
+      for (int qtr = 0; qtr < 4; ++qtr) {
+        uint32_t rs[32], rp[32];
+        tmem_ld32(tl + C::T_S + qtr * 32, rs);
+        tmem_ld32(tl + C::T_DP + qtr * 32, rp);
         tmem_wait_ld32(rs);
-        reg_fence32(rs + 32);
         reg_fence32(rp);
-        reg_fence32(rp + 32);
+        const float4* ct = reinterpret_cast<const float4*>(ctw + qtr * 32);
 #pragma unroll
-        for (int c2 = 0; c2 < 32; ++c2) {
-          float d[2];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 v4 = ct[c4];
+          const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+          float d[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * c2 + e, c = half * 64 + cl;
+          for (int e = 0; e < 4; ++e) {
+            const int cl = 4 * c4 + e, c = qtr * 32 + cl;
             const float x = __uint_as_float(rs[cl]);
             float t, dd = 1.f;
-            if (cap) {
+            if constexpr (CAP) {
               const float th = tanh_fast(x * p.cap_pre);
-              t = p.cap_post * th;
+              t = fmaf(p.cap_post, th, cv[e]);
               dd = 1.f - th * th;
             } else {
-              t = x * p.scale_log2;
+              t = fmaf(x, p.scale_log2, cv[e]);
             }
             const bool al = c >= clo && c <= chi && ((kw[c >> 5] >> (c & 31)) & 1u);
-            const float pv = al ? ex2(t + ctw[c] - l2) : 0.f;
+            const float pv = al ? ex2(t - l2) : 0.f;
             d[e] = pv * (__uint_as_float(rp[cl]) - dl) * dd;
           }
-          ds[half * 32 + c2] = pack_bf16(d[0], d[1]);
+          ds[qtr * 16 + 2 * c4] = pack_bf16(d[0], d[1]);
+          ds[qtr * 16 + 2 * c4 + 1] = pack_bf16(d[2], d[3]);
         }
       }
-      store_row_sw128(sS, row, ds);
-      fence_async_smem();
+      // the dS columns still feed the dQ MMA of the previous tile
+      if (n >= 1) {
+        ok = mbar_wait(bar + C::B_DQD, (n - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tl + C::T_DS, ds);
+      tmem_st32(tl + C::T_DS + 32, ds + 32);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_DS);
       ++n;
     }
-    if (ok && i < p.Sq) {
+    if (ok) {
       __nv_bfloat16* dst = p.dq + ((size_t)bh * p.Sq + i) * DQK;
       if (n == 0) {
-        for (int c = 0; c < DQK; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar + C::B_DQD, (n - 1) & 1, abort_flag));
-      if (ok) {
+        if (i < p.Sq)
+          for (int c = 0; c < DQK; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+      } else if (__all_sync(0xffffffffu, mbar_wait(bar + C::B_DONE, 0, abort_flag))) {
         tc_fence_after();
-        __nv_bfloat16* dst = p.dq + ((size_t)bh * p.Sq + i) * DQK;
 #pragma unroll 1
         for (int c0 = 0; c0 < DQK; c0 += 32) {
           uint32_t a[32];
@@ -714,19 +1067,28 @@ static int set_smem_once(K kern, int bytes, bool* flag) {
   return GBATTN_OK;
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool CAP>
 static int launch_bwd_main(const BwdParams& prm, const Shape& s, int deterministic, cudaStream_t st) {
   const int BH = s.B * s.H;
-  static bool f1 = false, f2 = false;
-  if (set_smem_once(dkdv_kernel<DQK, DV>, BwdCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
-  dkdv_kernel<DQK, DV><<<((s.Sk + 127) / 128) * BH, 192, BwdCfg<DQK, DV>::SMEM, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  if (deterministic) {
-    if (set_smem_once(dq_kernel<DQK, DV>, DqCfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
-    dq_kernel<DQK, DV><<<((s.Sq + 127) / 128) * BH, 192, DqCfg<DQK, DV>::SMEM, st>>>(prm);
-    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  if (!deterministic) {
+    static bool f1 = false;
+    if (set_smem_once(dkdv_kernel<DQK, DV>, BwdCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
+    dkdv_kernel<DQK, DV><<<((s.Sk + 127) / 128) * BH, 192, BwdCfg<DQK, DV>::SMEM, st>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
   }
-  return GBATTN_OK;
+  static bool f2 = false, f3 = false;
+  if (set_smem_once(dkdv2_kernel<DQK, DV, CAP>, Dkdv2Cfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
+  dkdv2_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 192, Dkdv2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  if (set_smem_once(dq2_kernel<DQK, DV, CAP>, Dq2Cfg<DQK, DV>::SMEM, &f3)) return GBATTN_ERR_CUDA;
+  dq2_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 192, Dq2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+template <int DQK, int DV>
+static int launch_bwd_cap(const BwdParams& prm, const Shape& s, int deterministic, bool cap, cudaStream_t st) {
+  return cap ? launch_bwd_main<DQK, DV, true>(prm, s, deterministic, st)
+             : launch_bwd_main<DQK, DV, false>(prm, s, deterministic, st);
 }
 
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -797,10 +1159,11 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   if (!deterministic && cudaMemsetAsync(prm.dq_acc, 0, (size_t)BH * s.Sq * s.Dqk * sizeof(float), st) != cudaSuccess)
     return GBATTN_ERR_CUDA;
   int rc;
-  if (s.Dqk == 32 && s.Dv == 32) rc = launch_bwd_main<32, 32>(prm, s, deterministic, st);
-  else if (s.Dqk == 64 && s.Dv == 64) rc = launch_bwd_main<64, 64>(prm, s, deterministic, st);
-  else if (s.Dqk == 128 && s.Dv == 128) rc = launch_bwd_main<128, 128>(prm, s, deterministic, st);
-  else if (s.Dqk == 192 && s.Dv == 128) rc = launch_bwd_main<192, 128>(prm, s, deterministic, st);
+  const bool cap = m.softcap > 0.f;
+  if (s.Dqk == 32 && s.Dv == 32) rc = launch_bwd_cap<32, 32>(prm, s, deterministic, cap, st);
+  else if (s.Dqk == 64 && s.Dv == 64) rc = launch_bwd_cap<64, 64>(prm, s, deterministic, cap, st);
+  else if (s.Dqk == 128 && s.Dv == 128) rc = launch_bwd_cap<128, 128>(prm, s, deterministic, cap, st);
+  else if (s.Dqk == 192 && s.Dv == 128) rc = launch_bwd_cap<192, 128>(prm, s, deterministic, cap, st);
   else return GBATTN_ERR_UNSUPPORTED;
   if (rc) return rc;
   if (!deterministic) {

@@ -8,14 +8,21 @@
 // "Kimi-K2.6 l1_p97" trace (m_new = max, rescale by exp(m_old - m_new)).
 //
 // One CTA = one (b, h, 128-row query tile); 6 warps:
-//   warp 0      TMA producer: Q once, then K and V tiles into a ring.
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (two buffers),
-//               O += P V with P read from TMEM (A operand) and V from smem.
-//   warps 2..5  softmax: thread = query row = TMEM lane. Loads its S row,
-//               masks, exp2 with the scale folded in, writes P (bf16) back
-//               over the S buffer, rescales O only when the row max grows by
-//               more than 2^8 ("lazy" rescale), final O / l and LSE.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv).
+//   warp 0      TMA producer: Q once, then K and V tiles into rings.
+//   warp 1      MMA issuer (one thread): S = Q K^T with Q read from TMEM
+//               (A operand) and K from shared memory, into one of two TMEM S
+//               buffers; O += P V with P read from TMEM and V (MN-major) from
+//               shared memory.
+//   warps 2..5  softmax: thread = query row = TMEM lane. Copies its Q row
+//               into TMEM once; per tile loads its S row, masks (partial
+//               tiles only), folds scale * log2(e) and the per-key bias term
+//               into one FMA, exp2, writes P (bf16) back over the S buffer,
+//               and rescales O only when the row max grows by more than 2^8
+//               ("lazy" rescale); final O / l and LSE.
+// Keeping Q in TMEM means the QK^T MMA reads only K from shared memory; the
+// shared-memory traffic per tile (K + V reads, K + V TMA writes) then fits
+// the time of the two MMAs.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv), Q [384, 384+Dqk/2).
 #include "kernels.h"
 #include "mask.cuh"
 
@@ -26,9 +33,8 @@ struct FwdParams {
   int B, H, Sq, Sk;
   int nqt;             // query tiles per head
   float scale_log2;    // scale * log2(e)
-  float cap_pre;       // scale / softcap (softcap on), else 0
+  float cap_pre;       // scale / softcap (softcap on)
   float cap_post;      // softcap * log2(e)
-  int has_colterm;     // key bias or rel-bias slope present
   MaskParams mask;
   int has_lists;
   int sub;             // sparse_n / 128
@@ -50,9 +56,11 @@ struct FwdCfg {
   static constexpr int VTILE = 128 * DV * 2;
   static constexpr int KST = DQK >= 192 ? 2 : 3;
   static constexpr int VST = DQK >= 128 ? 2 : 3;
-  // barriers: q_full, k_full[KST], k_empty[KST], v_full[VST], v_empty[VST],
-  // s_full[2], p_full[2], o_done, drain
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  static constexpr int T_O = 256, T_Q = 384;
+  static_assert(T_Q + DQK / 2 <= 512 && T_O + DV <= T_Q, "TMEM budget");
+  // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
+  // v_empty[VST], s_full[2], p_full[2], o_done, drain
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
   static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
@@ -61,7 +69,19 @@ struct FwdCfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
 };
 
-template <int DQK, int DV>
+// Loads 128 consecutive TMEM columns of this thread's lane into r[].
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
+  tmem_ld32(taddr + 0, r);
+  tmem_ld32(taddr + 32, r + 32);
+  tmem_ld32(taddr + 64, r + 64);
+  tmem_ld32(taddr + 96, r + 96);
+  tmem_wait_ld32(r);
+  reg_fence32(r + 32);
+  reg_fence32(r + 64);
+  reg_fence32(r + 96);
+}
+
+template <int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -72,7 +92,8 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
   float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 warps][2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
   uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
+  uint64_t* q_tmem = q_full + 1;
+  uint64_t* k_full = q_tmem + 1;
   uint64_t* k_empty = k_full + C::KST;
   uint64_t* v_full = k_empty + C::KST;
   uint64_t* v_empty = v_full + C::VST;
@@ -93,6 +114,7 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_tmem, 128);
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128); }
@@ -121,23 +143,32 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
     return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
                        : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
   };
+  // First slot this CTA visits (every role computes the same answer).
+  int first = nslots;
+  for (int s = 0; s < nslots; ++s) {
+    int kv0;
+    bool masked;
+    if (slot(s, &kv0, &masked)) {
+      first = s;
+      break;
+    }
+  }
+  const bool any_tile = first < nslots;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && any_tile) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
+      mbar_expect_tx(q_full, C::QTILE);
+      for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
       int n = 0, nk = 0, nv = 0;
       bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
+      for (int s = first; s < nslots && ok; ++s) {
         int kv0;
         bool masked;
         if (!slot(s, &kv0, &masked)) continue;
-        if (n == 0) {
-          mbar_expect_tx(q_full, C::QTILE);
-          for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
-        }
         const int ks = n % C::KST;
         if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
         mbar_expect_tx(k_full + ks, C::QTILE);
@@ -154,15 +185,15 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
       }
       if (*abort_flag) {
         // let every copy this thread started land before the CTA exits
-        if (nk > 0) mbar_drain(q_full, 0);
+        mbar_drain(q_full, 0);
         for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
         for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+    if (lane == 0 && any_tile) {
+      const uint32_t ka = smem_u32(sK), va = smem_u32(sV);
       auto issue_pv = [&](int j) -> bool {
         const int sb = j & 1;
         if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
@@ -173,19 +204,18 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
         for (int kk = 0; kk < 8; ++kk) {
           // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows
           const uint64_t bd = sdesc(va + vs * C::VTILE + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV));
-          umma_ts(tmem + 256, tmem + sb * 128 + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + C::T_O, tmem + sb * 128 + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(v_empty + vs);
         umma_commit(o_done);
         return true;
       };
       int n = 0;
-      bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
+      bool ok = mbar_wait(q_tmem, 0, abort_flag);
+      for (int s = first; s < nslots && ok; ++s) {
         int kv0;
         bool masked;
         if (!slot(s, &kv0, &masked)) continue;
-        if (n == 0 && !(ok = mbar_wait(q_full, 0, abort_flag))) break;
         const int ks = n % C::KST;
         if (!(ok = mbar_wait(k_full + ks, (n / C::KST) & 1, abort_flag))) break;
         tc_fence_after();
@@ -194,9 +224,8 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const int slab = (kk * 16) / (C::SWQ / 2);
           const int off = (kk * 32) % C::SWQ;
-          const uint64_t ad = sdesc(qa + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ));
           const uint64_t bd = sdesc(ka + ks * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ));
-          umma_ss(d, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          umma_ts(d, tmem + C::T_Q + kk * 8, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         umma_commit(k_empty + ks);
         umma_commit(s_full + (n & 1));
@@ -219,11 +248,36 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
     row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
     const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
-    const float slope_log2 = p.mask.slope * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     bool ok = true;
-    for (int s = 0; s < nslots && ok; ++s) {
+    if (any_tile) {
+      // copy this thread's Q row from the swizzled smem tile into TMEM
+      ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
+      if (ok) {
+        uint32_t qr[DQK / 2];
+#pragma unroll
+        for (int u = 0; u < DQK / 8; ++u) {
+          const int slab = u / (C::SWQ / 16), c16 = u % (C::SWQ / 16);
+          const int sw = (row * C::SWQ / 128) & (C::SWQ / 16 - 1);
+          const uint4 v = *reinterpret_cast<const uint4*>(sQ + slab * C::QSLAB + row * C::SWQ + ((c16 ^ sw) << 4));
+          qr[4 * u] = v.x;
+          qr[4 * u + 1] = v.y;
+          qr[4 * u + 2] = v.z;
+          qr[4 * u + 3] = v.w;
+        }
+        if constexpr (DQK / 2 >= 32) {
+#pragma unroll
+          for (int c = 0; c < DQK / 2; c += 32) tmem_st32(tl + C::T_Q + c, qr + c);
+        } else {
+          tmem_st16(tl + C::T_Q, qr);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(q_tmem);
+      }
+    }
+    for (int s = first; s < nslots && ok; ++s) {
       int kv0;
       bool masked;
       if (!slot(s, &kv0, &masked)) continue;
@@ -231,44 +285,34 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
       // per-key score term (key bias - slope * j) * log2(e); each warp keeps
       // its own copy (4 keys per lane), so only a warp-level sync is needed
       float* ctw = colterm + (quarter * 2 + sb) * 128;
-      if (p.has_colterm) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = kv0 + e * 32 + lane;
-          float c = 0.f;
-          if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
-          ctw[e * 32 + lane] = c;
-        }
-        __syncwarp();
+      for (int e = 0; e < 4; ++e) {
+        const int j = kv0 + e * 32 + lane;
+        float c = 0.f;
+        if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
+        ctw[e * 32 + lane] = c;
       }
+      __syncwarp();
       ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t r[128];
-      tmem_ld32(tl + sb * 128 + 0, r);
-      tmem_ld32(tl + sb * 128 + 32, r + 32);
-      tmem_ld32(tl + sb * 128 + 64, r + 64);
-      tmem_ld32(tl + sb * 128 + 96, r + 96);
-      tmem_wait_ld32(r);
-      reg_fence32(r + 32);
-      reg_fence32(r + 64);
-      reg_fence32(r + 96);
-      float t[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float x = __uint_as_float(r[c]);
-        x = (p.cap_pre != 0.f) ? p.cap_post * tanh_fast(x * p.cap_pre) : x * p.scale_log2;
-        t[c] = x;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
-      if (p.has_colterm) {
+      tc_fence_after();
+      float t[128];
+      tmem_ld128(tl + sb * 128, reinterpret_cast<uint32_t*>(t));
+      {
         const float4* ct = reinterpret_cast<const float4*>(ctw);
 #pragma unroll
         for (int c4 = 0; c4 < 32; ++c4) {
           const float4 v4 = ct[c4];
-          t[4 * c4 + 0] += v4.x;
-          t[4 * c4 + 1] += v4.y;
-          t[4 * c4 + 2] += v4.z;
-          t[4 * c4 + 3] += v4.w;
+          const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            if constexpr (CAP) t[c] = fmaf(p.cap_post, tanh_fast(t[c] * p.cap_pre), cv[e]);
+            else t[c] = fmaf(t[c], p.scale_log2, cv[e]);
+          }
         }
       }
       if (masked) {
@@ -291,9 +335,14 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
           for (int c = 0; c < 128; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
         }
       }
-      float mt = t[0];
+      // row max: 8 independent chains, then a short tree
+      float mx[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, t[c]);
+      for (int e = 0; e < 8; ++e) mx[e] = t[e];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], t[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float m_use = m_run, alpha = 1.f;
       bool resc = false;
       if (mt > m_run + 8.0f) {
@@ -304,30 +353,36 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
         m_use = mt;
       }
       const float msafe = (m_use == -INFINITY) ? 0.f : m_use;
-      float lsum = 0.f;
+      float ls[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float a0 = ex2(t[2 * c] - msafe);
         const float a1 = ex2(t[2 * c + 1] - msafe);
-        lsum += a0 + a1;
+        ls[c & 7] += a0 + a1;
         pk[c] = pack_bf16(a0, a1);
       }
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l_run = (resc ? l_run * alpha : l_run) + lsum;
       m_run = m_use;
       if (__any_sync(0xffffffffu, resc)) {
         // O must not be in flight: PV of the previous tile has completed
         ok = mbar_wait(o_done, (n - 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t orr[32];
-          tmem_ld32(tl + 256 + c0, orr);
+          tmem_ld32(tl + C::T_O + c0, orr);
           tmem_wait_ld32(orr);
 #pragma unroll
           for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-          tmem_st32(tl + 256 + c0, orr);
+          tmem_st32(tl + C::T_O + c0, orr);
         }
       }
       tmem_st32(tl + sb * 128 + 0, pk);
@@ -338,23 +393,21 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
       ++n;
     }
     // ---- epilogue
-    if (ok && i < p.Sq) {
+    if (ok && i < p.Sq && (n == 0 || l_run == 0.f)) {
       __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
-      if (n == 0 || l_run == 0.f) {
 #pragma unroll
-        for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-        if (p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
-      }
+      for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+      if (p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
     }
     if (ok && n > 0) {
       if (__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
         tc_fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
-#pragma unroll
+#pragma unroll 1
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t orr[32];
-          tmem_ld32(tl + 256 + c0, orr);
+          tmem_ld32(tl + C::T_O + c0, orr);
           tmem_wait_ld32(orr);
           if (i < p.Sq && l_run > 0.f) {
             uint32_t pkd[16];
@@ -379,10 +432,10 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool CAP>
 static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
-  auto kern = fwd_bf16_kernel<DQK, DV>;
+  auto kern = fwd_bf16_kernel<DQK, DV, CAP>;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
@@ -391,6 +444,11 @@ static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
   }
   kern<<<grid, 192, C::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+template <int DQK, int DV>
+static int launch_fwd_cap(const FwdParams& prm, int grid, bool cap, cudaStream_t st) {
+  return cap ? launch_fwd<DQK, DV, true>(prm, grid, st) : launch_fwd<DQK, DV, false>(prm, grid, st);
 }
 
 int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, const HostMask& m,
@@ -408,11 +466,11 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.Sk = s.Sk;
   prm.nqt = (s.Sq + 127) / 128;
   prm.scale_log2 = scale * kLog2e;
-  if (m.softcap > 0.f) {
+  const bool cap = m.softcap > 0.f;
+  if (cap) {
     prm.cap_pre = scale / m.softcap;
     prm.cap_post = m.softcap * kLog2e;
   }
-  prm.has_colterm = (m.key_bias != nullptr) || (m.slope != 0.f);
   prm.mask.kind = m.kind;
   prm.mask.window_left = m.window_left;
   prm.mask.block_size = m.block_size;
@@ -435,10 +493,10 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.o = reinterpret_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   const int grid = prm.nqt * BH;
-  if (s.Dqk == 32 && s.Dv == 32) return launch_fwd<32, 32>(prm, grid, st);
-  if (s.Dqk == 64 && s.Dv == 64) return launch_fwd<64, 64>(prm, grid, st);
-  if (s.Dqk == 128 && s.Dv == 128) return launch_fwd<128, 128>(prm, grid, st);
-  if (s.Dqk == 192 && s.Dv == 128) return launch_fwd<192, 128>(prm, grid, st);
+  if (s.Dqk == 32 && s.Dv == 32) return launch_fwd_cap<32, 32>(prm, grid, cap, st);
+  if (s.Dqk == 64 && s.Dv == 64) return launch_fwd_cap<64, 64>(prm, grid, cap, st);
+  if (s.Dqk == 128 && s.Dv == 128) return launch_fwd_cap<128, 128>(prm, grid, cap, st);
+  if (s.Dqk == 192 && s.Dv == 128) return launch_fwd_cap<192, 128>(prm, grid, cap, st);
   return GBATTN_ERR_UNSUPPORTED;
 }
 

@@ -470,7 +470,7 @@ struct Dkdv2Cfg {
 };
 
 template <int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ BwdParams p) {
   using C = Dkdv2Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
   const int k0 = (blockIdx.x / BH) * 128;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 128 : 1);
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -620,6 +620,9 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
     }
   } else {
     // ------------------------------------------------------------ P / dS warps
+    // two warps per TMEM lane quarter; each thread owns one key row and half
+    // (64) of the 128 query columns of the tile
+    const int sw = warp - 2, grp = sw >> 2, cb = grp * 64;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row
     const int j = k0 + row;
@@ -648,18 +651,18 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
       const float* sd = sl + 128;
       const int clo = masked ? (kept ? ilo - q0 : 128) : 0;
       const int chi = masked ? ihi - q0 : 127;
-      uint32_t pk[64], dc[CAP ? 64 : 1];
+      uint32_t pk[32], dc[CAP ? 32 : 1];
 #pragma unroll
-      for (int qtr = 0; qtr < 4; ++qtr) {
+      for (int qtr = 0; qtr < 2; ++qtr) {
         uint32_t r[32];
-        tmem_ld32(tl + C::T_R + qtr * 32, r);
+        tmem_ld32(tl + C::T_R + cb + qtr * 32, r);
         tmem_wait_ld32(r);
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
           float pr[2], dd[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * c2 + e, c = qtr * 32 + cl;
+            const int cl = 2 * c2 + e, c = cb + qtr * 32 + cl;
             const float x = __uint_as_float(r[cl]);
             float t;
             dd[e] = 1.f;
@@ -686,8 +689,7 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
         }
         tc_fence_after();
       }
-      tmem_st32(tl + C::T_X, pk);
-      tmem_st32(tl + C::T_X + 32, pk + 32);
+      tmem_st32(tl + C::T_X + grp * 32, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_P);
@@ -698,15 +700,15 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
         break;
       }
       tc_fence_after();
-      uint32_t ds[64];
+      uint32_t ds[32];
 #pragma unroll
-      for (int qtr = 0; qtr < 4; ++qtr) {
+      for (int qtr = 0; qtr < 2; ++qtr) {
         uint32_t r[32];
-        tmem_ld32(tl + C::T_R + qtr * 32, r);
+        tmem_ld32(tl + C::T_R + cb + qtr * 32, r);
         tmem_wait_ld32(r);
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-          const int c = qtr * 32 + 2 * c2;
+          const int c = cb + qtr * 32 + 2 * c2;
           const uint32_t pw = pk[qtr * 16 + c2];
           float d0 = bf_lo(pw) * (__uint_as_float(r[2 * c2]) - sd[c]);
           float d1 = bf_hi(pw) * (__uint_as_float(r[2 * c2 + 1]) - sd[c + 1]);
@@ -724,14 +726,14 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
         break;
       }
       tc_fence_after();
-      tmem_st32(tl + C::T_X, ds);
-      tmem_st32(tl + C::T_X + 32, ds + 32);
+      tmem_st32(tl + C::T_X + grp * 32, ds);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_DS);
       ++n;
     }
-    // ---- epilogue: dV, dK rows of this thread's key
+    // ---- epilogue: dV, dK rows of this thread's key (32-column chunks split
+    // between the two warps of a lane quarter)
     if (ok) {
       const bool wrote = n > 0;
       if (wrote) {
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(192, 1) dkdv2_kernel(const __grid_constant__ B
         __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + j) * DV;
         __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + j) * DQK;
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV + DQK; c0 += 32) {
+        for (int c0 = grp * 32; c0 < DV + DQK; c0 += 64) {
           const bool isv = c0 < DV;
           uint32_t a[32];
           if (wrote) {
@@ -791,14 +793,14 @@ struct Dq2Cfg {
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
   enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DS, B_DQD, B_DONE,
          B_DRAIN, NBAR };
-  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
+  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + NBAR * 8 + 16 + 4096;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t ID_DQ = idesc_bf16(128, DQK, false, true);
 };
 
 template <int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ BwdParams p) {
   using C = Dq2Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -806,7 +808,7 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
   uint8_t* sG = sQ + C::QTILE;
   uint8_t* sK = sG + C::VTILE;             // [KST]
   uint8_t* sV = sK + C::KST * C::QTILE;    // [VST]
-  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 warps][2][128]
+  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [8 warps][2][64]
   uint64_t* bar = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -818,7 +820,7 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
   const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * 128;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, b == C::B_DS ? 128 : 1);
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, b == C::B_DS ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -932,6 +934,9 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
       }
     }
   } else {
+    // two warps per TMEM lane quarter; each thread owns one query row and half
+    // (64) of the 128 key columns of the tile
+    const int sw = warp - 2, grp = sw >> 2, cb = grp * 64;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int i = q0 + row;
@@ -948,10 +953,10 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
       int kv0;
       bool masked;
       if (!slot(s, &kv0, &masked)) continue;
-      float* ctw = colterm + (quarter * 2 + (n & 1)) * 128;
+      float* ctw = colterm + (sw * 2 + (n & 1)) * 64;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int jj = kv0 + e * 32 + lane;
+      for (int e = 0; e < 2; ++e) {
+        const int jj = kv0 + cb + e * 32 + lane;
         float c = 0.f;
         if (jj < p.Sk) c = ((kb ? __ldg(kb + jj) : 0.f) - p.mask.slope * (float)jj) * kLog2e;
         ctw[e * 32 + lane] = c;
@@ -963,22 +968,22 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
         break;
       }
       tc_fence_after();
-      uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      uint32_t kw[2] = {0xffffffffu, 0xffffffffu};
       if (keep) {
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int wi = (kv0 >> 5) + w;
+        for (int w = 0; w < 2; ++w) {
+          const int wi = ((kv0 + cb) >> 5) + w;
           kw[w] = wi < p.mask.nkw ? __ldg(keep + wi) : 0u;
         }
       }
-      const int clo = masked ? lo - kv0 : 0;
-      const int chi = masked ? min(hi, p.Sk - 1) - kv0 : 127;
-      uint32_t ds[64];
+      const int clo = masked ? lo - kv0 - cb : 0;
+      const int chi = masked ? min(hi, p.Sk - 1) - kv0 - cb : 63;
+      uint32_t ds[32];
 #pragma unroll
-      for (int qtr = 0; qtr < 4; ++qtr) {
+      for (int qtr = 0; qtr < 2; ++qtr) {
         uint32_t rs[32], rp[32];
-        tmem_ld32(tl + C::T_S + qtr * 32, rs);
-        tmem_ld32(tl + C::T_DP + qtr * 32, rp);
+        tmem_ld32(tl + C::T_S + cb + qtr * 32, rs);
+        tmem_ld32(tl + C::T_DP + cb + qtr * 32, rp);
         tmem_wait_ld32(rs);
         reg_fence32(rp);
         const float4* ct = reinterpret_cast<const float4*>(ctw + qtr * 32);
@@ -989,7 +994,7 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
           float d[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cl = 4 * c4 + e, c = qtr * 32 + cl;
+            const int cl = 4 * c4 + e, c = qtr * 32 + cl;  // column within this half
             const float x = __uint_as_float(rs[cl]);
             float t, dd = 1.f;
             if constexpr (CAP) {
@@ -1016,8 +1021,7 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
         }
         tc_fence_after();
       }
-      tmem_st32(tl + C::T_DS, ds);
-      tmem_st32(tl + C::T_DS + 32, ds + 32);
+      tmem_st32(tl + C::T_DS + grp * 32, ds);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_DS);
@@ -1027,11 +1031,12 @@ __global__ void __launch_bounds__(192, 1) dq2_kernel(const __grid_constant__ Bwd
       __nv_bfloat16* dst = p.dq + ((size_t)bh * p.Sq + i) * DQK;
       if (n == 0) {
         if (i < p.Sq)
-          for (int c = 0; c < DQK; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+          for (int c = grp * 32; c < DQK; c += 64)
+            for (int e = 0; e < 32; e += 8) *reinterpret_cast<uint4*>(dst + c + e) = make_uint4(0, 0, 0, 0);
       } else if (__all_sync(0xffffffffu, mbar_wait(bar + C::B_DONE, 0, abort_flag))) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
+        for (int c0 = grp * 32; c0 < DQK; c0 += 64) {
           uint32_t a[32];
           tmem_ld32(tl + C::T_DQ + c0, a);
           tmem_wait_ld32(a);
@@ -1078,10 +1083,10 @@ static int launch_bwd_main(const BwdParams& prm, const Shape& s, int determinist
   }
   static bool f2 = false, f3 = false;
   if (set_smem_once(dkdv2_kernel<DQK, DV, CAP>, Dkdv2Cfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
-  dkdv2_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 192, Dkdv2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  dkdv2_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 320, Dkdv2Cfg<DQK, DV>::SMEM, st>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
   if (set_smem_once(dq2_kernel<DQK, DV, CAP>, Dq2Cfg<DQK, DV>::SMEM, &f3)) return GBATTN_ERR_CUDA;
-  dq2_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 192, Dq2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  dq2_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 320, Dq2Cfg<DQK, DV>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

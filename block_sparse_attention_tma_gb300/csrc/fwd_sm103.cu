@@ -7,18 +7,22 @@
 // running max / sum update is the online-softmax merge of the POPCORNBENCH
 // "Kimi-K2.6 l1_p97" trace (m_new = max, rescale by exp(m_old - m_new)).
 //
-// One CTA = one (b, h, 128-row query tile); 6 warps:
+// One CTA = one (b, h, 128-row query tile); 10 warps:
 //   warp 0      TMA producer: Q once, then K and V tiles into rings.
 //   warp 1      MMA issuer (one thread): S = Q K^T with Q read from TMEM
 //               (A operand) and K from shared memory, into one of two TMEM S
 //               buffers; O += P V with P read from TMEM and V (MN-major) from
 //               shared memory.
-//   warps 2..5  softmax: thread = query row = TMEM lane. Copies its Q row
-//               into TMEM once; per tile loads its S row, masks (partial
-//               tiles only), folds scale * log2(e) and the per-key bias term
-//               into one FMA, exp2, writes P (bf16) back over the S buffer,
-//               and rescales O only when the row max grows by more than 2^8
-//               ("lazy" rescale); final O / l and LSE.
+//   warps 2..9  softmax, two warps per TMEM lane quarter: thread = (query
+//               row, half of the 128 key columns). Group 0 copies the Q rows
+//               into TMEM once. Per tile each thread loads its 64 S values,
+//               masks (partial tiles only), folds scale * log2(e) and the
+//               per-key bias term into one FMA, exchanges its partial row max
+//               with the other half through shared memory, exp2, writes its
+//               half of P (bf16) back over the S buffer, and rescales its half
+//               of O only when the row max grows by more than 2^8 ("lazy"
+//               rescale); final O / l and LSE. Two warps per SM sub-partition
+//               hide the latencies one warp alone cannot.
 // Keeping Q in TMEM means the QK^T MMA reads only K from shared memory; the
 // shared-memory traffic per tile (K + V reads, K + V TMA writes) then fits
 // the time of the two MMAs.
@@ -59,11 +63,14 @@ struct FwdCfg {
   static constexpr int T_O = 256, T_Q = 384;
   static_assert(T_Q + DQK / 2 <= 512 && T_O + DV <= T_Q, "TMEM budget");
   // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
-  // v_empty[VST], s_full[2], p_full[2], o_done, drain
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2], fin
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 2 + 1;
+  static constexpr int THREADS = 320;
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
-  static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + NBAR * 8 + 16 + 4096;
+  // colterm [8 warps][2][64] + row-max exchange [2][2][128] + row sums [2][128]
+  static constexpr int SMEM_USED =
+      1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 4 * 128 * 4 + 2 * 128 * 4 + NBAR * 8 + 16 + 4096;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
@@ -82,15 +89,17 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
 }
 
 template <int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sK = sQ + C::QTILE;
   uint8_t* sV = sK + C::KST * C::QTILE;
-  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 warps][2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
+  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [8 warps][2][64]
+  float* xmax = colterm + 8 * 128;                                     // [2][2 halves][128 rows]
+  float* xsum = xmax + 4 * 128;                                        // [2 halves][128 rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + 2 * 128);
   uint64_t* q_full = bars;
   uint64_t* q_tmem = q_full + 1;
   uint64_t* k_full = q_tmem + 1;
@@ -101,6 +110,8 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 1;
+  uint64_t* xbar = drain + 1;  // [2]
+  uint64_t* fin = xbar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -117,9 +128,10 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
     mbar_init(q_tmem, 128);
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 256); mbar_init(xbar + i, 256); }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(fin, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -240,9 +252,13 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;
+    const int sw = warp - 2;       // 0..7
+    const int grp = sw >> 2;       // which half of the key columns
+    const int quarter = warp & 3;  // TMEM lane quarter
     const int row = quarter * 32 + lane;
     const int i = q0 + row;
+    const int cb = grp * 64;       // first S column of this thread
+    constexpr int DVH = DV / 2;    // O columns of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     int lo, hi;
     row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     bool ok = true;
-    if (any_tile) {
+    if (any_tile && grp == 0) {
       // copy this thread's Q row from the swizzled smem tile into TMEM
       ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag));
       if (ok) {
@@ -259,8 +275,8 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
 #pragma unroll
         for (int u = 0; u < DQK / 8; ++u) {
           const int slab = u / (C::SWQ / 16), c16 = u % (C::SWQ / 16);
-          const int sw = (row * C::SWQ / 128) & (C::SWQ / 16 - 1);
-          const uint4 v = *reinterpret_cast<const uint4*>(sQ + slab * C::QSLAB + row * C::SWQ + ((c16 ^ sw) << 4));
+          const int swz = (row * C::SWQ / 128) & (C::SWQ / 16 - 1);
+          const uint4 v = *reinterpret_cast<const uint4*>(sQ + slab * C::QSLAB + row * C::SWQ + ((c16 ^ swz) << 4));
           qr[4 * u] = v.x;
           qr[4 * u + 1] = v.y;
           qr[4 * u + 2] = v.z;
@@ -282,12 +298,12 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
       bool masked;
       if (!slot(s, &kv0, &masked)) continue;
       const int sb = n & 1;
-      // per-key score term (key bias - slope * j) * log2(e); each warp keeps
-      // its own copy (4 keys per lane), so only a warp-level sync is needed
-      float* ctw = colterm + (quarter * 2 + sb) * 128;
+      // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
+      // columns; each warp keeps its own copy, so only a warp sync is needed
+      float* ctw = colterm + (sw * 2 + sb) * 64;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = kv0 + e * 32 + lane;
+      for (int e = 0; e < 2; ++e) {
+        const int j = kv0 + cb + e * 32 + lane;
         float c = 0.f;
         if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
         ctw[e * 32 + lane] = c;
@@ -299,12 +315,15 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
         break;
       }
       tc_fence_after();
-      float t[128];
-      tmem_ld128(tl + sb * 128, reinterpret_cast<uint32_t*>(t));
+      float t[64];
+      tmem_ld32(tl + sb * 128 + cb, reinterpret_cast<uint32_t*>(t));
+      tmem_ld32(tl + sb * 128 + cb + 32, reinterpret_cast<uint32_t*>(t) + 32);
+      tmem_wait_ld32(reinterpret_cast<uint32_t*>(t));
+      reg_fence32(reinterpret_cast<uint32_t*>(t) + 32);
       {
         const float4* ct = reinterpret_cast<const float4*>(ctw);
 #pragma unroll
-        for (int c4 = 0; c4 < 32; ++c4) {
+        for (int c4 = 0; c4 < 16; ++c4) {
           const float4 v4 = ct[c4];
           const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
@@ -316,33 +335,41 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
         }
       }
       if (masked) {
-        const int clo = lo - kv0;
-        const int chi = min(hi, p.Sk - 1) - kv0;
+        const int clo = lo - kv0 - cb;
+        const int chi = min(hi, p.Sk - 1) - kv0 - cb;
         if (keep) {
-          uint32_t kw[4];
+          uint32_t kw[2];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int wi = (kv0 >> 5) + w;
+          for (int w = 0; w < 2; ++w) {
+            const int wi = ((kv0 + cb) >> 5) + w;
             kw[w] = wi < p.mask.nkw ? __ldg(keep + wi) : 0u;
           }
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < 64; ++c) {
             const bool okc = (c >= clo) && (c <= chi) && ((kw[c >> 5] >> (c & 31)) & 1u);
             t[c] = okc ? t[c] : -INFINITY;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
         }
       }
-      // row max: 8 independent chains, then a short tree
+      // row max: 8 independent chains over this half, then the other half's
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = t[e];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], t[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], t[c]);
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float* xm = xmax + sb * 256;
+      xm[grp * 128 + row] = mt;
+      mbar_arrive(xbar + sb);
+      ok = mbar_wait(xbar + sb, (n >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      mt = fmaxf(mt, xm[(grp ^ 1) * 128 + row]);
       float m_use = m_run, alpha = 1.f;
       bool resc = false;
       if (mt > m_run + 8.0f) {
@@ -356,9 +383,9 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
       float ls[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float a0 = ex2(t[2 * c] - msafe);
         const float a1 = ex2(t[2 * c + 1] - msafe);
         ls[c & 7] += a0 + a1;
@@ -375,53 +402,76 @@ __global__ void __launch_bounds__(192, 1) fwd_bf16_kernel(const __grid_constant_
           break;
         }
         tc_fence_after();
+        if constexpr (DVH >= 32) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-          uint32_t orr[32];
-          tmem_ld32(tl + C::T_O + c0, orr);
-          tmem_wait_ld32(orr);
+          for (int c0 = 0; c0 < DVH; c0 += 32) {
+            uint32_t orr[32];
+            tmem_ld32(tl + C::T_O + grp * DVH + c0, orr);
+            tmem_wait_ld32(orr);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
-          tmem_st32(tl + C::T_O + c0, orr);
+            for (int c = 0; c < 32; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+            tmem_st32(tl + C::T_O + grp * DVH + c0, orr);
+          }
+        } else {
+          uint32_t orr[16];
+          tmem_ld16(tl + C::T_O + grp * DVH, orr);
+          tmem_wait_ld16(orr);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) orr[c] = __float_as_uint(__uint_as_float(orr[c]) * alpha);
+          tmem_st16(tl + C::T_O + grp * DVH, orr);
         }
       }
-      tmem_st32(tl + sb * 128 + 0, pk);
-      tmem_st32(tl + sb * 128 + 32, pk + 32);
+      tmem_st32(tl + sb * 128 + grp * 32, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + sb);
       ++n;
     }
-    // ---- epilogue
-    if (ok && i < p.Sq && (n == 0 || l_run == 0.f)) {
-      __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
+    // ---- epilogue: combine the two halves' row sums, normalise my O half
+    if (ok) {
+      float l_tot = 0.f;
+      if (n > 0) {
+        xsum[grp * 128 + row] = l_run;
+        mbar_arrive(fin);
+        ok = __all_sync(0xffffffffu, mbar_wait(fin, 0, abort_flag));
+        if (ok) l_tot = xsum[row] + xsum[128 + row];
+      }
+      if (ok) {
+        const bool live = n > 0 && l_tot > 0.f;
+        __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV + grp * DVH;
+        if (!live && i < p.Sq) {
 #pragma unroll
-      for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-      if (p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
-    }
-    if (ok && n > 0) {
-      if (__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
-        tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV;
-#pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-          uint32_t orr[32];
-          tmem_ld32(tl + C::T_O + c0, orr);
-          tmem_wait_ld32(orr);
-          if (i < p.Sq && l_run > 0.f) {
-            uint32_t pkd[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              pkd[c] = pack_bf16(__uint_as_float(orr[2 * c]) * inv, __uint_as_float(orr[2 * c + 1]) * inv);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              *reinterpret_cast<uint4*>(orow + c0 + 8 * c) =
-                  make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
-          }
+          for (int c = 0; c < DVH; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          if (grp == 0 && p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
         }
-        if (i < p.Sq && l_run > 0.f && p.lse)
-          p.lse[(size_t)bh * p.Sq + i] = (m_run + __log2f(l_run)) * kLn2 + p.mask.slope * (float)i;
+        if (n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
+          tc_fence_after();
+          const float inv = live ? 1.f / l_tot : 0.f;
+          constexpr int CH = DVH >= 32 ? 32 : 16;
+#pragma unroll 1
+          for (int c0 = 0; c0 < DVH; c0 += CH) {
+            uint32_t orr[CH];
+            if constexpr (CH == 32) {
+              tmem_ld32(tl + C::T_O + grp * DVH + c0, orr);
+              tmem_wait_ld32(orr);
+            } else {
+              tmem_ld16(tl + C::T_O + grp * DVH + c0, orr);
+              tmem_wait_ld16(orr);
+            }
+            if (i < p.Sq && live) {
+              uint32_t pkd[CH / 2];
+#pragma unroll
+              for (int c = 0; c < CH / 2; ++c)
+                pkd[c] = pack_bf16(__uint_as_float(orr[2 * c]) * inv, __uint_as_float(orr[2 * c + 1]) * inv);
+#pragma unroll
+              for (int c = 0; c < CH / 8; ++c)
+                *reinterpret_cast<uint4*>(orow + c0 + 8 * c) =
+                    make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+            }
+          }
+          if (grp == 0 && i < p.Sq && live && p.lse)
+            p.lse[(size_t)bh * p.Sq + i] = (m_run + __log2f(l_tot)) * kLn2 + p.mask.slope * (float)i;
+        }
       }
     }
   }
@@ -442,7 +492,7 @@ static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
       return GBATTN_ERR_CUDA;
     attr_set = true;
   }
-  kern<<<grid, 192, C::SMEM, st>>>(prm);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

@@ -462,7 +462,9 @@ struct Dkdv2Cfg {
   static_assert(192 + DV + DQK <= 512, "TMEM budget");
   enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_P, B_DP, B_DVD,
          B_DS, B_DKD, B_DONE, B_DRAIN, NBAR };
-  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + NBAR * 8 + 16 + 4096;
+  static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
+  static constexpr int SMEM_USED =
+      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + TCAP * 2 + NBAR * 8 + 16 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
   static constexpr uint32_t ID_DV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
@@ -479,25 +481,16 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
   uint8_t* sQ = sV + C::VTILE;                  // [QST]
   uint8_t* sG = sQ + C::QST * C::QTILE;         // [GST]
   float* sLD = reinterpret_cast<float*>(sG + C::GST * C::VTILE);  // [QST][lse2 128 | delta 128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sLD + C::QST * 256);
+  uint16_t* tlist = reinterpret_cast<uint16_t*>(sLD + C::QST * 256);  // [TCAP]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int bh = blockIdx.x % BH;
   const int k0 = (blockIdx.x / BH) * 128;
-
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 256 : 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   TileWalk walk;
   int nslots;
@@ -511,16 +504,28 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
     return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, q0, masked)
                        : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, q0, masked);
   };
+  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (threadIdx.x == 32) {
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 256 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = *tcount;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int n = 0, nq = 0, ng = 0;
       bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int q0;
-        bool masked;
-        if (!slot(s, &q0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int q0;
+      bool masked;
+      while (ok && it.next(&q0, &masked)) {
         if (n == 0) {
           mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
@@ -553,35 +558,41 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), qa = smem_u32(sQ), ga = smem_u32(sG);
+      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));     // K, K-major
+      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));     // Q, K-major
+      const SDesc qm = make_sdesc(smem_u32(sQ), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // Q, MN-major
+      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));     // V, K-major
+      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));     // dO, K-major
+      const SDesc gm = make_sdesc(smem_u32(sG), C::VSLAB, 8 * C::SWV, swz_code(C::SWV));  // dO, MN-major
       auto issue_dk = [&](int j) {
         const int qs = j % C::QST;
+        const uint32_t blo = qm.lo + ((qs * C::QTILE) >> 4);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_X + kk * 8,
-                  sdesc(qa + qs * C::QTILE + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DK,
-                  (j > 0 || kk > 0));
+          mma_ts(tmem + C::T_DK, tmem + C::T_X + kk * 8, blo + mnmajor_step(kk, C::SWQ), qm.hi, C::ID_DK,
+                 kk > 0 ? 1u : acc0);
         umma_commit(bar + C::B_DKD);
         umma_commit(bar + C::B_QE + qs);
       };
       int n = 0;
       bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int q0;
-        bool masked;
-        if (!slot(s, &q0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int q0;
+      bool masked;
+      while (ok && it.next(&q0, &masked)) {
         if (n == 0 && !(ok = mbar_wait(bar + C::B_KV, 0, abort_flag))) break;
         const int qs = n % C::QST;
         if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
         // R is free once the dS warps have read dP^T of the previous tile
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
         tc_fence_after();
+        {
+          const uint32_t blo = qd.lo + ((qs * C::QTILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWQ / 2), off = (kk * 32) % C::SWQ;
-          umma_ss(tmem + C::T_R, sdesc(ka + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)),
-                  sdesc(qa + qs * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_ST,
-                  kk > 0);
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            mma_ss(tmem + C::T_R, kd.lo + kmajor_step(kk, C::SWQ, C::QSLAB), kd.hi,
+                   blo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
         if (n >= 1) issue_dk(n - 1);
@@ -589,19 +600,22 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
         const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
         tc_fence_after();
+        {
+          const uint32_t blo = gd.lo + ((gs * C::VTILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWV / 2), off = (kk * 32) % C::SWV;
-          umma_ss(tmem + C::T_R, sdesc(va + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)),
-                  sdesc(ga + gs * C::VTILE + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_ST,
-                  kk > 0);
+          for (int kk = 0; kk < DV / 16; ++kk)
+            mma_ss(tmem + C::T_R, vd.lo + kmajor_step(kk, C::SWV, C::VSLAB), vd.hi,
+                   blo + kmajor_step(kk, C::SWV, C::VSLAB), gd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_DP);
+        {
+          const uint32_t blo = gm.lo + ((gs * C::VTILE) >> 4);
+          const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_X + kk * 8,
-                  sdesc(ga + gs * C::VTILE + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV)), C::ID_DV,
-                  (n > 0 || kk > 0));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::T_DV, tmem + C::T_X + kk * 8, blo + mnmajor_step(kk, C::SWV), gm.hi, C::ID_DV,
+                   kk > 0 ? 1u : acc0);
+        }
         umma_commit(bar + C::B_DVD);
         umma_commit(bar + C::B_GE + gs);
         ++n;
@@ -635,10 +649,10 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
     const float kt = (kb - p.mask.slope * (float)j) * kLog2e;  // per-key score term, log2 units
     int n = 0;
     bool ok = true;
-    for (int s = 0; s < nslots && ok; ++s) {
-      int q0;
-      bool masked;
-      if (!slot(s, &q0, &masked)) continue;
+    auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+    int q0;
+    bool masked;
+    while (ok && it.next(&q0, &masked)) {
       const int qs = n % C::QST;
       ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
       if (ok) ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag);  // lse2 / delta landed
@@ -793,7 +807,9 @@ struct Dq2Cfg {
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
   enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DS, B_DQD, B_DONE,
          B_DRAIN, NBAR };
-  static constexpr int SMEM_USED = 1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + NBAR * 8 + 16 + 4096;
+  static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
+  static constexpr int SMEM_USED =
+      1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + TCAP * 2 + NBAR * 8 + 16 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t ID_DQ = idesc_bf16(128, DQK, false, true);
@@ -809,26 +825,17 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
   uint8_t* sK = sG + C::VTILE;             // [KST]
   uint8_t* sV = sK + C::KST * C::QTILE;    // [VST]
   float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [8 warps][2][64]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(colterm + 8 * 128);
+  uint16_t* tlist = reinterpret_cast<uint16_t*>(colterm + 8 * 128);  // [TCAP]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqt = (p.Sq + 127) / 128;
   const int bh = blockIdx.x % BH;
   const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * 128;
-
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, b == C::B_DS ? 256 : 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   TileWalk walk;
   int nslots;
@@ -842,15 +849,27 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
     return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
                        : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
   };
+  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (threadIdx.x == 32) {
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, b == C::B_DS ? 256 : 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = *tcount;
 
   if (warp == 0) {
     if (lane == 0) {
       int n = 0, nk = 0, nv = 0;
       bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int kv0;
-        bool masked;
-        if (!slot(s, &kv0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int kv0;
+      bool masked;
+      while (ok && it.next(&kv0, &masked)) {
         if (n == 0) {
           mbar_expect_tx(bar + C::B_QG, C::QTILE + C::VTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
@@ -880,23 +899,28 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t qa = smem_u32(sQ), ga = smem_u32(sG), ka = smem_u32(sK), va = smem_u32(sV);
+      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));     // Q, K-major
+      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));     // dO, K-major
+      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));     // K, K-major
+      const SDesc km = make_sdesc(smem_u32(sK), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // K, MN-major
+      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));     // V, K-major
       auto issue_dq = [&](int jt) {
         const int ks = jt % C::KST;
+        const uint32_t blo = km.lo + ((ks * C::QTILE) >> 4);
+        const uint32_t acc0 = jt > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::T_DQ, tmem + C::T_DS + kk * 8,
-                  sdesc(ka + ks * C::QTILE + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DQ,
-                  (jt > 0 || kk > 0));
+          mma_ts(tmem + C::T_DQ, tmem + C::T_DS + kk * 8, blo + mnmajor_step(kk, C::SWQ), km.hi, C::ID_DQ,
+                 kk > 0 ? 1u : acc0);
         umma_commit(bar + C::B_DQD);
         umma_commit(bar + C::B_KE + ks);
       };
       int n = 0;
       bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int kv0;
-        bool masked;
-        if (!slot(s, &kv0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int kv0;
+      bool masked;
+      while (ok && it.next(&kv0, &masked)) {
         if (n == 0 && !(ok = mbar_wait(bar + C::B_QG, 0, abort_flag))) break;
         const int ks = n % C::KST, vs = n % C::VST;
         if (!(ok = mbar_wait(bar + C::B_KF + ks, (n / C::KST) & 1, abort_flag))) break;
@@ -904,17 +928,19 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
         // S / dP buffers are free once the dS warps have read the previous tile
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
         tc_fence_after();
+        {
+          const uint32_t blo = kd.lo + ((ks * C::QTILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWQ / 2), off = (kk * 32) % C::SWQ;
-          umma_ss(tmem + C::T_S, sdesc(qa + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)),
-                  sdesc(ka + ks * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_S, kk > 0);
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            mma_ss(tmem + C::T_S, qd.lo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi,
+                   blo + kmajor_step(kk, C::SWQ, C::QSLAB), kd.hi, C::ID_S, kk > 0 ? 1u : 0u);
         }
+        {
+          const uint32_t blo = vd.lo + ((vs * C::VTILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWV / 2), off = (kk * 32) % C::SWV;
-          umma_ss(tmem + C::T_DP, sdesc(ga + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)),
-                  sdesc(va + vs * C::VTILE + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_S, kk > 0);
+          for (int kk = 0; kk < DV / 16; ++kk)
+            mma_ss(tmem + C::T_DP, gd.lo + kmajor_step(kk, C::SWV, C::VSLAB), gd.hi,
+                   blo + kmajor_step(kk, C::SWV, C::VSLAB), vd.hi, C::ID_S, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
         umma_commit(bar + C::B_VE + vs);
@@ -949,10 +975,10 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
     const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
     int n = 0;
     bool ok = true;
-    for (int s = 0; s < nslots && ok; ++s) {
-      int kv0;
-      bool masked;
-      if (!slot(s, &kv0, &masked)) continue;
+    auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+    int kv0;
+    bool masked;
+    while (ok && it.next(&kv0, &masked)) {
       float* ctw = colterm + (sw * 2 + (n & 1)) * 64;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {

@@ -176,6 +176,51 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Shared-memory matrix descriptor kept as two 32-bit halves. Successive MMA
+// k-steps only move the start address (low 14 bits of lo), so an issue loop
+// adds a compile-time byte offset >> 4 to lo and reuses hi: no 64-bit
+// arithmetic on the issuing thread's critical path.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  SDesc d;
+  d.lo = ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+  d.hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (swz << 29);
+  return d;
+}
+// D(tmem) (+)= A(smem) * B(smem); a/b given as descriptor halves.
+__device__ __forceinline__ void mma_ss(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                       uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem).
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// K-major operand tile of 128 rows x K (bf16) in `sw`-byte swizzled slabs of
+// 128 rows; step kk (16 elements) starts at slab (kk*16)/(sw/2), byte
+// (kk*32) % sw. Returns the descriptor-lo increment (bytes >> 4) of step kk.
+__host__ __device__ constexpr uint32_t kmajor_step(int kk, int sw, int slab_bytes) {
+  return (uint32_t)((((kk * 16) / (sw / 2)) * slab_bytes + (kk * 32) % sw) >> 4);
+}
+// MN-major operand: step kk covers 16 K-rows of `sw` bytes each.
+__host__ __device__ constexpr uint32_t mnmajor_step(int kk, int sw) { return (uint32_t)((kk * 16 * sw) >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B
 // format, 15/16 A/B major (1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.

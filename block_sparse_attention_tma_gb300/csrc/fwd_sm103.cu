@@ -69,8 +69,9 @@ struct FwdCfg {
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
   // colterm [8 warps][2][64] + row-max exchange [2][2][128] + row sums [2][128]
-  static constexpr int SMEM_USED =
-      1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 4 * 128 * 4 + 2 * 128 * 4 + NBAR * 8 + 16 + 4096;
+  static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
+  static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 4 * 128 * 4 + 2 * 128 * 4 +
+                                   TCAP * 2 + NBAR * 8 + 16 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
@@ -99,7 +100,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [8 warps][2][64]
   float* xmax = colterm + 8 * 128;                                     // [2][2 halves][128 rows]
   float* xsum = xmax + 4 * 128;                                        // [2 halves][128 rows]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xsum + 2 * 128);
+  uint16_t* tlist = reinterpret_cast<uint16_t*>(xsum + 2 * 128);  // [TCAP]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint64_t* q_full = bars;
   uint64_t* q_tmem = q_full + 1;
   uint64_t* k_full = q_tmem + 1;
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   uint64_t* fin = xbar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -123,7 +126,22 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   const int bh = L % BH;
   const int q0 = qt * 128;
 
-  if (threadIdx.x == 0) {
+  // Tile walk of this CTA; warp 0 compacts it into shared memory once.
+  TileWalk walk;
+  int nslots;
+  if (p.has_lists) {
+    const int r = q0 / p.sparse_m;
+    walk = make_walk(p.mcnt, p.midx, p.fcnt, p.fidx, bh * p.nqb + r, p.nkb, p.sub, p.Sk);
+    nslots = walk.nslots;
+  } else {
+    nslots = (p.Sk + 127) / 128;
+  }
+  auto slot = [&](int s, int* kv0, bool* masked) -> bool {
+    return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
+                       : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
+  };
+  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (threadIdx.x == 32) {
     mbar_init(q_full, 1);
     mbar_init(q_tmem, 128);
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
@@ -140,32 +158,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  // Tile walk of this CTA (identical in every role).
-  TileWalk walk;
-  int nslots;
-  if (p.has_lists) {
-    const int r = q0 / p.sparse_m;
-    walk = make_walk(p.mcnt, p.midx, p.fcnt, p.fidx, bh * p.nqb + r, p.nkb, p.sub, p.Sk);
-    nslots = walk.nslots;
-  } else {
-    nslots = (p.Sk + 127) / 128;
-  }
-  auto slot = [&](int s, int* kv0, bool* masked) -> bool {
-    return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
-                       : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
-  };
-  // First slot this CTA visits (every role computes the same answer).
-  int first = nslots;
-  for (int s = 0; s < nslots; ++s) {
-    int kv0;
-    bool masked;
-    if (slot(s, &kv0, &masked)) {
-      first = s;
-      break;
-    }
-  }
-  const bool any_tile = first < nslots;
+  const int ntiles = *tcount;
+  const bool any_tile = ntiles > 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -177,10 +171,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
       int n = 0, nk = 0, nv = 0;
       bool ok = true;
-      for (int s = first; s < nslots && ok; ++s) {
-        int kv0;
-        bool masked;
-        if (!slot(s, &kv0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int kv0;
+      bool masked;
+      while (ok && it.next(&kv0, &masked)) {
         const int ks = n % C::KST;
         if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
         mbar_expect_tx(k_full + ks, C::QTILE);
@@ -205,40 +199,39 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && any_tile) {
-      const uint32_t ka = smem_u32(sK), va = smem_u32(sV);
+      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));
+      const SDesc vd = make_sdesc(smem_u32(sV), C::VSLAB, 8 * C::SWV, swz_code(C::SWV));
       auto issue_pv = [&](int j) -> bool {
         const int sb = j & 1;
         if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
         const int vs = j % C::VST;
         if (!mbar_wait(v_full + vs, (j / C::VST) & 1, abort_flag)) return false;
         tc_fence_after();
+        // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows
+        const uint32_t vlo = vd.lo + ((vs * C::VTILE) >> 4);
+        const uint32_t pa = tmem + sb * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows
-          const uint64_t bd = sdesc(va + vs * C::VTILE + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV));
-          umma_ts(tmem + C::T_O, tmem + sb * 128 + kk * 8, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::T_O, pa + kk * 8, vlo + mnmajor_step(kk, C::SWV), vd.hi, C::IDESC_PV, kk > 0 ? 1u : acc0);
         umma_commit(v_empty + vs);
         umma_commit(o_done);
         return true;
       };
       int n = 0;
       bool ok = mbar_wait(q_tmem, 0, abort_flag);
-      for (int s = first; s < nslots && ok; ++s) {
-        int kv0;
-        bool masked;
-        if (!slot(s, &kv0, &masked)) continue;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int kv0;
+      bool masked;
+      while (ok && it.next(&kv0, &masked)) {
         const int ks = n % C::KST;
         if (!(ok = mbar_wait(k_full + ks, (n / C::KST) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + (n & 1) * 128;
+        const uint32_t klo = kd.lo + ((ks * C::QTILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWQ / 2);
-          const int off = (kk * 32) % C::SWQ;
-          const uint64_t bd = sdesc(ka + ks * C::QTILE + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ));
-          umma_ts(d, tmem + C::T_Q + kk * 8, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          mma_ts(d, tmem + C::T_Q + kk * 8, klo + kmajor_step(kk, C::SWQ, C::QSLAB), kd.hi, C::IDESC_S, kk > 0 ? 1u : 0u);
         umma_commit(k_empty + ks);
         umma_commit(s_full + (n & 1));
         if (n >= 1 && !(ok = issue_pv(n - 1))) break;
@@ -293,10 +286,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         mbar_arrive(q_tmem);
       }
     }
-    for (int s = first; s < nslots && ok; ++s) {
-      int kv0;
-      bool masked;
-      if (!slot(s, &kv0, &masked)) continue;
+    auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+    int kv0;
+    bool masked;
+    while (ok && it.next(&kv0, &masked)) {
       const int sb = n & 1;
       // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
       // columns; each warp keeps its own copy, so only a warp sync is needed

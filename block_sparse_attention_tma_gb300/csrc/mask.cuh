@@ -180,4 +180,50 @@ __device__ __forceinline__ bool dense_slot(int s, const MaskParams& m, bool forw
   return true;
 }
 
+// The visited tiles of a CTA, computed once into shared memory by one warp
+// (32 slots at a time, compacted in slot order), so that every role reads its
+// next tile with one shared load. Entry = (start / 128) << 1 | masked. If a
+// CTA visits more than `cap` tiles the roles walk the slots themselves.
+template <class SlotFn>
+__device__ __forceinline__ void build_tile_list(SlotFn slot, int nslots, uint16_t* list, int cap, int* count) {
+  const int lane = threadIdx.x & 31;
+  int cnt = 0;
+  for (int s0 = 0; s0 < nslots; s0 += 32) {
+    const int s = s0 + lane;
+    int st = 0;
+    bool mk = false;
+    const bool v = (s < nslots) && slot(s, &st, &mk);
+    const unsigned b = __ballot_sync(0xffffffffu, v);
+    const int pos = cnt + __popc(b & ((1u << lane) - 1u));
+    if (v && pos < cap) list[pos] = (uint16_t)(((st >> 7) << 1) | (mk ? 1 : 0));
+    cnt += __popc(b);
+  }
+  if (lane == 0) *count = cnt;
+}
+
+template <class SlotFn>
+struct TileSeq {
+  const uint16_t* list;
+  int count, use_list, nslots, s, t;
+  SlotFn slot;
+  __device__ __forceinline__ bool next(int* start, bool* masked) {
+    if (use_list) {
+      if (t >= count) return false;
+      const uint32_t e = list[t++];
+      *start = (int)(e >> 1) * 128;
+      *masked = (e & 1u) != 0;
+      return true;
+    }
+    while (s < nslots) {
+      if (slot(s++, start, masked)) return true;
+    }
+    return false;
+  }
+};
+template <class SlotFn>
+__device__ __forceinline__ TileSeq<SlotFn> tile_seq(SlotFn slot, const uint16_t* list, int count, int cap,
+                                                    int nslots) {
+  return TileSeq<SlotFn>{list, count, count <= cap ? 1 : 0, nslots, 0, 0, slot};
+}
+
 }  // namespace gb

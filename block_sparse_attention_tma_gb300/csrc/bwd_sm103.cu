@@ -663,36 +663,48 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
       tc_fence_after();
       const float* sl = sLD + qs * 256;
       const float* sd = sl + 128;
-      const int clo = masked ? (kept ? ilo - q0 : 128) : 0;
-      const int chi = masked ? ihi - q0 : 127;
+      // P^T = exp2(S^T * scale * log2e + key term - lse2[q]), two 32-column halves
       uint32_t pk[32], dc[CAP ? 32 : 1];
+      const int clo = masked ? (kept ? ilo - q0 : 128) - cb : 0;
+      const int chi = masked ? ihi - q0 - cb : 63;
 #pragma unroll
-      for (int qtr = 0; qtr < 2; ++qtr) {
+      for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
-        tmem_ld32(tl + C::T_R + cb + qtr * 32, r);
+        tmem_ld32(tl + C::T_R + cb + hh * 32, r);
         tmem_wait_ld32(r);
+        const float4* sl4 = reinterpret_cast<const float4*>(sl + cb + hh * 32);
+        float pf[32];
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          float pr[2], dd[2];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = sl4[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float dd[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cl = 2 * c2 + e, c = cb + qtr * 32 + cl;
-            const float x = __uint_as_float(r[cl]);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const float x = __uint_as_float(r[c]);
             float t;
-            dd[e] = 1.f;
             if constexpr (CAP) {
               const float th = tanh_fast(x * p.cap_pre);
-              t = p.cap_post * th;
+              t = fmaf(p.cap_post, th, kt);
               dd[e] = 1.f - th * th;
             } else {
-              t = x * p.scale_log2;
+              t = fmaf(x, p.scale_log2, kt);
+              dd[e] = 1.f;
             }
-            const float v = ex2(t + kt - sl[c]);
-            pr[e] = (c >= clo && c <= chi) ? v : 0.f;
+            pf[c] = ex2(t - lv[e]);
           }
-          pk[qtr * 16 + c2] = pack_bf16(pr[0], pr[1]);
-          if constexpr (CAP) dc[qtr * 16 + c2] = pack_bf16(dd[0], dd[1]);
+          if constexpr (CAP) {
+            dc[hh * 16 + 2 * c4] = pack_bf16(dd[0], dd[1]);
+            dc[hh * 16 + 2 * c4 + 1] = pack_bf16(dd[2], dd[3]);
+          }
         }
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pf[c] = (hh * 32 + c >= clo && hh * 32 + c <= chi) ? pf[c] : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[hh * 16 + c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
       }
       // X still holds dS^T of the previous tile until its dK MMA completes
       if (n >= 1) {
@@ -707,7 +719,7 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_P);
-      // dP^T -> dS^T
+      // dP^T -> dS^T = P^T (dP^T - delta[q])
       ok = mbar_wait(bar + C::B_DP, n & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -716,21 +728,27 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
       tc_fence_after();
       uint32_t ds[32];
 #pragma unroll
-      for (int qtr = 0; qtr < 2; ++qtr) {
+      for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
-        tmem_ld32(tl + C::T_R + cb + qtr * 32, r);
+        tmem_ld32(tl + C::T_R + cb + hh * 32, r);
         tmem_wait_ld32(r);
+        const float4* sd4 = reinterpret_cast<const float4*>(sd + cb + hh * 32);
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const int c = cb + qtr * 32 + 2 * c2;
-          const uint32_t pw = pk[qtr * 16 + c2];
-          float d0 = bf_lo(pw) * (__uint_as_float(r[2 * c2]) - sd[c]);
-          float d1 = bf_hi(pw) * (__uint_as_float(r[2 * c2 + 1]) - sd[c + 1]);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = sd4[c4];
+          const uint32_t p01 = pk[hh * 16 + 2 * c4], p23 = pk[hh * 16 + 2 * c4 + 1];
+          float d0 = bf_lo(p01) * (__uint_as_float(r[4 * c4 + 0]) - d4.x);
+          float d1 = bf_hi(p01) * (__uint_as_float(r[4 * c4 + 1]) - d4.y);
+          float d2 = bf_lo(p23) * (__uint_as_float(r[4 * c4 + 2]) - d4.z);
+          float d3 = bf_hi(p23) * (__uint_as_float(r[4 * c4 + 3]) - d4.w);
           if constexpr (CAP) {
-            d0 *= bf_lo(dc[qtr * 16 + c2]);
-            d1 *= bf_hi(dc[qtr * 16 + c2]);
+            d0 *= bf_lo(dc[hh * 16 + 2 * c4]);
+            d1 *= bf_hi(dc[hh * 16 + 2 * c4]);
+            d2 *= bf_lo(dc[hh * 16 + 2 * c4 + 1]);
+            d3 *= bf_hi(dc[hh * 16 + 2 * c4 + 1]);
           }
-          ds[qtr * 16 + c2] = pack_bf16(d0, d1);
+          ds[hh * 16 + 2 * c4] = pack_bf16(d0, d1);
+          ds[hh * 16 + 2 * c4 + 1] = pack_bf16(d2, d3);
         }
       }
       // X holds P^T until the dV MMA completes
@@ -1013,14 +1031,14 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
         tmem_wait_ld32(rs);
         reg_fence32(rp);
         const float4* ct = reinterpret_cast<const float4*>(ctw + qtr * 32);
+        float d[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 v4 = ct[c4];
           const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
-          float d[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cl = 4 * c4 + e, c = qtr * 32 + cl;  // column within this half
+            const int cl = 4 * c4 + e;
             const float x = __uint_as_float(rs[cl]);
             float t, dd = 1.f;
             if constexpr (CAP) {
@@ -1030,13 +1048,19 @@ __global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ Bwd
             } else {
               t = fmaf(x, p.scale_log2, cv[e]);
             }
-            const bool al = c >= clo && c <= chi && ((kw[c >> 5] >> (c & 31)) & 1u);
-            const float pv = al ? ex2(t - l2) : 0.f;
-            d[e] = pv * (__uint_as_float(rp[cl]) - dl) * dd;
+            d[cl] = ex2(t - l2) * (__uint_as_float(rp[cl]) - dl) * dd;
           }
-          ds[qtr * 16 + 2 * c4] = pack_bf16(d[0], d[1]);
-          ds[qtr * 16 + 2 * c4 + 1] = pack_bf16(d[2], d[3]);
         }
+        if (masked) {
+#pragma unroll
+          for (int cl = 0; cl < 32; ++cl) {
+            const int c = qtr * 32 + cl;  // column within this half
+            const bool al = c >= clo && c <= chi && ((kw[c >> 5] >> (c & 31)) & 1u);
+            d[cl] = al ? d[cl] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) ds[qtr * 16 + c2] = pack_bf16(d[2 * c2], d[2 * c2 + 1]);
       }
       // the dS columns still feed the dQ MMA of the previous tile
       if (n >= 1) {

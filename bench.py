@@ -4,8 +4,8 @@
 One step = every row of the path on its workload:
   * 16K block-sparse causal MLA prefill: B=1, H=16, Sq=Sk=16384, Dqk=192,
     Dv=128, bf16, 256 x 512 sparse tiles, rel bias 0.01 (q - kv):
-    build_block_mask -> attn_fwd -> attn_bwd (preprocess, dK/dV kernel,
-    query-parallel dQ kernel; --bwd atomic selects fp32-atomic dQ instead).
+    build_block_mask -> attn_fwd -> attn_bwd (preprocess, key-parallel dK/dV
+    kernel, query-parallel dQ kernel).
   * split-KV decode: B=32, H=32, Sq=1, Sk=65536, D=128, bf16, once per split
     count in {1, 2, 4, 8, 16} (partial + combine).
 `value` is the prefill forward+backward throughput in TFLOP/s counting only
@@ -158,7 +158,6 @@ def run_ours(args, rank, world, local_rank):
     dws = torch.empty(max(ga.attn_fwd_splitkv_workspace_bytes(D["B"], D["H"], D["Sq"], D["D"], n)
                           for n in D["splits"]), dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream(dev)
-    det = args.bwd == "deterministic"
     do_prefill = args.only in ("all", "prefill")
     do_decode = args.only in ("all", "decode")
     names = (["mask", "fwd", "bwd"] if do_prefill else []) + ([f"dec{n}" for n in D["splits"]] if do_decode else [])
@@ -183,8 +182,8 @@ def run_ours(args, rank, world, local_rank):
             mark()
             ga.attn_fwd(g["q"], g["k"], g["v"], 0.0, spec, lists, o=o, lse=lse)
             mark()
-            ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists, deterministic=det, dq=dq, dk=dk,
-                        dv=dv, workspace=ws)
+            ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists, dq=dq, dk=dk, dv=dv,
+                        workspace=ws)
             mark()
         if do_decode:
             for n in D["splits"]:
@@ -268,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
     roof["kernel"] = dom
     roof["share_of_step"] = round(share[dom] / sum(per.values()), 4)
     roof["peak_source"] = f"{peaks['source']} ({'sustained bf16' if roof['unit'] == 'TFLOP/s' else 'hbm copy'})"
-    launches_per_step = 2 + 1 + 3 + sum(1 if n == 1 else 2 for n in D["splits"])
+    launches_per_step = 2 + 1 + 3 + sum(1 if n == 1 else 2 for n in D["splits"])  # lists 2, fwd 1, bwd 3
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
@@ -278,7 +277,6 @@ def run_ours(args, rank, world, local_rank):
                               "kernel tiles 128x128, rel bias 0.01(q-kv)",
                    "decode": "B=32 H=32 Sq=1 Sk=65536 D=128 bf16, splits 1,2,4,8,16",
                    "parallelism": f"replicas x{world} (independent heads per rank, no collective)",
-                   "bwd": args.bwd,
                    "l2": "inputs larger than L2 (0.34 GB prefill + 34.4 GB decode per step); no flush"},
         "fwd_tflops": round(fwd_f / (per["fwd"] * 1e-3) / 1e12, 2),
         "bwd_tflops": round(bwd_f / (per["bwd"] * 1e-3) / 1e12, 2),
@@ -327,8 +325,7 @@ def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
             d_in[n].copy_(h_in[n], non_blocking=True)
         ga.build_block_mask(B, H, S, S, spec, lists)
         ga.attn_fwd(d_in["q"], d_in["k"], d_in["v"], 0.0, spec, lists, o=o, lse=lse)
-        ga.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse, 0.0, spec, lists,
-                    deterministic=args.bwd == "deterministic", dq=dq, dk=dk, dv=dv,
+        ga.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse, 0.0, spec, lists, dq=dq, dk=dk, dv=dv,
                     workspace=ws)
         for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
             h_out[n].copy_(t, non_blocking=True)
@@ -445,8 +442,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
     ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
-    ap.add_argument("--bwd", choices=["deterministic", "atomic"], default="deterministic",
-                    help="dQ by the query-parallel kernel (default, bitwise reproducible) or by fp32 atomics")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time one part only (profiling runs); prints a short line, not the bench line")
     ap.add_argument("--decode-sk", type=int, default=DECODE["Sk"], help="decode keys (profiling runs only)")

@@ -15,7 +15,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t bwd_workspace_bytes(const Shape& s) {
   const size_t BH = (size_t)s.B * s.H;
   const size_t sq_pad = align_up((size_t)s.Sq, 128);
-  return align_up(BH * s.Sq * s.Dqk * sizeof(float), 256) + 2 * align_up(BH * sq_pad * sizeof(float), 256);
+  return 2 * align_up(BH * sq_pad * sizeof(float), 256);
 }
 
 namespace {
@@ -281,7 +281,7 @@ int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
   const float sc = resolve_scale(scale, Dqk);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GBATTN_BF16)
-    return bwd_bf16_launch(s, q, k, v, o, dout, lse, sc, hm, deterministic, dq, dk, dv, workspace, st);
+    return bwd_bf16_launch(s, q, k, v, o, dout, lse, sc, hm, dq, dk, dv, workspace, st);
   return bwd_fp32_launch(s, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
                          static_cast<const float*>(o), static_cast<const float*>(dout), lse, sc, hm,
                          static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv), workspace, st);

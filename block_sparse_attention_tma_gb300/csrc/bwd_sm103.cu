@@ -6,19 +6,21 @@
 // lists of q-blocks, sub-tiled to 128 x 128 kernel tiles; QK/V dims 192/128;
 // the rel-bias score_mod passes the gradient through unchanged).
 //
-// Kernels:
+// Kernels (the score matrix never reaches memory; dQ needs no atomics, so
+// every gradient is bitwise reproducible):
 //   bwd_pre      delta_i = sum_d dO_id O_id; lse2_i = LSE_i log2(e) - (row part
 //                of the rel bias) in log2 units (+inf for rows with no key or
 //                padding rows, so that their P is exactly 0).
-//   dkdv         CTA = (b, h, 128-key tile). For each listed 128-row query
-//                tile: S^T = K Q^T and dP^T = V dO^T (TMEM), P^T and dS^T =
-//                P^T (dP^T - delta) by the thread owning the key row, dV +=
-//                P^T dO (P^T read from TMEM), dK += dS^T Q (dS^T from smem)
-//                and, unless deterministic, dQ_tile = dS K added into an fp32
-//                accumulator with vector atomics.
-//   dq           (deterministic) CTA = (b, h, 128-row query tile): S, dP,
-//                dS = P (dP - delta), dQ += dS K; no atomics.
-//   dq_convert   dQ = bf16(scale * accumulator).
+//   dkdv         CTA = (b, h, 128-key tile), walking the backward lists over
+//                128-row query tiles: S^T = K Q^T and dP^T = V dO^T in TMEM,
+//                P^T and dS^T = P^T (dP^T - delta) by the threads owning the
+//                key rows, dV += P^T dO and dK += dS^T Q with P^T / dS^T read
+//                from TMEM as the A operand.
+//   dq           CTA = (b, h, 128-row query tile), walking the forward lists:
+//                S = Q K^T, dP = dO V^T, dS = P (dP - delta) -> TMEM,
+//                dQ += dS K; dQ is written as bf16 by the same kernel.
+// Recomputing S and dP in the dQ kernel costs two extra MMAs per tile pair
+// but removes the fp32 dQ accumulator, its atomics and its memory traffic.
 #include "kernels.h"
 #include "mask.cuh"
 
@@ -34,24 +36,11 @@ struct BwdParams {
   const int32_t *kmc, *kmi, *kfc, *kfi;
   const float* lse2;   // [BH][sq_pad]
   const float* delta;  // [BH][sq_pad]
-  float* dq_acc;       // [BH][Sq][Dqk]
   __nv_bfloat16 *dq, *dk, *dv;
-  int atomic_dq;
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-
-// Writes one 128-value bf16 row (64 packed words) of a 128 x 128 tile kept in
-// the 128-byte-swizzled K-major layout (two 64-column slabs of 16 KB).
-__device__ __forceinline__ void store_row_sw128(uint8_t* tile, int row, const uint32_t* pk) {
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    const int slab = u >> 3, c16 = u & 7;
-    uint4* dst = reinterpret_cast<uint4*>(tile + slab * 16384 + row * 128 + ((c16 ^ (row & 7)) << 4));
-    *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-  }
-}
 
 // ------------------------------------------------------------------ preprocess
 __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ g,
@@ -82,366 +71,6 @@ __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_b
   }
 }
 
-__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, size_t n4,
-                                  float scale) {
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4; e += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[e];
-    uint2 w;
-    w.x = pack_bf16(a.x * scale, a.y * scale);
-    w.y = pack_bf16(a.z * scale, a.w * scale);
-    reinterpret_cast<uint2*>(dq)[e] = w;
-  }
-}
-
-// ------------------------------------------------------------------ dK / dV
-template <int DQK, int DV>
-struct BwdCfg {
-  static constexpr int SWQ = DQK >= 64 ? 128 : 64;
-  static constexpr int SWV = DV >= 64 ? 128 : 64;
-  static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
-  static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
-  static constexpr int DSTILE = 128 * 128 * 2;
-  // TMEM columns
-  static constexpr int T_R = 0, T_P = 128, T_DV = 192, T_DK = 192 + DV, T_DQ = 0;
-  static_assert(192 + DV + DQK <= 512, "TMEM budget");
-  // barriers
-  enum { B_KV, B_QF, B_QE, B_DOF, B_DOE, B_S, B_P, B_DP, B_DS, B_DSE, B_DQF, B_DQFREE, B_DONE, B_DRAIN, NBAR };
-  static constexpr int SMEM_USED = 1024 + QTILE /*K*/ + VTILE /*V*/ + QTILE /*Q*/ + VTILE /*dO*/ + DSTILE +
-                                   2 * 512 + NBAR * 8 + 16 + 4096;
-  static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
-  static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);    // S^T = K Q^T
-  static constexpr uint32_t ID_DV = idesc_bf16(128, DV, false, true);      // dV += P^T dO
-  static constexpr uint32_t ID_DK = idesc_bf16(128, DQK, false, true);     // dK += dS^T Q
-  static constexpr uint32_t ID_DQ = idesc_bf16(128, DQK, true, true);      // dQ = dS K (A MN-major)
-};
-
-template <int DQK, int DV>
-__global__ void __launch_bounds__(192, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
-  using C = BwdCfg<DQK, DV>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = base;
-  uint8_t* sV = sK + C::QTILE;
-  uint8_t* sQ = sV + C::VTILE;
-  uint8_t* sG = sQ + C::QTILE;
-  uint8_t* sS = sG + C::VTILE;
-  float* sL = reinterpret_cast<float*>(sS + C::DSTILE);  // lse2 of the q tile [128]
-  float* sD = sL + 128;                                  // delta [128]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sD + 128);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int k0 = (blockIdx.x / BH) * 128;
-
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_DQFREE) ? 128 : 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  TileWalk walk;
-  int nslots;
-  if (p.has_lists) {
-    walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
-    nslots = walk.nslots;
-  } else {
-    nslots = (p.Sq + 127) / 128;
-  }
-  auto slot = [&](int s, int* q0, bool* masked) -> bool {
-    return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, q0, masked)
-                       : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, q0, masked);
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int n = 0, nq = 0, ng = 0;
-      bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int q0;
-        bool masked;
-        if (!slot(s, &q0, &masked)) continue;
-        if (n == 0) {
-          mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
-          for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bh);
-          for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bh);
-        }
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_QE, (n - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_QF, C::QTILE + 1024);
-        for (int j = 0; j < C::NQSLAB; ++j)
-          tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, bar + C::B_QF, j * (C::SWQ / 2), q0, bh);
-        bulk_load(sL, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF);
-        bulk_load(sD, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF);
-        ++nq;
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_DOE, (n - 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_DOF, C::VTILE);
-        for (int j = 0; j < C::NVSLAB; ++j)
-          tma_load_3d(sG + j * C::VSLAB, &p.tm_do, bar + C::B_DOF, j * (C::SWV / 2), q0, bh);
-        ++ng;
-        ++n;
-      }
-      if (*abort_flag) {
-        if (nq > 0) mbar_drain(bar + C::B_KV, 0);
-        if (nq > 0) mbar_drain(bar + C::B_QF, (nq - 1) & 1);
-        if (ng > 0) mbar_drain(bar + C::B_DOF, (ng - 1) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t ka = smem_u32(sK), va = smem_u32(sV), qa = smem_u32(sQ), ga = smem_u32(sG), sa = smem_u32(sS);
-      int n = 0;
-      bool ok = true;
-      for (int s = 0; s < nslots && ok; ++s) {
-        int q0;
-        bool masked;
-        if (!slot(s, &q0, &masked)) continue;
-        if (n == 0 && !(ok = mbar_wait(bar + C::B_KV, 0, abort_flag))) break;
-        if (!(ok = mbar_wait(bar + C::B_QF, n & 1, abort_flag))) break;
-        // R must be free: dQ of the previous tile read out (atomic mode); in
-        // deterministic mode dS_ready of the previous tile already implies it.
-        if (n >= 1 && p.atomic_dq && !(ok = mbar_wait(bar + C::B_DQFREE, (n - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        // S^T = K Q^T : M = keys, N = queries, K = DQK
-#pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWQ / 2), off = (kk * 32) % C::SWQ;
-          umma_ss(tmem + C::T_R, sdesc(ka + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)),
-                  sdesc(qa + slab * C::QSLAB + off, 16, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_ST, kk > 0);
-        }
-        umma_commit(bar + C::B_S);
-        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(bar + C::B_DOF, n & 1, abort_flag))) break;
-        tc_fence_after();
-        // dP^T = V dO^T : M = keys, N = queries, K = DV
-#pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {
-          const int slab = (kk * 16) / (C::SWV / 2), off = (kk * 32) % C::SWV;
-          umma_ss(tmem + C::T_R, sdesc(va + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)),
-                  sdesc(ga + slab * C::VSLAB + off, 16, 8 * C::SWV, swz_code(C::SWV)), C::ID_ST, kk > 0);
-        }
-        // dV += P^T dO : A = P^T (TMEM), B = dO MN-major (N = DV, K = queries)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8,
-                  sdesc(ga + kk * 16 * C::SWV, C::VSLAB, 8 * C::SWV, swz_code(C::SWV)), C::ID_DV, (n > 0 || kk > 0));
-        umma_commit(bar + C::B_DP);
-        umma_commit(bar + C::B_DOE);
-        if (!(ok = mbar_wait(bar + C::B_DS, n & 1, abort_flag))) break;
-        tc_fence_after();
-        // dK += dS^T Q : A = dS^T (K-major, rows = keys), B = Q MN-major (N = DQK)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int slab = kk >> 2, off = (kk & 3) * 32;
-          umma_ss(tmem + C::T_DK, sdesc(sa + slab * 16384 + off, 16, 1024, 2),
-                  sdesc(qa + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DK, (n > 0 || kk > 0));
-        }
-        umma_commit(bar + C::B_QE);
-        if (p.atomic_dq) {
-          // dQ = dS K : A = dS (MN-major view of the dS^T tile), B = K MN-major
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss(tmem + C::T_DQ, sdesc(sa + kk * 2048, 16384, 1024, 2),
-                    sdesc(ka + kk * 16 * C::SWQ, C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ)), C::ID_DQ, kk > 0);
-          umma_commit(bar + C::B_DQF);
-        }
-        umma_commit(bar + C::B_DSE);
-        ++n;
-      }
-      umma_commit(bar + C::B_DONE);
-      if (*abort_flag) {
-        umma_commit(bar + C::B_DRAIN);
-        mbar_drain(bar + C::B_DRAIN, 0);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ dS warps
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // key row (and query row for the dQ read-out)
-    const int j = k0 + row;
-    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    int ilo, ihi;
-    col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
-    bool kept = j < p.Sk;
-    if (kept && p.mask.keep) kept = (__ldg(p.mask.keep + (size_t)bh * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
-    const float kb = (j < p.Sk && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bh * p.Sk + j) : 0.f;
-    const float kt = (kb - p.mask.slope * (float)j) * kLog2e;  // per-key score term, log2 units
-    int n = 0;
-    bool ok = true;
-    for (int s = 0; s < nslots && ok; ++s) {
-      int q0;
-      bool masked;
-      if (!slot(s, &q0, &masked)) continue;
-      ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar + C::B_QF, n & 1, abort_flag);  // lse2 / delta vectors landed
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t r[128];
-      tmem_ld32(tl + C::T_R + 0, r);
-      tmem_ld32(tl + C::T_R + 32, r + 32);
-      tmem_ld32(tl + C::T_R + 64, r + 64);
-      tmem_ld32(tl + C::T_R + 96, r + 96);
-      tmem_wait_ld32(r);
-      reg_fence32(r + 32);
-      reg_fence32(r + 64);
-      reg_fence32(r + 96);
-      const int clo = masked ? (kept ? ilo - q0 : 128) : 0;
-      const int chi = masked ? ihi - q0 : 127;
-      uint32_t pk[64], dc[64];
-      const bool cap = p.cap_pre != 0.f;
-#pragma unroll
-      for (int c2 = 0; c2 < 64; ++c2) {
-        float pr[2], dd[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * c2 + e;
-          const float x = __uint_as_float(r[c]);
-          float t;
-          dd[e] = 1.f;
-          if (cap) {
-            const float th = tanh_fast(x * p.cap_pre);
-            t = p.cap_post * th;
-            dd[e] = 1.f - th * th;
-          } else {
-            t = x * p.scale_log2;
-          }
-          const float v = ex2(t + kt - sL[c]);
-          pr[e] = (c >= clo && c <= chi) ? v : 0.f;
-        }
-        pk[c2] = pack_bf16(pr[0], pr[1]);
-        dc[c2] = pack_bf16(dd[0], dd[1]);
-      }
-      tmem_st32(tl + C::T_P, pk);
-      tmem_st32(tl + C::T_P + 32, pk + 32);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar + C::B_P);
-      // dP^T
-      ok = mbar_wait(bar + C::B_DP, n & 1, abort_flag);
-      if (ok && n >= 1) ok = mbar_wait(bar + C::B_DSE, (n - 1) & 1, abort_flag);  // dS tile free
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      tmem_ld32(tl + C::T_R + 0, r);
-      tmem_ld32(tl + C::T_R + 32, r + 32);
-      tmem_ld32(tl + C::T_R + 64, r + 64);
-      tmem_ld32(tl + C::T_R + 96, r + 96);
-      tmem_wait_ld32(r);
-      reg_fence32(r + 32);
-      reg_fence32(r + 64);
-      reg_fence32(r + 96);
-      uint32_t ds[64];
-#pragma unroll
-      for (int c2 = 0; c2 < 64; ++c2) {
-        const int c = 2 * c2;
-        float d0 = bf_lo(pk[c2]) * (__uint_as_float(r[c]) - sD[c]);
-        float d1 = bf_hi(pk[c2]) * (__uint_as_float(r[c + 1]) - sD[c + 1]);
-        if (cap) {
-          d0 *= bf_lo(dc[c2]);
-          d1 *= bf_hi(dc[c2]);
-        }
-        ds[c2] = pack_bf16(d0, d1);
-      }
-      store_row_sw128(sS, row, ds);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar + C::B_DS);
-      if (p.atomic_dq) {
-        // read dQ of this query tile (lane = query row) and add it to the accumulator
-        ok = mbar_wait(bar + C::B_DQF, n & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        const int i = q0 + row;
-        float* dst = p.dq_acc + ((size_t)bh * p.Sq + i) * DQK;
-#pragma unroll 1
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
-          uint32_t a[32];
-          tmem_ld32(tl + C::T_DQ + c0, a);
-          tmem_wait_ld32(a);
-          if (i < p.Sq) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              atomicAdd(reinterpret_cast<float4*>(dst + c0 + c),
-                        make_float4(__uint_as_float(a[c]), __uint_as_float(a[c + 1]), __uint_as_float(a[c + 2]),
-                                    __uint_as_float(a[c + 3])));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar + C::B_DQFREE);
-      }
-      ++n;
-    }
-    // ---- epilogue: dV, dK rows of this thread's key
-    if (ok) {
-      const bool wrote = n > 0;
-      if (wrote) {
-        ok = mbar_wait(bar + C::B_DONE, 0, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-      }
-      if (ok) {
-        __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + j) * DV;
-        __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + j) * DQK;
-#pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-          uint32_t a[32];
-          if (wrote) {
-            tmem_ld32(tl + C::T_DV + c0, a);
-            tmem_wait_ld32(a);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) a[c] = 0u;
-          }
-          if (j < p.Sk) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 8)
-              *reinterpret_cast<uint4*>(dvrow + c0 + c) =
-                  make_uint4(pack_bf16(__uint_as_float(a[c]), __uint_as_float(a[c + 1])),
-                             pack_bf16(__uint_as_float(a[c + 2]), __uint_as_float(a[c + 3])),
-                             pack_bf16(__uint_as_float(a[c + 4]), __uint_as_float(a[c + 5])),
-                             pack_bf16(__uint_as_float(a[c + 6]), __uint_as_float(a[c + 7])));
-          }
-        }
-#pragma unroll 1
-        for (int c0 = 0; c0 < DQK; c0 += 32) {
-          uint32_t a[32];
-          if (wrote) {
-            tmem_ld32(tl + C::T_DK + c0, a);
-            tmem_wait_ld32(a);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) a[c] = 0u;
-          }
-          const float sc = p.scale;
-          if (j < p.Sk) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 8)
-              *reinterpret_cast<uint4*>(dkrow + c0 + c) =
-                  make_uint4(pack_bf16(sc * __uint_as_float(a[c]), sc * __uint_as_float(a[c + 1])),
-                             pack_bf16(sc * __uint_as_float(a[c + 2]), sc * __uint_as_float(a[c + 3])),
-                             pack_bf16(sc * __uint_as_float(a[c + 4]), sc * __uint_as_float(a[c + 5])),
-                             pack_bf16(sc * __uint_as_float(a[c + 6]), sc * __uint_as_float(a[c + 7])));
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
-}
-
 // ------------------------------------------------------------------ dK / dV, TMEM-resident (no dQ)
 // CTA = (b, h, 128-key tile). Per listed query tile n (thread = key row):
 //   S^T_n = K Q_n^T -> R;   P^T_n = exp2(...) -> X (bf16);
@@ -451,7 +80,7 @@ __global__ void __launch_bounds__(192, 1) dkdv_kernel(const __grid_constant__ Bw
 // S^T_{n+1} / dK_n / dP^T_{n+1} / dV_{n+1} back to back while the dS warps
 // work. TMEM: R [0,128), X [128,192), dV [192,192+Dv), dK [192+Dv, +Dqk).
 template <int DQK, int DV>
-struct Dkdv2Cfg {
+struct DkdvCfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
   static constexpr int SWV = DV >= 64 ? 128 : 64;
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
@@ -472,8 +101,8 @@ struct Dkdv2Cfg {
 };
 
 template <int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ BwdParams p) {
-  using C = Dkdv2Cfg<DQK, DV>;
+__global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = DkdvCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = base;
@@ -814,7 +443,7 @@ __global__ void __launch_bounds__(320, 1) dkdv2_kernel(const __grid_constant__ B
 // dS_n = P (dP - delta) -> [448,512) (bf16); dQ += dS_n K_n -> [256,256+Dqk).
 // dQ of tile n is issued after S / dP of tile n+1.
 template <int DQK, int DV>
-struct Dq2Cfg {
+struct DqCfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
   static constexpr int SWV = DV >= 64 ? 128 : 64;
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
@@ -834,8 +463,8 @@ struct Dq2Cfg {
 };
 
 template <int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(320, 1) dq2_kernel(const __grid_constant__ BwdParams p) {
-  using C = Dq2Cfg<DQK, DV>;
+__global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = DqCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
@@ -1123,31 +752,24 @@ static int set_smem_once(K kern, int bytes, bool* flag) {
 }
 
 template <int DQK, int DV, bool CAP>
-static int launch_bwd_main(const BwdParams& prm, const Shape& s, int deterministic, cudaStream_t st) {
+static int launch_bwd_main(const BwdParams& prm, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H;
-  if (!deterministic) {
-    static bool f1 = false;
-    if (set_smem_once(dkdv_kernel<DQK, DV>, BwdCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
-    dkdv_kernel<DQK, DV><<<((s.Sk + 127) / 128) * BH, 192, BwdCfg<DQK, DV>::SMEM, st>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
-  }
-  static bool f2 = false, f3 = false;
-  if (set_smem_once(dkdv2_kernel<DQK, DV, CAP>, Dkdv2Cfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
-  dkdv2_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 320, Dkdv2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  static bool f1 = false, f2 = false;
+  if (set_smem_once(dkdv_kernel<DQK, DV, CAP>, DkdvCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
+  dkdv_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  if (set_smem_once(dq2_kernel<DQK, DV, CAP>, Dq2Cfg<DQK, DV>::SMEM, &f3)) return GBATTN_ERR_CUDA;
-  dq2_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 320, Dq2Cfg<DQK, DV>::SMEM, st>>>(prm);
+  if (set_smem_once(dq_kernel<DQK, DV, CAP>, DqCfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
+  dq_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 320, DqCfg<DQK, DV>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
 template <int DQK, int DV>
-static int launch_bwd_cap(const BwdParams& prm, const Shape& s, int deterministic, bool cap, cudaStream_t st) {
-  return cap ? launch_bwd_main<DQK, DV, true>(prm, s, deterministic, st)
-             : launch_bwd_main<DQK, DV, false>(prm, s, deterministic, st);
+static int launch_bwd_cap(const BwdParams& prm, const Shape& s, bool cap, cudaStream_t st) {
+  return cap ? launch_bwd_main<DQK, DV, true>(prm, s, st) : launch_bwd_main<DQK, DV, false>(prm, s, st);
 }
 
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dout,
-                    const float* lse, float scale, const HostMask& m, int deterministic, void* dq, void* dk, void* dv,
+                    const float* lse, float scale, const HostMask& m, void* dq, void* dk, void* dv,
                     void* ws, cudaStream_t st) {
   BwdParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -1194,40 +816,26 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
     prm.kfi = m.k_full_idx;
   }
   char* w = static_cast<char*>(ws);
-  const size_t acc_bytes = align_up((size_t)BH * s.Sq * s.Dqk * sizeof(float), 256);
   const size_t vec_bytes = align_up((size_t)BH * prm.sq_pad * sizeof(float), 256);
-  prm.dq_acc = reinterpret_cast<float*>(w);
-  float* delta = reinterpret_cast<float*>(w + acc_bytes);
-  float* lse2 = reinterpret_cast<float*>(w + acc_bytes + vec_bytes);
+  float* delta = reinterpret_cast<float*>(w);
+  float* lse2 = reinterpret_cast<float*>(w + vec_bytes);
   prm.delta = delta;
   prm.lse2 = lse2;
   prm.dq = static_cast<__nv_bfloat16*>(dq);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
-  prm.atomic_dq = deterministic ? 0 : 1;
 
   const long long rows = (long long)BH * prm.sq_pad;
   bwd_pre_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, BH, s.Sq, prm.sq_pad, s.Dv,
       m.slope * kLog2e, delta, lse2);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  if (!deterministic && cudaMemsetAsync(prm.dq_acc, 0, (size_t)BH * s.Sq * s.Dqk * sizeof(float), st) != cudaSuccess)
-    return GBATTN_ERR_CUDA;
-  int rc;
   const bool cap = m.softcap > 0.f;
-  if (s.Dqk == 32 && s.Dv == 32) rc = launch_bwd_cap<32, 32>(prm, s, deterministic, cap, st);
-  else if (s.Dqk == 64 && s.Dv == 64) rc = launch_bwd_cap<64, 64>(prm, s, deterministic, cap, st);
-  else if (s.Dqk == 128 && s.Dv == 128) rc = launch_bwd_cap<128, 128>(prm, s, deterministic, cap, st);
-  else if (s.Dqk == 192 && s.Dv == 128) rc = launch_bwd_cap<192, 128>(prm, s, deterministic, cap, st);
-  else return GBATTN_ERR_UNSUPPORTED;
-  if (rc) return rc;
-  if (!deterministic) {
-    const size_t n4 = (size_t)BH * s.Sq * s.Dqk / 4;
-    dq_convert_kernel<<<(unsigned)((n4 + 255) / 256 < 2432 ? (n4 + 255) / 256 : 2432), 256, 0, st>>>(
-        prm.dq_acc, prm.dq, n4, scale);
-    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  }
-  return GBATTN_OK;
+  if (s.Dqk == 32 && s.Dv == 32) return launch_bwd_cap<32, 32>(prm, s, cap, st);
+  if (s.Dqk == 64 && s.Dv == 64) return launch_bwd_cap<64, 64>(prm, s, cap, st);
+  if (s.Dqk == 128 && s.Dv == 128) return launch_bwd_cap<128, 128>(prm, s, cap, st);
+  if (s.Dqk == 192 && s.Dv == 128) return launch_bwd_cap<192, 128>(prm, s, cap, st);
+  return GBATTN_ERR_UNSUPPORTED;
 }
 
 GB_DEFINE_ERROR_READER(bwd_take_error)

@@ -37,8 +37,8 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
 int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, float scale,
                     const HostMask& m, float* o, float* lse, cudaStream_t st);
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o,
-                    const void* dout, const float* lse, float scale, const HostMask& m, int deterministic,
-                    void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
+                    const void* dout, const float* lse, float scale, const HostMask& m, void* dq, void* dk,
+                    void* dv, void* ws, cudaStream_t st);
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
                     const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
                     float* dv, void* ws, cudaStream_t st);
@@ -58,7 +58,7 @@ int simt_take_error();
 int decode_take_error();
 int blockmask_take_error();
 
-// Workspace layout of attn_bwd: [dq_accum fp32 BHxSqxDqk][delta fp32 BHxSq][pad]
+// Workspace layout of attn_bwd: [delta fp32 BH x ceil128(Sq)][lse2 fp32 BH x ceil128(Sq)]
 size_t bwd_workspace_bytes(const Shape& s);
 size_t align_up(size_t x, size_t a);
 

@@ -439,7 +439,7 @@ int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
   prm.dk = dk;
   prm.dv = dv;
   const size_t BH = (size_t)s.B * s.H;
-  prm.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(BH * s.Sq * s.Dqk * sizeof(float), 256));
+  prm.delta = reinterpret_cast<float*>(ws);
   const long long rows = (long long)BH * s.Sq;
   simt_delta_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;

@@ -147,21 +147,23 @@ int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
              const gbattn_mask* mask, const gbattn_blocks* blocks,
              void* o, float* lse, gbattn_stream stream);
 
-/* Workspace bytes attn_bwd needs for this shape (fp32 dQ accumulator and two
- * per-row fp32 vectors). Returns 0 for invalid dims. */
+/* Workspace bytes attn_bwd needs for this shape: two per-row fp32 vectors
+ * (rowsum(dO o O) and the log2-domain LSE) of B*H*ceil(Sq/128)*128 entries.
+ * Returns 0 for invalid dims. */
 size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv);
 
 /*
  * attn_bwd - gradients of O for the loss <dO, O> ([FSA] backward, "seq-k
  * parallel" path with an optional deterministic mode; [FA2C] `_flash_attn_bwd`
- * with the backward block lists). Steps: D_i = sum_d dO_id O_id; per kv tile,
- * recompute P from LSE, dV += P^T dO, dP = dO V^T, dS = P (dP - D),
- * dK += scale dS^T Q, dQ += scale dS K. deterministic = 0 accumulates dQ
- * with fp32 atomics across kv tiles; deterministic = 1 computes dQ in a
- * separate query-parallel pass so that dQ is bitwise reproducible. o and lse
- * must be the outputs of attn_fwd for the same inputs. workspace is device
- * memory of at least attn_bwd_workspace_bytes(); its contents on entry do not
- * matter.
+ * with the backward block lists). Steps: D_i = sum_d dO_id O_id; per kv tile
+ * (key-parallel), recompute P from LSE, dV += P^T dO, dP = dO V^T,
+ * dS = P (dP - D), dK += scale dS^T Q; per query tile (query-parallel),
+ * recompute S and dP and accumulate dQ = scale dS K. No gradient is
+ * accumulated with atomics, so every output is bitwise reproducible whatever
+ * `deterministic` says (0 or 1 are both accepted; any other value is
+ * GBATTN_ERR_ARG). o and lse must be the outputs of attn_fwd for the same
+ * inputs. workspace is device memory of at least attn_bwd_workspace_bytes();
+ * its contents on entry do not matter.
  */
 int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
              const void* q, const void* k, const void* v, const void* o,

@@ -55,8 +55,9 @@ def test_block_mask_sizes():
 
 def test_workspace_queries():
     lib = ga.load_library()
-    # dq accumulator fp32 [2,8,2048,64] + 2 row vectors of [2,8,2048]
-    assert lib.attn_bwd_workspace_bytes(0, 2, 8, 2048, 2048, 64, 64) == 2 * 8 * 2048 * 64 * 4 + 2 * 2 * 8 * 2048 * 4
+    # 2 row vectors of [2,8,2048] fp32 (rows padded to 128)
+    assert lib.attn_bwd_workspace_bytes(0, 2, 8, 2048, 2048, 64, 64) == 2 * 2 * 8 * 2048 * 4
+    assert lib.attn_bwd_workspace_bytes(0, 1, 1, 100, 100, 64, 64) == 2 * 512
     assert lib.attn_bwd_workspace_bytes(0, 0, 8, 2048, 2048, 64, 64) == 0
     assert lib.attn_fwd_splitkv_workspace_bytes(32, 32, 1, 128, 1) == 0
     assert lib.attn_fwd_splitkv_workspace_bytes(32, 32, 1, 128, 4) == 4 * 1024 * 128 * 4 + 4 * 1024 * 4

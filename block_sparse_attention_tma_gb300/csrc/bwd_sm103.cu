@@ -89,8 +89,10 @@ struct DkdvCfg {
   static constexpr int GST = DQK >= 192 ? 1 : 2;
   static constexpr int T_R = 0, T_X = 128, T_DV = 192, T_DK = 192 + DV;
   static_assert(192 + DV + DQK <= 512, "TMEM budget");
-  enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_P, B_DP, B_DVD,
-         B_DS, B_DKD, B_DONE, B_DRAIN, NBAR };
+  // B_RA / B_RB: the elementwise warps have copied S^T / dP^T out of R (R may
+  // be overwritten); B_P / B_DS: P^T / dS^T written to X.
+  enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_RA, B_P, B_DP, B_RB,
+         B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
       1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + TCAP * 2 + NBAR * 8 + 16 + 2048;
@@ -135,7 +137,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   };
   if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
   if (threadIdx.x == 32) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_P || b == C::B_DS) ? 256 : 1);
+    for (int b = 0; b < C::NBAR; ++b)
+      mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -204,6 +207,9 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         umma_commit(bar + C::B_DKD);
         umma_commit(bar + C::B_QE + qs);
       };
+      // Issue order per query tile n: S^T_n, dK_{n-1}, dP^T_n, dV_n. R is
+      // reused as soon as the elementwise warps have copied it to registers,
+      // so dP^T_n runs while P^T_n is computed and S^T_{n+1} while dS^T_n is.
       int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -213,8 +219,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         if (n == 0 && !(ok = mbar_wait(bar + C::B_KV, 0, abort_flag))) break;
         const int qs = n % C::QST;
         if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
-        // R is free once the dS warps have read dP^T of the previous tile
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
+        if (n >= 1 && !(ok = mbar_wait(bar + C::B_RB, (n - 1) & 1, abort_flag))) break;  // dP^T_{n-1} read
         tc_fence_after();
         {
           const uint32_t blo = qd.lo + ((qs * C::QTILE) >> 4);
@@ -224,8 +229,12 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
-        if (n >= 1) issue_dk(n - 1);
-        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;
+        if (n >= 1) {
+          if (!(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;  // dS^T_{n-1} in X
+          tc_fence_after();
+          issue_dk(n - 1);
+        }
+        if (!(ok = mbar_wait(bar + C::B_RA, n & 1, abort_flag))) break;  // S^T_n read
         const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
         tc_fence_after();
@@ -237,6 +246,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
                    blo + kmajor_step(kk, C::SWV, C::VSLAB), gd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_DP);
+        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;  // P^T_n in X
+        tc_fence_after();
         {
           const uint32_t blo = gm.lo + ((gs * C::VTILE) >> 4);
           const uint32_t acc0 = n > 0 ? 1u : 0u;
@@ -292,19 +303,23 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       tc_fence_after();
       const float* sl = sLD + qs * 256;
       const float* sd = sl + 128;
-      // P^T = exp2(S^T * scale * log2e + key term - lse2[q]), two 32-column halves
+      // copy S^T out of R, then let the MMA warp reuse R for dP^T
+      uint32_t r[64];
+      tmem_ld32(tl + C::T_R + cb, r);
+      tmem_ld32(tl + C::T_R + cb + 32, r + 32);
+      tmem_wait_ld32(r);
+      reg_fence32(r + 32);
+      tc_fence_before();
+      mbar_arrive(bar + C::B_RA);
+      // P^T = exp2(S^T * scale * log2e + key term - lse2[q])
       uint32_t pk[32], dc[CAP ? 32 : 1];
       const int clo = masked ? (kept ? ilo - q0 : 128) - cb : 0;
       const int chi = masked ? ihi - q0 - cb : 63;
+      {
+        const float4* sl4 = reinterpret_cast<const float4*>(sl + cb);
+        float* pf = reinterpret_cast<float*>(r);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::T_R + cb + hh * 32, r);
-        tmem_wait_ld32(r);
-        const float4* sl4 = reinterpret_cast<const float4*>(sl + cb + hh * 32);
-        float pf[32];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l4 = sl4[c4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           float dd[4];
@@ -324,16 +339,16 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
             pf[c] = ex2(t - lv[e]);
           }
           if constexpr (CAP) {
-            dc[hh * 16 + 2 * c4] = pack_bf16(dd[0], dd[1]);
-            dc[hh * 16 + 2 * c4 + 1] = pack_bf16(dd[2], dd[3]);
+            dc[2 * c4] = pack_bf16(dd[0], dd[1]);
+            dc[2 * c4 + 1] = pack_bf16(dd[2], dd[3]);
           }
         }
         if (masked) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pf[c] = (hh * 32 + c >= clo && hh * 32 + c <= chi) ? pf[c] : 0.f;
+          for (int c = 0; c < 64; ++c) pf[c] = (c >= clo && c <= chi) ? pf[c] : 0.f;
         }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[hh * 16 + c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
       }
       // X still holds dS^T of the previous tile until its dK MMA completes
       if (n >= 1) {
@@ -348,36 +363,38 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_P);
-      // dP^T -> dS^T = P^T (dP^T - delta[q])
+      // dP^T: copy out of R (then R is free for S^T of the next tile), dS^T = P^T (dP^T - delta[q])
       ok = mbar_wait(bar + C::B_DP, n & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      tmem_ld32(tl + C::T_R + cb, r);
+      tmem_ld32(tl + C::T_R + cb + 32, r + 32);
+      tmem_wait_ld32(r);
+      reg_fence32(r + 32);
+      tc_fence_before();
+      mbar_arrive(bar + C::B_RB);
       uint32_t ds[32];
+      {
+        const float4* sd4 = reinterpret_cast<const float4*>(sd + cb);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::T_R + cb + hh * 32, r);
-        tmem_wait_ld32(r);
-        const float4* sd4 = reinterpret_cast<const float4*>(sd + cb + hh * 32);
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c4 = 0; c4 < 16; ++c4) {
           const float4 d4 = sd4[c4];
-          const uint32_t p01 = pk[hh * 16 + 2 * c4], p23 = pk[hh * 16 + 2 * c4 + 1];
+          const uint32_t p01 = pk[2 * c4], p23 = pk[2 * c4 + 1];
           float d0 = bf_lo(p01) * (__uint_as_float(r[4 * c4 + 0]) - d4.x);
           float d1 = bf_hi(p01) * (__uint_as_float(r[4 * c4 + 1]) - d4.y);
           float d2 = bf_lo(p23) * (__uint_as_float(r[4 * c4 + 2]) - d4.z);
           float d3 = bf_hi(p23) * (__uint_as_float(r[4 * c4 + 3]) - d4.w);
           if constexpr (CAP) {
-            d0 *= bf_lo(dc[hh * 16 + 2 * c4]);
-            d1 *= bf_hi(dc[hh * 16 + 2 * c4]);
-            d2 *= bf_lo(dc[hh * 16 + 2 * c4 + 1]);
-            d3 *= bf_hi(dc[hh * 16 + 2 * c4 + 1]);
+            d0 *= bf_lo(dc[2 * c4]);
+            d1 *= bf_hi(dc[2 * c4]);
+            d2 *= bf_lo(dc[2 * c4 + 1]);
+            d3 *= bf_hi(dc[2 * c4 + 1]);
           }
-          ds[hh * 16 + 2 * c4] = pack_bf16(d0, d1);
-          ds[hh * 16 + 2 * c4 + 1] = pack_bf16(d2, d3);
+          ds[2 * c4] = pack_bf16(d0, d1);
+          ds[2 * c4 + 1] = pack_bf16(d2, d3);
         }
       }
       // X holds P^T until the dV MMA completes
@@ -452,8 +469,10 @@ struct DqCfg {
   static constexpr int VST = DQK >= 192 ? 1 : 2;
   static constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 448;
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
-  enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DS, B_DQD, B_DONE,
-         B_DRAIN, NBAR };
+  // B_RS / B_RP: the elementwise warps have copied S / dP out of TMEM;
+  // B_DS: dS written to TMEM.
+  enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DP, B_RS, B_RP, B_DS,
+         B_DQD, B_DONE, B_DRAIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
       1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + TCAP * 2 + NBAR * 8 + 16 + 2048;
@@ -498,7 +517,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   };
   if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
   if (threadIdx.x == 32) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, b == C::B_DS ? 256 : 1);
+    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_DS || b == C::B_RS || b == C::B_RP) ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -562,6 +581,8 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         umma_commit(bar + C::B_DQD);
         umma_commit(bar + C::B_KE + ks);
       };
+      // Issue order per kv tile n: S_n, dP_n, dQ_{n-1}. S and dP are reused as
+      // soon as the elementwise warps have copied them to registers.
       int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -571,9 +592,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         if (n == 0 && !(ok = mbar_wait(bar + C::B_QG, 0, abort_flag))) break;
         const int ks = n % C::KST, vs = n % C::VST;
         if (!(ok = mbar_wait(bar + C::B_KF + ks, (n / C::KST) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(bar + C::B_VF + vs, (n / C::VST) & 1, abort_flag))) break;
-        // S / dP buffers are free once the dS warps have read the previous tile
-        if (n >= 1 && !(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
+        if (n >= 1 && !(ok = mbar_wait(bar + C::B_RS, (n - 1) & 1, abort_flag))) break;  // S_{n-1} read
         tc_fence_after();
         {
           const uint32_t blo = kd.lo + ((ks * C::QTILE) >> 4);
@@ -582,6 +601,10 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
             mma_ss(tmem + C::T_S, qd.lo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi,
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), kd.hi, C::ID_S, kk > 0 ? 1u : 0u);
         }
+        umma_commit(bar + C::B_S);
+        if (!(ok = mbar_wait(bar + C::B_VF + vs, (n / C::VST) & 1, abort_flag))) break;
+        if (n >= 1 && !(ok = mbar_wait(bar + C::B_RP, (n - 1) & 1, abort_flag))) break;  // dP_{n-1} read
+        tc_fence_after();
         {
           const uint32_t blo = vd.lo + ((vs * C::VTILE) >> 4);
 #pragma unroll
@@ -589,9 +612,13 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
             mma_ss(tmem + C::T_DP, gd.lo + kmajor_step(kk, C::SWV, C::VSLAB), gd.hi,
                    blo + kmajor_step(kk, C::SWV, C::VSLAB), vd.hi, C::ID_S, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar + C::B_S);
+        umma_commit(bar + C::B_DP);
         umma_commit(bar + C::B_VE + vs);
-        if (n >= 1) issue_dq(n - 1);
+        if (n >= 1) {
+          if (!(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_dq(n - 1);
+        }
         ++n;
       }
       if (ok && n >= 1) {
@@ -635,12 +662,6 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         ctw[e * 32 + lane] = c;
       }
       __syncwarp();
-      ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       uint32_t kw[2] = {0xffffffffu, 0xffffffffu};
       if (keep) {
 #pragma unroll
@@ -651,45 +672,76 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
       }
       const int clo = masked ? lo - kv0 - cb : 0;
       const int chi = masked ? min(hi, p.Sk - 1) - kv0 - cb : 63;
-      uint32_t ds[32];
+      ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // S: copy out of TMEM (the MMA warp may then reuse it), P in place
+      uint32_t rs[64];
+      tmem_ld32(tl + C::T_S + cb, rs);
+      tmem_ld32(tl + C::T_S + cb + 32, rs + 32);
+      tmem_wait_ld32(rs);
+      reg_fence32(rs + 32);
+      tc_fence_before();
+      mbar_arrive(bar + C::B_RS);
+      float* pf = reinterpret_cast<float*>(rs);
+      float dd[CAP ? 64 : 1];
+      {
+        const float4* ct = reinterpret_cast<const float4*>(ctw);
 #pragma unroll
-      for (int qtr = 0; qtr < 2; ++qtr) {
-        uint32_t rs[32], rp[32];
-        tmem_ld32(tl + C::T_S + cb + qtr * 32, rs);
-        tmem_ld32(tl + C::T_DP + cb + qtr * 32, rp);
-        tmem_wait_ld32(rs);
-        reg_fence32(rp);
-        const float4* ct = reinterpret_cast<const float4*>(ctw + qtr * 32);
-        float d[32];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c4 = 0; c4 < 16; ++c4) {
           const float4 v4 = ct[c4];
           const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cl = 4 * c4 + e;
-            const float x = __uint_as_float(rs[cl]);
-            float t, dd = 1.f;
+            const int c = 4 * c4 + e;
+            const float x = __uint_as_float(rs[c]);
+            float t;
             if constexpr (CAP) {
               const float th = tanh_fast(x * p.cap_pre);
               t = fmaf(p.cap_post, th, cv[e]);
-              dd = 1.f - th * th;
+              dd[c] = 1.f - th * th;
             } else {
               t = fmaf(x, p.scale_log2, cv[e]);
             }
-            d[cl] = ex2(t - l2) * (__uint_as_float(rp[cl]) - dl) * dd;
+            pf[c] = ex2(t - l2);
           }
         }
         if (masked) {
 #pragma unroll
-          for (int cl = 0; cl < 32; ++cl) {
-            const int c = qtr * 32 + cl;  // column within this half
+          for (int c = 0; c < 64; ++c) {
             const bool al = c >= clo && c <= chi && ((kw[c >> 5] >> (c & 31)) & 1u);
-            d[cl] = al ? d[cl] : 0.f;
+            pf[c] = al ? pf[c] : 0.f;
           }
         }
+      }
+      ok = mbar_wait(bar + C::B_DP, n & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t ds[32];
+      {
+        uint32_t rp[64];
+        tmem_ld32(tl + C::T_DP + cb, rp);
+        tmem_ld32(tl + C::T_DP + cb + 32, rp + 32);
+        tmem_wait_ld32(rp);
+        reg_fence32(rp + 32);
+        tc_fence_before();
+        mbar_arrive(bar + C::B_RP);
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) ds[qtr * 16 + c2] = pack_bf16(d[2 * c2], d[2 * c2 + 1]);
+        for (int c2 = 0; c2 < 32; ++c2) {
+          float d0 = pf[2 * c2] * (__uint_as_float(rp[2 * c2]) - dl);
+          float d1 = pf[2 * c2 + 1] * (__uint_as_float(rp[2 * c2 + 1]) - dl);
+          if constexpr (CAP) {
+            d0 *= dd[2 * c2];
+            d1 *= dd[2 * c2 + 1];
+          }
+          ds[c2] = pack_bf16(d0, d1);
+        }
       }
       // the dS columns still feed the dQ MMA of the previous tile
       if (n >= 1) {

@@ -41,7 +41,8 @@ class _Mask(ctypes.Structure):
 class _Blocks(ctypes.Structure):
     _fields_ = [("sparse_m", ctypes.c_int), ("sparse_n", ctypes.c_int)] + [
         (n, ctypes.c_void_p) for n in ("q_mask_cnt", "q_mask_idx", "q_full_cnt", "q_full_idx",
-                                       "k_mask_cnt", "k_mask_idx", "k_full_cnt", "k_full_idx", "keep_bits")]
+                                       "k_mask_cnt", "k_mask_idx", "k_full_cnt", "k_full_idx", "keep_bits",
+                                       "keep_idx")]
 
 
 _lib = None
@@ -50,7 +51,7 @@ _lib = None
 _SIGS = [
     ("gbattn_version", ctypes.c_int, []),
     ("gbattn_strerror", ctypes.c_char_p, [ctypes.c_int]),
-    ("gbattn_block_mask_sizes", ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)] * 5),
+    ("gbattn_block_mask_sizes", ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)] * 6),
     ("build_block_mask", ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(_Mask), ctypes.POINTER(_Blocks),
                                                               ctypes.c_void_p]),
     ("attn_fwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.POINTER(_Mask),
@@ -60,7 +61,7 @@ _SIGS = [
     ("attn_bwd_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 7),
     ("attn_bwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.POINTER(_Mask),
                                                                               ctypes.POINTER(_Blocks), ctypes.c_int]
-     + [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
+     + [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p]),
     ("attn_fwd_splitkv_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 5),
     ("attn_fwd_splitkv", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float,
                                                                                       ctypes.POINTER(_Mask),
@@ -145,16 +146,22 @@ class BlockLists:
         return b
 
 
-def alloc_block_lists(B, H, Sq, Sk, sparse_m, sparse_n, device="cuda") -> BlockLists:
+def alloc_block_lists(B, H, Sq, Sk, sparse_m, sparse_n, device="cuda", gather=True) -> BlockLists:
+    """Allocates every list array. gather=True also allocates the dynamic
+    mask's kept-key index list, with which the bf16 kernels stream only the
+    kept keys; gather=False leaves it NULL (the kernels then walk the lists
+    and test the keep bits)."""
     lib = load_library()
-    sz = [ctypes.c_size_t() for _ in range(5)]
+    sz = [ctypes.c_size_t() for _ in range(6)]
     _check(lib.gbattn_block_mask_sizes(B, H, Sq, Sk, sparse_m, sparse_n, *[ctypes.byref(s) for s in sz]),
            "gbattn_block_mask_sizes")
-    qc, qi, kc, ki, kw = (s.value // 4 for s in sz)
+    qc, qi, kc, ki, kw, kx = (s.value // 4 for s in sz)
     mk = lambda n: torch.empty(max(n, 1), dtype=torch.int32, device=device)  # noqa: E731
     t = {"q_mask_cnt": mk(qc), "q_mask_idx": mk(qi), "q_full_cnt": mk(qc), "q_full_idx": mk(qi),
          "k_mask_cnt": mk(kc), "k_mask_idx": mk(ki), "k_full_cnt": mk(kc), "k_full_idx": mk(ki),
          "keep_bits": mk(kw)}
+    if gather:
+        t["keep_idx"] = mk(kx)
     return BlockLists(sparse_m, sparse_n, t)
 
 
@@ -190,7 +197,9 @@ def attn_bwd_workspace_bytes(dtype, B, H, Sq, Sk, Dqk, Dv) -> int:
 
 def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
              lists: Optional[BlockLists] = None, deterministic=False, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, dkey_bias: Optional[torch.Tensor] = None):
+    """Returns (dq, dk, dv); when dkey_bias (fp32 [B, H, Sk] on the GPU) is
+    given it receives the gradient of the key bias."""
     lib = load_library()
     B, H, Sq, Dqk = q.shape
     Sk, Dv = k.shape[2], v.shape[3]
@@ -205,7 +214,7 @@ def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
     cb = lists.c() if lists is not None else None
     _check(lib.attn_bwd(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
                         _ptr(lse), float(scale), ctypes.byref(cm), ctypes.byref(cb) if cb is not None else None,
-                        int(bool(deterministic)), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                        int(bool(deterministic)), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkey_bias), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)), "attn_bwd")
     return dq, dk, dv
 

@@ -123,7 +123,20 @@ int check_blocks(const gbattn_blocks* b, int Sq, int Sk, bool need_fwd, bool nee
   hm->k_full_cnt = b->k_full_cnt;
   hm->k_full_idx = b->k_full_idx;
   hm->keep = b->keep_bits;
+  hm->keep_idx = b->keep_idx;
   return GBATTN_OK;
+}
+
+// Gathered keys: the bf16 kernels stream only the kept keys of a dynamic
+// mask when the caller passed the kept-key index list (row indices of the
+// 2-D gather maps must fit in int32).
+void choose_gather(int dtype, const Shape& s, HostMask* hm) {
+  hm->gather = 0;
+  hm->kept = s.Sk;
+  if (dtype != GBATTN_BF16 || hm->kind != GBATTN_MASK_DYNAMIC_TOPK || !hm->has_lists || !hm->keep_idx) return;
+  if ((long long)s.B * s.H * s.Sk >= (1ll << 31)) return;
+  hm->gather = 1;
+  hm->kept = hm->topk < s.Sk ? hm->topk : s.Sk;
 }
 
 float resolve_scale(float scale, int Dqk) { return (scale > 0.f && isfinite(scale)) ? scale : 1.0f / sqrtf((float)Dqk); }
@@ -162,13 +175,27 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, int S, int BH,
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, int D, long long rows, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {(cuuint32_t)(swizzle_bytes / 2), 1};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace gb
 
 using namespace gb;
 
 extern "C" {
 
-int gbattn_version(void) { return 100; }
+int gbattn_version(void) { return 101; }
 
 const char* gbattn_strerror(int status) {
   switch (status) {
@@ -186,7 +213,7 @@ const char* gbattn_strerror(int status) {
 
 int gbattn_block_mask_sizes(int B, int H, int Sq, int Sk, int sparse_m, int sparse_n, size_t* q_cnt_bytes,
                             size_t* q_idx_bytes, size_t* k_cnt_bytes, size_t* k_idx_bytes,
-                            size_t* keep_bits_bytes) {
+                            size_t* keep_bits_bytes, size_t* keep_idx_bytes) {
   if (!dims_ok(B, H, Sq, Sk)) return GBATTN_ERR_ARG;
   if (sparse_m < 128 || sparse_n < 128 || sparse_m % 128 || sparse_n % 128) return GBATTN_ERR_ARG;
   const size_t BH = (size_t)B * H;
@@ -196,6 +223,7 @@ int gbattn_block_mask_sizes(int B, int H, int Sq, int Sk, int sparse_m, int spar
   if (k_cnt_bytes) *k_cnt_bytes = BH * nkb * 4;
   if (k_idx_bytes) *k_idx_bytes = BH * nkb * nqb * 4;
   if (keep_bits_bytes) *keep_bits_bytes = BH * ((Sk + 31) / 32) * 4;
+  if (keep_idx_bytes) *keep_idx_bytes = BH * (size_t)Sk * 4;
   return GBATTN_OK;
 }
 
@@ -211,6 +239,7 @@ int build_block_mask(int B, int H, int Sq, int Sk, const gbattn_mask* mask, gbat
       !out->k_mask_idx || !out->k_full_cnt || !out->k_full_idx)
     return GBATTN_ERR_ARG;
   if (hm.kind == GBATTN_MASK_DYNAMIC_TOPK && !out->keep_bits) return GBATTN_ERR_ARG;
+  if (out->keep_idx && !aligned4(out->keep_idx)) return GBATTN_ERR_ALIGN;
   rc = device_check();
   if (rc) return rc;
   return blockmask_launch(B, H, Sq, Sk, hm, out, static_cast<cudaStream_t>(stream));
@@ -238,6 +267,7 @@ int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
   rc = device_check();
   if (rc) return rc;
   const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  choose_gather(dtype, s, &hm);
   const float sc = resolve_scale(scale, Dqk);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GBATTN_BF16) return fwd_bf16_launch(s, q, k, v, sc, hm, o, lse, st);
@@ -253,13 +283,13 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk
 
 int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k, const void* v,
              const void* o, const void* dout, const float* lse, float scale, const gbattn_mask* mask,
-             const gbattn_blocks* blocks, int deterministic, void* dq, void* dk, void* dv, void* workspace,
-             size_t workspace_bytes, gbattn_stream stream) {
+             const gbattn_blocks* blocks, int deterministic, void* dq, void* dk, void* dv, float* dkey_bias,
+             void* workspace, size_t workspace_bytes, gbattn_stream stream) {
   if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return GBATTN_ERR_ARG;
   if (deterministic != 0 && deterministic != 1) return GBATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (dkey_bias && !aligned4(dkey_bias)))
     return GBATTN_ERR_ALIGN;
   if (dtype == GBATTN_BF16) {
     if (!bf16_dims_ok(Dqk, Dv)) return GBATTN_ERR_UNSUPPORTED;
@@ -278,13 +308,15 @@ int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
   if (!aligned16(workspace)) return GBATTN_ERR_ALIGN;
   rc = device_check();
   if (rc) return rc;
+  choose_gather(dtype, s, &hm);
   const float sc = resolve_scale(scale, Dqk);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GBATTN_BF16)
-    return bwd_bf16_launch(s, q, k, v, o, dout, lse, sc, hm, dq, dk, dv, workspace, st);
+    return bwd_bf16_launch(s, q, k, v, o, dout, lse, sc, hm, dq, dk, dv, dkey_bias, workspace, st);
   return bwd_fp32_launch(s, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
                          static_cast<const float*>(o), static_cast<const float*>(dout), lse, sc, hm,
-                         static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv), workspace, st);
+                         static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv), dkey_bias,
+                         workspace, st);
 }
 
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Dv, int num_splits) {

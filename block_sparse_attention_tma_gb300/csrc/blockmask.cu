@@ -108,6 +108,39 @@ __global__ void __launch_bounds__(kTopkThreads) topk_keep_kernel(const float* __
   }
 }
 
+// One CTA per (b, h): the kept-key index list, i.e. the indices of the set
+// bits of the keep mask in ascending order, then 0 up to Sk. A block-wide
+// exclusive scan of the kept flags gives each kept key its slot.
+__global__ void __launch_bounds__(kTopkThreads) keep_index_kernel(const uint32_t* __restrict__ keep, int Sk,
+                                                                  int nkw, int32_t* __restrict__ idx) {
+  const int bh = blockIdx.x;
+  const uint32_t* kw = keep + (size_t)bh * nkw;
+  int32_t* out = idx + (size_t)bh * Sk;
+  __shared__ int warp_sums[kTopkThreads / 32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < Sk; base += blockDim.x) {
+    const int j = base + tid;
+    const bool kept = j < Sk && ((__ldg(kw + (j >> 5)) >> (j & 31)) & 1u);
+    const unsigned b = __ballot_sync(0xffffffffu, kept);
+    if (lane == 0) warp_sums[warp] = __popc(b);
+    __syncthreads();
+    int before = s_carry;
+    for (int w = 0; w < warp; ++w) before += warp_sums[w];
+    if (kept) out[before + __popc(b & ((1u << lane) - 1u))] = j;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_sums[w];
+      s_carry += tot;
+    }
+    __syncthreads();
+  }
+  for (int t = s_carry + tid; t < Sk; t += blockDim.x) out[t] = 0;
+}
+
 struct ListArgs {
   MaskParams mask;
   int Sq, Sk, sm, sn, nqb, nkb, BH;
@@ -231,6 +264,10 @@ int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbat
     topk_keep_kernel<<<a.BH, kTopkThreads, 0, st>>>(m.key_bias, Sk, m.topk, out->keep_bits, a.mask.nkw);
     if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
     a.mask.keep = out->keep_bits;
+    if (out->keep_idx) {
+      keep_index_kernel<<<a.BH, kTopkThreads, 0, st>>>(out->keep_bits, Sk, a.mask.nkw, out->keep_idx);
+      if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+    }
   }
   const long long wf = (long long)a.BH * a.nqb, wb = (long long)a.BH * a.nkb;
   fwd_lists_kernel<<<(unsigned)((wf * 32 + 127) / 128), 128, 0, st>>>(a);

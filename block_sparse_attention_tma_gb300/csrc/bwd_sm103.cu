@@ -21,6 +21,13 @@
 //                dQ += dS K; dQ is written as bf16 by the same kernel.
 // Recomputing S and dP in the dQ kernel costs two extra MMAs per tile pair
 // but removes the fp32 dQ accumulator, its atomics and its memory traffic.
+//
+// Gathered keys (dynamic top-k mask with its kept-key index list): both
+// kernels work on compact tiles of kept keys built by TMA row gathers; dK / dV
+// rows are written back to the keys' original rows and a small kernel zeroes
+// the rows of the keys outside the keep set. The key-bias gradient
+// (dkey_bias_j = sum_i dS_ij before the softcap factor) is the row sum of
+// dS^T that the dK/dV threads already hold, one key row per thread.
 #include "kernels.h"
 #include "mask.cuh"
 
@@ -37,7 +44,32 @@ struct BwdParams {
   const float* lse2;   // [BH][sq_pad]
   const float* delta;  // [BH][sq_pad]
   __nv_bfloat16 *dq, *dk, *dv;
+  float* dbias;        // [BH][Sk] key-bias gradient, or nullptr
+  int gather;          // gathered keys: tm_k / tm_v are 2-D row-gather maps
+  int Skv;             // key extent the kernels stream (Sk, or the kept-key count)
+  const int32_t* kidx; // [BH][Sk] kept key indices (gathered keys)
 };
+
+// Zeroes dK, dV (and dkey_bias) rows of the keys outside the keep set when
+// the kernels gather kept keys only. One warp per (b, h, 32-key word).
+__global__ void unkept_zero_kernel(const uint32_t* __restrict__ keep, int nkw, int BH, int Sk, int Dqk, int Dv,
+                                   __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                   float* __restrict__ dbias) {
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= (long long)BH * nkw) return;
+  const int lane = threadIdx.x & 31;
+  const int bh = (int)(gw / nkw), w = (int)(gw % nkw);
+  const uint32_t bits = __ldg(keep + gw);
+  for (int b = 0; b < 32; ++b) {
+    const int j = w * 32 + b;
+    if (j >= Sk) break;
+    if ((bits >> b) & 1u) continue;
+    const size_t r = (size_t)bh * Sk + j;
+    for (int c = lane * 8; c < Dqk; c += 256) *reinterpret_cast<uint4*>(dk + r * Dqk + c) = make_uint4(0, 0, 0, 0);
+    for (int c = lane * 8; c < Dv; c += 256) *reinterpret_cast<uint4*>(dv + r * Dv + c) = make_uint4(0, 0, 0, 0);
+    if (lane == 0 && dbias) dbias[r] = 0.f;
+  }
+}
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
@@ -91,18 +123,19 @@ struct DkdvCfg {
   static_assert(192 + DV + DQK <= 512, "TMEM budget");
   // B_RA / B_RB: the elementwise warps have copied S^T / dP^T out of R (R may
   // be overwritten); B_P / B_DS: P^T / dS^T written to X.
+  // B_FIN: the second half's key-bias partial sums are in shared memory.
   enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_RA, B_P, B_DP, B_RB,
-         B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, NBAR };
+         B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, B_FIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
-      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + TCAP * 2 + NBAR * 8 + 16 + 2048;
+      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 + TCAP * 2 + NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
   static constexpr uint32_t ID_DV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
   static constexpr uint32_t ID_DK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
 };
 
-template <int DQK, int DV, bool CAP>
+template <int DQK, int DV, bool CAP, bool GAT, bool DB>
 __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = DkdvCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -112,33 +145,55 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   uint8_t* sQ = sV + C::VTILE;                  // [QST]
   uint8_t* sG = sQ + C::QST * C::QTILE;         // [GST]
   float* sLD = reinterpret_cast<float*>(sG + C::GST * C::VTILE);  // [QST][lse2 128 | delta 128]
-  uint16_t* tlist = reinterpret_cast<uint16_t*>(sLD + C::QST * 256);  // [TCAP]
+  float* sDB = sLD + C::QST * 256;                                  // [128] key-bias partial sums
+  uint16_t* tlist = reinterpret_cast<uint16_t*>(sDB + 128);         // [TCAP]
   uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
+  int* gpos = reinterpret_cast<int*>(tmem_slot + 4);  // [2] first / last key of a gathered tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int bh = blockIdx.x % BH;
   const int k0 = (blockIdx.x / BH) * 128;
+  constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
+  const int Skv = p.Skv;
+  const int delta = p.Sk - p.Sq;
+  const int32_t* pos_h = gat ? p.kidx + (size_t)bh * p.Sk : nullptr;
 
   TileWalk walk;
   int nslots;
-  if (p.has_lists) {
+  int p_first = 0, p_last = 0;
+  if (gat) {
+    nslots = (p.Sq + 127) / 128;
+  } else if (p.has_lists) {
     walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
     nslots = walk.nslots;
   } else {
     nslots = (p.Sq + 127) / 128;
   }
   auto slot = [&](int s, int* q0, bool* masked) -> bool {
+    if (gat) return gathered_slot_cols(s, p_first, p_last, k0 + 128 <= Skv, delta, p.Sq, q0, masked);
     return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, q0, masked)
                        : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, q0, masked);
   };
-  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (warp == 0) {
+    if (gat) {
+      p_first = __ldg(pos_h + k0);
+      p_last = __ldg(pos_h + min(k0 + 127, Skv - 1));
+      if (lane == 0) {
+        gpos[0] = p_first;
+        gpos[1] = p_last;
+      }
+    }
+    build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  }
   if (threadIdx.x == 32) {
     for (int b = 0; b < C::NBAR; ++b)
-      mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? 256 : 1);
+      mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? 256
+                         : b == C::B_FIN                                             ? 128
+                                                                                     : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -148,10 +203,55 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = *tcount;
+  if (gat && warp != 0) {
+    p_first = gpos[0];
+    p_last = gpos[1];
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if constexpr (!GAT) {
+      if (lane == 0) {
+        int n = 0, nq = 0, ng = 0;
+        bool ok = true;
+        auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+        int q0;
+        bool masked;
+        while (ok && it.next(&q0, &masked)) {
+          if (n == 0) {
+            mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
+            for (int j = 0; j < C::NQSLAB; ++j)
+              tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bh);
+            for (int j = 0; j < C::NVSLAB; ++j)
+              tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bh);
+          }
+          const int qs = n % C::QST;
+          if (n >= C::QST && !(ok = mbar_wait(bar + C::B_QE + qs, ((n / C::QST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
+          for (int j = 0; j < C::NQSLAB; ++j)
+            tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
+          bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+          bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+          ++nq;
+          const int gs = n % C::GST;
+          if (n >= C::GST && !(ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
+          for (int j = 0; j < C::NVSLAB; ++j)
+            tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bh);
+          ++ng;
+          ++n;
+        }
+        if (*abort_flag) {
+          if (nq > 0) mbar_drain(bar + C::B_KV, 0);
+          for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t)
+            mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
+          for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t)
+            mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
+        }
+      }
+    } else {
+      // gathered keys: every lane gathers 4 rows of the K and V tiles; lane 0
+      // waits and issues the query-side loads
       int n = 0, nq = 0, ng = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -159,32 +259,50 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       bool masked;
       while (ok && it.next(&q0, &masked)) {
         if (n == 0) {
-          mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
+          if (lane == 0) mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
+          int gr[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(k0 + 4 * lane + e, Skv - 1));
+          __syncwarp();
+#pragma unroll
           for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bh);
+            tma_gather4(sK + j * C::QSLAB + 4 * lane * C::SWQ, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), gr[0], gr[1],
+                        gr[2], gr[3]);
+#pragma unroll
           for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bh);
+            tma_gather4(sV + j * C::VSLAB + 4 * lane * C::SWV, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), gr[0], gr[1],
+                        gr[2], gr[3]);
         }
-        const int qs = n % C::QST;
-        if (n >= C::QST && !(ok = mbar_wait(bar + C::B_QE + qs, ((n / C::QST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
-        for (int j = 0; j < C::NQSLAB; ++j)
-          tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
-        bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
-        bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
-        ++nq;
-        const int gs = n % C::GST;
-        if (n >= C::GST && !(ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
-        for (int j = 0; j < C::NVSLAB; ++j)
-          tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bh);
-        ++ng;
+        if (lane == 0) {
+          const int qs = n % C::QST;
+          if (n >= C::QST) ok = mbar_wait(bar + C::B_QE + qs, ((n / C::QST) + 1) & 1, abort_flag);
+          if (ok) {
+            mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
+            for (int j = 0; j < C::NQSLAB; ++j)
+              tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
+            bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+            bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+            ++nq;
+            const int gs = n % C::GST;
+            if (n >= C::GST) ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag);
+            if (ok) {
+              mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
+              for (int j = 0; j < C::NVSLAB; ++j)
+                tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0,
+                            bh);
+              ++ng;
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         ++n;
       }
-      if (*abort_flag) {
-        if (nq > 0) mbar_drain(bar + C::B_KV, 0);
-        for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t) mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
-        for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t) mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
+      if (lane == 0 && *abort_flag) {
+        if (n > 0) mbar_drain(bar + C::B_KV, 0);
+        for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t)
+          mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
+        for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t)
+          mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
       }
     }
   } else if (warp == 1) {
@@ -279,14 +397,27 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
     const int sw = warp - 2, grp = sw >> 2, cb = grp * 64;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row
-    const int j = k0 + row;
+    const int j = k0 + row;  // key (compact index when gathered)
+    // original key index (recomputed where needed, to keep registers free)
+    auto orig = [&]() -> int { return gat ? (j < Skv ? __ldg(pos_h + j) : 0) : j; };
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     int ilo, ihi;
-    col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
-    bool kept = j < p.Sk;
-    if (kept && p.mask.keep) kept = (__ldg(p.mask.keep + (size_t)bh * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
-    const float kb = (j < p.Sk && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bh * p.Sk + j) : 0.f;
-    const float kt = (kb - p.mask.slope * (float)j) * kLog2e;  // per-key score term, log2 units
+    float kt;  // per-key score term, log2 units
+    bool kept = j < Skv;
+    {
+      const int jo = orig();
+      if (gat) {
+        ilo = max(0, jo - delta);
+        ihi = p.Sq - 1;
+      } else {
+        col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
+      }
+      if (kept && p.mask.keep && !gat)
+        kept = (__ldg(p.mask.keep + (size_t)bh * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
+      const float kb = (j < Skv && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bh * p.Sk + jo) : 0.f;
+      kt = (kb - p.mask.slope * (float)jo) * kLog2e;
+    }
+    float dbs = 0.f;  // key-bias gradient: this half's sum of dS^T (before the softcap factor)
     int n = 0;
     bool ok = true;
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -387,6 +518,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
           float d1 = bf_hi(p01) * (__uint_as_float(r[4 * c4 + 1]) - d4.y);
           float d2 = bf_lo(p23) * (__uint_as_float(r[4 * c4 + 2]) - d4.z);
           float d3 = bf_hi(p23) * (__uint_as_float(r[4 * c4 + 3]) - d4.w);
+          if constexpr (DB) dbs += (d0 + d1) + (d2 + d3);
           if constexpr (CAP) {
             d0 *= bf_lo(dc[2 * c4]);
             d1 *= bf_hi(dc[2 * c4]);
@@ -418,9 +550,20 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         ok = __all_sync(0xffffffffu, mbar_wait(bar + C::B_DONE, 0, abort_flag));
         tc_fence_after();
       }
+      const bool jin = j < Skv;
+      const int jo = orig();
+      if constexpr (DB) {
+        // key-bias gradient of this key: both halves' sums
+        if (ok && grp == 1) {
+          sDB[row] = dbs;
+          mbar_arrive(bar + C::B_FIN);
+        } else if (ok && mbar_wait(bar + C::B_FIN, 0, abort_flag) && jin) {
+          p.dbias[(size_t)bh * p.Sk + jo] = dbs + sDB[row];
+        }
+      }
       if (ok) {
-        __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + j) * DV;
-        __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + j) * DQK;
+        __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + jo) * DV;
+        __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + jo) * DQK;
 #pragma unroll 1
         for (int c0 = grp * 32; c0 < DV + DQK; c0 += 64) {
           const bool isv = c0 < DV;
@@ -434,7 +577,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
           }
           const float sc = isv ? 1.f : p.scale;
           __nv_bfloat16* dst = isv ? dvrow + c0 : dkrow + (c0 - DV);
-          if (j < p.Sk) {
+          if (jin) {
 #pragma unroll
             for (int c = 0; c < 32; c += 8)
               *reinterpret_cast<uint4*>(dst + c) =
@@ -475,13 +618,13 @@ struct DqCfg {
          B_DQD, B_DONE, B_DRAIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
-      1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + TCAP * 2 + NBAR * 8 + 16 + 2048;
+      1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + TCAP * 2 + NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t ID_DQ = idesc_bf16(128, DQK, false, true);
 };
 
-template <int DQK, int DV, bool CAP>
+template <int DQK, int DV, bool CAP, bool GAT>
 __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -496,26 +639,46 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
+  int* gcount = reinterpret_cast<int*>(tmem_slot + 4);  // [2] gathered keys seen by the first / last row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqt = (p.Sq + 127) / 128;
   const int bh = blockIdx.x % BH;
   const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * 128;
+  constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
+  const int Skv = p.Skv;
+  const int delta = p.Sk - p.Sq;
+  const uint32_t* keep_h = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
+  const int32_t* pos_h = gat ? p.kidx + (size_t)bh * p.Sk : nullptr;
 
   TileWalk walk;
   int nslots;
-  if (p.has_lists) {
+  int c_first = 0, c_last = 0;
+  if (gat) {
+    nslots = (Skv + 127) / 128;
+  } else if (p.has_lists) {
     walk = make_walk(p.qmc, p.qmi, p.qfc, p.qfi, bh * p.nqb + q0 / p.sparse_m, p.nkb, p.sub_k, p.Sk);
     nslots = walk.nslots;
   } else {
     nslots = (p.Sk + 127) / 128;
   }
   auto slot = [&](int s, int* kv0, bool* masked) -> bool {
+    if (gat) return gathered_slot_rows(s, c_first, c_last, kv0, masked);
     return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
                        : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
   };
-  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (warp == 0) {
+    if (gat) {
+      c_first = warp_kept_upto(keep_h, p.mask.nkw, q0 + delta);
+      c_last = warp_kept_upto(keep_h, p.mask.nkw, min(q0 + 127, p.Sq - 1) + delta);
+      if (lane == 0) {
+        gcount[0] = c_first;
+        gcount[1] = c_last;
+      }
+    }
+    build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  }
   if (threadIdx.x == 32) {
     for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_DS || b == C::B_RS || b == C::B_RP) ? 256 : 1);
     *abort_flag = 0;
@@ -527,40 +690,97 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = *tcount;
+  if (gat && warp != 0) {
+    c_first = gcount[0];
+    c_last = gcount[1];
+  }
 
   if (warp == 0) {
-    if (lane == 0) {
+    if constexpr (!GAT) {
+      if (lane == 0) {
+        int n = 0, nk = 0, nv = 0;
+        bool ok = true;
+        auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+        int kv0;
+        bool masked;
+        while (ok && it.next(&kv0, &masked)) {
+          if (n == 0) {
+            mbar_expect_tx(bar + C::B_QG, C::QTILE + C::VTILE);
+            for (int j = 0; j < C::NQSLAB; ++j)
+              tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, bar + C::B_QG, j * (C::SWQ / 2), q0, bh);
+            for (int j = 0; j < C::NVSLAB; ++j)
+              tma_load_3d(sG + j * C::VSLAB, &p.tm_do, bar + C::B_QG, j * (C::SWV / 2), q0, bh);
+          }
+          const int ks = n % C::KST;
+          if (n >= C::KST && !(ok = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
+          for (int j = 0; j < C::NQSLAB; ++j)
+            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bh);
+          ++nk;
+          const int vs = n % C::VST;
+          if (n >= C::VST && !(ok = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
+          for (int j = 0; j < C::NVSLAB; ++j)
+            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, bar + C::B_VF + vs, j * (C::SWV / 2), kv0, bh);
+          ++nv;
+          ++n;
+        }
+        if (*abort_flag) {
+          if (nk > 0) mbar_drain(bar + C::B_QG, 0);
+          for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t)
+            mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
+          for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t)
+            mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
+        }
+      }
+    } else {
+      // gathered keys: lane 0 waits and issues Q / dO; every lane gathers 4
+      // rows of each K and V tile
       int n = 0, nk = 0, nv = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
       int kv0;
       bool masked;
       while (ok && it.next(&kv0, &masked)) {
-        if (n == 0) {
+        if (n == 0 && lane == 0) {
           mbar_expect_tx(bar + C::B_QG, C::QTILE + C::VTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
             tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, bar + C::B_QG, j * (C::SWQ / 2), q0, bh);
           for (int j = 0; j < C::NVSLAB; ++j)
             tma_load_3d(sG + j * C::VSLAB, &p.tm_do, bar + C::B_QG, j * (C::SWV / 2), q0, bh);
         }
+        int gr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
         const int ks = n % C::KST;
-        if (n >= C::KST && !(ok = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
+        bool w = true;
+        if (lane == 0 && n >= C::KST) w = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag);
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+        if (lane == 0) mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
+        __syncwarp();
+#pragma unroll
         for (int j = 0; j < C::NQSLAB; ++j)
-          tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bh);
+          tma_gather4(sK + ks * C::QTILE + j * C::QSLAB + 4 * lane * C::SWQ, &p.tm_k, bar + C::B_KF + ks,
+                      j * (C::SWQ / 2), gr[0], gr[1], gr[2], gr[3]);
         ++nk;
         const int vs = n % C::VST;
-        if (n >= C::VST && !(ok = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
+        if (lane == 0 && n >= C::VST) w = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag);
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+        if (lane == 0) mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
+        __syncwarp();
+#pragma unroll
         for (int j = 0; j < C::NVSLAB; ++j)
-          tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, bar + C::B_VF + vs, j * (C::SWV / 2), kv0, bh);
+          tma_gather4(sV + vs * C::VTILE + j * C::VSLAB + 4 * lane * C::SWV, &p.tm_v, bar + C::B_VF + vs,
+                      j * (C::SWV / 2), gr[0], gr[1], gr[2], gr[3]);
         ++nv;
         ++n;
       }
-      if (*abort_flag) {
+      if (lane == 0 && *abort_flag) {
         if (nk > 0) mbar_drain(bar + C::B_QG, 0);
-        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
-        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
+        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t)
+          mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
+        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t)
+          mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
       }
     }
   } else if (warp == 1) {
@@ -641,12 +861,13 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
     const int row = quarter * 32 + lane;
     const int i = q0 + row;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    int lo, hi;
-    row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
+    int lo = 0, hi;
+    if constexpr (GAT) hi = gathered_row_hi(keep_h, p.mask.nkw, q0 + quarter * 32 + delta);
+    else row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
     const float l2 = p.lse2[(size_t)bh * p.sq_pad + i];
     const float dl = p.delta[(size_t)bh * p.sq_pad + i];
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
-    const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
+    const uint32_t* keep = gat ? nullptr : keep_h;  // gathered keys are all kept
     int n = 0;
     bool ok = true;
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -658,7 +879,11 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
       for (int e = 0; e < 2; ++e) {
         const int jj = kv0 + cb + e * 32 + lane;
         float c = 0.f;
-        if (jj < p.Sk) c = ((kb ? __ldg(kb + jj) : 0.f) - p.mask.slope * (float)jj) * kLog2e;
+        if (jj < Skv) {
+          int jo = jj;  // original key index
+          if constexpr (GAT) jo = __ldg(pos_h + jj);
+          c = ((kb ? __ldg(kb + jo) : 0.f) - p.mask.slope * (float)jo) * kLog2e;
+        }
         ctw[e * 32 + lane] = c;
       }
       __syncwarp();
@@ -671,7 +896,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         }
       }
       const int clo = masked ? lo - kv0 - cb : 0;
-      const int chi = masked ? min(hi, p.Sk - 1) - kv0 - cb : 63;
+      const int chi = masked ? min(hi, Skv - 1) - kv0 - cb : 63;
       ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -803,34 +1028,54 @@ static int set_smem_once(K kern, int bytes, bool* flag) {
   return GBATTN_OK;
 }
 
-template <int DQK, int DV, bool CAP>
+template <int DQK, int DV, bool CAP, bool GAT, bool DB>
 static int launch_bwd_main(const BwdParams& prm, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H;
   static bool f1 = false, f2 = false;
-  if (set_smem_once(dkdv_kernel<DQK, DV, CAP>, DkdvCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
-  dkdv_kernel<DQK, DV, CAP><<<((s.Sk + 127) / 128) * BH, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  if (set_smem_once(dq_kernel<DQK, DV, CAP>, DqCfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
-  dq_kernel<DQK, DV, CAP><<<((s.Sq + 127) / 128) * BH, 320, DqCfg<DQK, DV>::SMEM, st>>>(prm);
+  if (set_smem_once(dkdv_kernel<DQK, DV, CAP, GAT, DB>, DkdvCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
+  const int nkt = (prm.Skv + 127) / 128;  // key tiles (compact tiles when gathered)
+  if (nkt > 0) {
+    dkdv_kernel<DQK, DV, CAP, GAT, DB><<<nkt * BH, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  }
+  if (set_smem_once(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
+  dq_kernel<DQK, DV, CAP, GAT><<<((s.Sq + 127) / 128) * BH, 320, DqCfg<DQK, DV>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+template <int DQK, int DV, bool CAP, bool GAT>
+static int launch_bwd_db(const BwdParams& prm, const Shape& s, cudaStream_t st) {
+  return prm.dbias ? launch_bwd_main<DQK, DV, CAP, GAT, true>(prm, s, st)
+                   : launch_bwd_main<DQK, DV, CAP, GAT, false>(prm, s, st);
 }
 
 template <int DQK, int DV>
 static int launch_bwd_cap(const BwdParams& prm, const Shape& s, bool cap, cudaStream_t st) {
-  return cap ? launch_bwd_main<DQK, DV, true>(prm, s, st) : launch_bwd_main<DQK, DV, false>(prm, s, st);
+  if (prm.gather)
+    return cap ? launch_bwd_db<DQK, DV, true, true>(prm, s, st) : launch_bwd_db<DQK, DV, false, true>(prm, s, st);
+  return cap ? launch_bwd_db<DQK, DV, true, false>(prm, s, st) : launch_bwd_db<DQK, DV, false, false>(prm, s, st);
 }
 
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, float scale, const HostMask& m, void* dq, void* dk, void* dv,
-                    void* ws, cudaStream_t st) {
+                    float* dkey_bias, void* ws, cudaStream_t st) {
   BwdParams prm;
   memset(&prm, 0, sizeof(prm));
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+  if (m.gather) {
+    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BH * s.Sk, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BH * s.Sk, swv)) return GBATTN_ERR_CUDA;
+  } else {
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+  }
   if (!make_tmap_bf16_3d(&prm.tm_do, dout, s.Dv, s.Sq, BH, swv)) return GBATTN_ERR_CUDA;
+  prm.gather = m.gather;
+  prm.Skv = m.gather ? m.kept : s.Sk;
+  prm.kidx = m.gather ? m.keep_idx : nullptr;
+  prm.dbias = dkey_bias;
   prm.B = s.B;
   prm.H = s.H;
   prm.Sq = s.Sq;
@@ -850,8 +1095,8 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.mask.key_bias = m.key_bias;
   prm.mask.keep = m.kind == GBATTN_MASK_DYNAMIC_TOPK ? m.keep : nullptr;
   prm.mask.nkw = (s.Sk + 31) / 32;
-  prm.has_lists = m.has_lists;
-  if (m.has_lists) {
+  prm.has_lists = m.gather ? 0 : m.has_lists;
+  if (prm.has_lists) {
     prm.sub_q = m.sparse_m / 128;
     prm.sub_k = m.sparse_n / 128;
     prm.nqb = m.nqb;
@@ -882,6 +1127,13 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, BH, s.Sq, prm.sq_pad, s.Dv,
       m.slope * kLog2e, delta, lse2);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  if (m.gather) {
+    // rows of the keys outside the keep set: zero gradients
+    const long long warps = (long long)BH * prm.mask.nkw;
+    unkept_zero_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(
+        m.keep, prm.mask.nkw, BH, s.Sk, s.Dqk, s.Dv, prm.dk, prm.dv, dkey_bias);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  }
   const bool cap = m.softcap > 0.f;
   if (s.Dqk == 32 && s.Dv == 32) return launch_bwd_cap<32, 32>(prm, s, cap, st);
   if (s.Dqk == 64 && s.Dv == 64) return launch_bwd_cap<64, 64>(prm, s, cap, st);

@@ -26,6 +26,11 @@
 // Keeping Q in TMEM means the QK^T MMA reads only K from shared memory; the
 // shared-memory traffic per tile (K + V reads, K + V TMA writes) then fits
 // the time of the two MMAs.
+// Gathered keys (dynamic top-k mask with its kept-key index list): the key
+// tiles are compact tiles of kept keys only, built by TMA row gathers (each
+// producer lane gathers 4 of the 128 rows); the bias and rel-bias terms use
+// each key's original index and the element mask is the prefix of compact
+// keys each row sees. No key outside the keep set is loaded or multiplied.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv), Q [384, 384+Dqk/2).
 #include "kernels.h"
 #include "mask.cuh"
@@ -41,6 +46,9 @@ struct FwdParams {
   float cap_post;      // softcap * log2(e)
   MaskParams mask;
   int has_lists;
+  int gather;          // gathered keys: tm_k / tm_v are 2-D row-gather maps
+  int Skv;             // streamed key extent (Sk, or the kept-key count)
+  const int32_t* kidx; // [B*H, Sk] kept key indices (gathered keys)
   int sub;             // sparse_n / 128
   int nqb, nkb, sparse_m;
   const int32_t *mcnt, *midx, *fcnt, *fidx;  // forward lists
@@ -71,7 +79,7 @@ struct FwdCfg {
   // colterm [8 warps][2][64] + row-max exchange [2][2][128] + row sums [2][128]
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 4 * 128 * 4 + 2 * 128 * 4 +
-                                   TCAP * 2 + NBAR * 8 + 16 + 2048;
+                                   TCAP * 2 + NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
@@ -89,7 +97,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
   reg_fence32(r + 96);
 }
 
-template <int DQK, int DV, bool CAP>
+template <int DQK, int DV, bool CAP, bool GAT>
 __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +125,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
+  int* gcount = reinterpret_cast<int*>(tmem_slot + 4);  // [2] gathered keys seen by the first / last row
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -125,11 +134,19 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
   const int bh = L % BH;
   const int q0 = qt * 128;
+  constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
+  const int Skv = p.Skv;
+  const int delta = p.Sk - p.Sq;
+  const uint32_t* keep_h = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
+  const int32_t* pos_h = gat ? p.kidx + (size_t)bh * p.Sk : nullptr;
 
   // Tile walk of this CTA; warp 0 compacts it into shared memory once.
   TileWalk walk;
   int nslots;
-  if (p.has_lists) {
+  int c_first = 0, c_last = 0;
+  if (gat) {
+    nslots = (Skv + 127) / 128;
+  } else if (p.has_lists) {
     const int r = q0 / p.sparse_m;
     walk = make_walk(p.mcnt, p.midx, p.fcnt, p.fidx, bh * p.nqb + r, p.nkb, p.sub, p.Sk);
     nslots = walk.nslots;
@@ -137,10 +154,21 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     nslots = (p.Sk + 127) / 128;
   }
   auto slot = [&](int s, int* kv0, bool* masked) -> bool {
+    if (gat) return gathered_slot_rows(s, c_first, c_last, kv0, masked);
     return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
                        : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
   };
-  if (warp == 0) build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  if (warp == 0) {
+    if (gat) {
+      c_first = warp_kept_upto(keep_h, p.mask.nkw, q0 + delta);
+      c_last = warp_kept_upto(keep_h, p.mask.nkw, min(q0 + 127, p.Sq - 1) + delta);
+      if (lane == 0) {
+        gcount[0] = c_first;
+        gcount[1] = c_last;
+      }
+    }
+    build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
+  }
   if (threadIdx.x == 32) {
     mbar_init(q_full, 1);
     mbar_init(q_tmem, 128);
@@ -160,37 +188,90 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   const int ntiles = *tcount;
   const bool any_tile = ntiles > 0;
+  if (gat && warp != 0) {
+    c_first = gcount[0];
+    c_last = gcount[1];
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && any_tile) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      mbar_expect_tx(q_full, C::QTILE);
-      for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+    if constexpr (!GAT) {
+      if (lane == 0 && any_tile) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        mbar_expect_tx(q_full, C::QTILE);
+        for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+        int n = 0, nk = 0, nv = 0;
+        bool ok = true;
+        auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+        int kv0;
+        bool masked;
+        while (ok && it.next(&kv0, &masked)) {
+          const int ks = n % C::KST;
+          if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(k_full + ks, C::QTILE);
+          for (int j = 0; j < C::NQSLAB; ++j)
+            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bh);
+          ++nk;
+          const int vs = n % C::VST;
+          if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
+          mbar_expect_tx(v_full + vs, C::VTILE);
+          for (int j = 0; j < C::NVSLAB; ++j)
+            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bh);
+          ++nv;
+          ++n;
+        }
+        if (*abort_flag) {
+          // let every copy this thread started land before the CTA exits
+          mbar_drain(q_full, 0);
+          for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
+          for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
+        }
+      }
+    } else if (any_tile) {
+      // gathered keys: lane 0 waits and issues Q; every lane gathers 4 rows
+      // of each K and V tile
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        mbar_expect_tx(q_full, C::QTILE);
+        for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+      }
       int n = 0, nk = 0, nv = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
       int kv0;
       bool masked;
       while (ok && it.next(&kv0, &masked)) {
+        int gr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
         const int ks = n % C::KST;
-        if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(k_full + ks, C::QTILE);
+        bool w = true;
+        if (lane == 0 && n >= C::KST) w = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag);
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+        if (lane == 0) mbar_expect_tx(k_full + ks, C::QTILE);
+        __syncwarp();
+#pragma unroll
         for (int j = 0; j < C::NQSLAB; ++j)
-          tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bh);
+          tma_gather4(sK + ks * C::QTILE + j * C::QSLAB + 4 * lane * C::SWQ, &p.tm_k, k_full + ks, j * (C::SWQ / 2),
+                      gr[0], gr[1], gr[2], gr[3]);
         ++nk;
         const int vs = n % C::VST;
-        if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
-        mbar_expect_tx(v_full + vs, C::VTILE);
+        if (lane == 0 && n >= C::VST) w = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag);
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+        if (lane == 0) mbar_expect_tx(v_full + vs, C::VTILE);
+        __syncwarp();
+#pragma unroll
         for (int j = 0; j < C::NVSLAB; ++j)
-          tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bh);
+          tma_gather4(sV + vs * C::VTILE + j * C::VSLAB + 4 * lane * C::SWV, &p.tm_v, v_full + vs, j * (C::SWV / 2),
+                      gr[0], gr[1], gr[2], gr[3]);
         ++nv;
         ++n;
       }
-      if (*abort_flag) {
-        // let every copy this thread started land before the CTA exits
+      if (lane == 0 && *abort_flag) {
         mbar_drain(q_full, 0);
         for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
         for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
@@ -253,10 +334,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     const int cb = grp * 64;       // first S column of this thread
     constexpr int DVH = DV / 2;    // O columns of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    int lo, hi;
-    row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
+    int lo = 0, hi;
+    if constexpr (GAT) hi = gathered_row_hi(keep_h, p.mask.nkw, q0 + quarter * 32 + delta);
+    else row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
-    const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
+    const uint32_t* keep = GAT ? nullptr : keep_h;  // gathered keys are all kept
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     bool ok = true;
@@ -298,7 +380,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       for (int e = 0; e < 2; ++e) {
         const int j = kv0 + cb + e * 32 + lane;
         float c = 0.f;
-        if (j < p.Sk) c = ((kb ? __ldg(kb + j) : 0.f) - p.mask.slope * (float)j) * kLog2e;
+        if (j < Skv) {
+          int jo = j;  // original key index
+          if constexpr (GAT) jo = __ldg(pos_h + j);
+          c = ((kb ? __ldg(kb + jo) : 0.f) - p.mask.slope * (float)jo) * kLog2e;
+        }
         ctw[e * 32 + lane] = c;
       }
       __syncwarp();
@@ -329,7 +415,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       }
       if (masked) {
         const int clo = lo - kv0 - cb;
-        const int chi = min(hi, p.Sk - 1) - kv0 - cb;
+        const int chi = min(hi, Skv - 1) - kv0 - cb;
         if (keep) {
           uint32_t kw[2];
 #pragma unroll
@@ -475,10 +561,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int DQK, int DV, bool CAP>
+template <int DQK, int DV, bool CAP, bool GAT>
 static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
-  auto kern = fwd_bf16_kernel<DQK, DV, CAP>;
+  auto kern = fwd_bf16_kernel<DQK, DV, CAP, GAT>;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
@@ -491,7 +577,9 @@ static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
 
 template <int DQK, int DV>
 static int launch_fwd_cap(const FwdParams& prm, int grid, bool cap, cudaStream_t st) {
-  return cap ? launch_fwd<DQK, DV, true>(prm, grid, st) : launch_fwd<DQK, DV, false>(prm, grid, st);
+  if (prm.gather)
+    return cap ? launch_fwd<DQK, DV, true, true>(prm, grid, st) : launch_fwd<DQK, DV, false, true>(prm, grid, st);
+  return cap ? launch_fwd<DQK, DV, true, false>(prm, grid, st) : launch_fwd<DQK, DV, false, false>(prm, grid, st);
 }
 
 int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, const HostMask& m,
@@ -501,8 +589,16 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+  if (m.gather) {
+    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BH * s.Sk, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BH * s.Sk, swv)) return GBATTN_ERR_CUDA;
+  } else {
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+  }
+  prm.gather = m.gather;
+  prm.Skv = m.gather ? m.kept : s.Sk;
+  prm.kidx = m.gather ? m.keep_idx : nullptr;
   prm.B = s.B;
   prm.H = s.H;
   prm.Sq = s.Sq;
@@ -522,8 +618,8 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.mask.key_bias = m.key_bias;
   prm.mask.keep = m.kind == GBATTN_MASK_DYNAMIC_TOPK ? m.keep : nullptr;
   prm.mask.nkw = (s.Sk + 31) / 32;
-  prm.has_lists = m.has_lists;
-  if (m.has_lists) {
+  prm.has_lists = m.gather ? 0 : m.has_lists;
+  if (prm.has_lists) {
     prm.sub = m.sparse_n / 128;
     prm.nqb = m.nqb;
     prm.nkb = m.nkb;

@@ -25,11 +25,18 @@ struct HostMask {
   int sparse_m, sparse_n, nqb, nkb;
   const int32_t *q_mask_cnt, *q_mask_idx, *q_full_cnt, *q_full_idx;
   const int32_t *k_mask_cnt, *k_mask_idx, *k_full_cnt, *k_full_idx;
+  // gathered keys (bf16 DYNAMIC_TOPK with the kept-key index list): the
+  // kernels stream only the `kept` = min(topk, Sk) keys listed in keep_idx
+  int gather, kept;
+  const int32_t* keep_idx;
 };
 
 // Encodes a 3-D bf16 tensor map over [BH, S, D] (D innermost) with a box of
 // (swizzle_bytes/2) x 128 x 1 and the given swizzle (64 or 128 bytes).
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes);
+// Encodes a 2-D bf16 tensor map over [rows, D] with a box one row high and
+// (swizzle_bytes/2) wide, for TMA row gathers (tile::gather4).
+bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, int D, long long rows, int swizzle_bytes);
 
 // Kernel launchers: return GBATTN_OK or GBATTN_ERR_CUDA.
 int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale,
@@ -38,10 +45,10 @@ int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
                     const HostMask& m, float* o, float* lse, cudaStream_t st);
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o,
                     const void* dout, const float* lse, float scale, const HostMask& m, void* dq, void* dk,
-                    void* dv, void* ws, cudaStream_t st);
+                    void* dv, float* dkey_bias, void* ws, cudaStream_t st);
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
                     const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
-                    float* dv, void* ws, cudaStream_t st);
+                    float* dv, float* dkey_bias, void* ws, cudaStream_t st);
 int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
                    int num_splits, void* o, float* lse, void* ws, cudaStream_t st);
 // Split-KV forward with its split partials in the library's static scratch

@@ -9,6 +9,12 @@
 // (a = i + Sk - Sq), every closed-form kind allows, for query i, one interval
 // of keys [lo_i, hi_i]; lo_i and hi_i never decrease with i. The dynamic kind
 // is the causal interval intersected with a per-(b,h) keep bitmask.
+//
+// Gathered keys (dynamic kind with the kept-key index list): the kernels
+// stream only the kept keys, in ascending index order, as compact tiles.
+// Compact key c stands for key pos[c]; query i sees compact keys
+// [0, kept(<= i + Sk - Sq)), a prefix, so the tile classes and the element
+// masks reduce to one count per query row (and one position per key).
 #pragma once
 
 #include "common.cuh"
@@ -25,6 +31,75 @@ struct MaskParams {
   const uint32_t* keep;    // [B*H, nkw] (dynamic) or nullptr
   int nkw;                 // words per (b,h) in keep
 };
+
+// ---- gathered keys ----------------------------------------------------------
+// Number of kept keys with index <= a among the keep bits of one head (nkw
+// words); warp-collective (every lane gets the count), a warp-uniform.
+__device__ __forceinline__ int warp_kept_upto(const uint32_t* keep, int nkw, int a) {
+  if (a < 0) return 0;
+  const int lane = threadIdx.x & 31;
+  const int wa = min(a >> 5, nkw - 1);
+  const uint32_t last = (a >> 5) > wa ? 0xffffffffu : ((2u << (a & 31)) - 1u);
+  int cnt = 0;
+#pragma unroll 4
+  for (int w = lane; w <= wa; w += 32) {
+    const uint32_t b = __ldg(keep + w);
+    cnt += __popc(w == wa ? (b & last) : b);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  return cnt;
+}
+
+// Kept keys with index in [lo, hi] (a short range: a few words).
+__device__ __forceinline__ int kept_between(const uint32_t* keep, int nkw, int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, nkw * 32 - 1);
+  int cnt = 0;
+  for (int w = lo >> 5; w <= (hi >> 5); ++w) {
+    uint32_t b = __ldg(keep + w);
+    const int wb = w << 5;
+    if (lo > wb) b &= ~((1u << (lo - wb)) - 1u);
+    if (hi < wb + 31) b &= (2u << (hi - wb)) - 1u;
+    cnt += __popc(b);
+  }
+  return cnt;
+}
+
+// Compact-key count seen by each query row of a warp (32 consecutive rows
+// i0 + lane, i.e. positions a0 + lane with a0 = i0 + Sk - Sq): returns the
+// lane's last visible compact key (count - 1; -1 when none). Warp-collective.
+__device__ __forceinline__ int gathered_row_hi(const uint32_t* keep, int nkw, int a0) {
+  const int lane = threadIdx.x & 31;
+  const int base = warp_kept_upto(keep, nkw, a0 - 1);
+  const int a = a0 + lane;
+  const int extra = a < 0 ? 0 : kept_between(keep, nkw, max(a0, 0), a);
+  return base + extra - 1;
+}
+
+// Forward direction (fixed 128-row query tile, streamed compact key tiles):
+// c_first / c_last = compact keys visible to the tile's first / last row.
+__device__ __forceinline__ bool gathered_slot_rows(int s, int c_first, int c_last, int* start, bool* masked) {
+  const int st = s * 128;
+  if (st >= c_last) return false;
+  *start = st;
+  *masked = st + 128 > c_first;
+  return true;
+}
+
+// Backward direction (fixed compact key tile, streamed 128-row query tiles):
+// p_first / p_last = original index of the tile's first / last key; kfull =
+// the key tile has 128 keys; delta = Sk - Sq. Query i sees key p iff
+// p <= i + delta.
+__device__ __forceinline__ bool gathered_slot_cols(int s, int p_first, int p_last, bool kfull, int delta, int Sq,
+                                                   int* start, bool* masked) {
+  const int st = s * 128;
+  const int q1 = min(st + 128, Sq);
+  if (st >= Sq || p_first > q1 - 1 + delta) return false;
+  *start = st;
+  *masked = !(kfull && q1 - st == 128 && p_last <= st + delta);
+  return true;
+}
 
 // Allowed keys of query i: [lo, hi] (inclusive, clipped to [0, Sk-1]);
 // empty when lo > hi.

@@ -25,6 +25,7 @@ struct SimtParams {
   const int32_t *kmc, *kmi, *kfc, *kfi;  // backward lists (per k-block)
   const float *q, *k, *v, *o, *dout, *lse;
   float *out, *lse_out, *dq, *dk, *dv, *delta;
+  float* dbias;  // [B*H, Sk] key-bias gradient, or nullptr
 };
 
 // Score of (i, j) from a raw dot product, in natural-log units, and the
@@ -290,10 +291,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
     sV[e] = (k0 + r < p.Sk) ? p.v[((size_t)bh * p.Sk + k0 + r) * DV + d] : 0.f;
   }
   float ak[16][4], av[16][4];
+  float dbk[16];  // key-bias gradient: this lane's rows' sum of dS (before the softcap factor)
   int lo[16], hi[16];
   bool kept[16];
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
+    dbk[kk] = 0.f;
 #pragma unroll
     for (int t = 0; t < 4; ++t) ak[kk][t] = av[kk][t] = 0.f;
     const int j = k0 + warp * 16 + kk;
@@ -338,7 +341,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
         const float sc = simt_score(p, dot, i, j, kb, &dcap);
         const bool al = kept[kk] && i >= lo[kk] && i <= hi[kk] && i < p.Sq && lse != -INFINITY;
         const float pj = al ? expf(sc - lse) : 0.f;
-        const float ds = pj * (dp - dl) * dcap;
+        const float ds0 = pj * (dp - dl);
+        dbk[kk] += ds0;
+        const float ds = ds0 * dcap;
         for (int ii = 0; ii < kChunk; ++ii) {
           const float pb = __shfl_sync(0xffffffffu, pj, ii);
           const float db = __shfl_sync(0xffffffffu, ds, ii);
@@ -355,7 +360,11 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const int j = k0 + warp * 16 + kk;
+    float db = dbk[kk];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
     if (j >= p.Sk) continue;
+    if (p.dbias && lane == 0) p.dbias[(size_t)bh * p.Sk + j] = db;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int d = lane + 32 * t;
@@ -425,8 +434,8 @@ int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
 }
 
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o, const float* dout,
-                    const float* lse, float scale, const HostMask& m, float* dq, float* dk, float* dv, void* ws,
-                    cudaStream_t st) {
+                    const float* lse, float scale, const HostMask& m, float* dq, float* dk, float* dv,
+                    float* dkey_bias, void* ws, cudaStream_t st) {
   SimtParams prm;
   fill_simt(prm, s, scale, m);
   prm.q = q;
@@ -438,6 +447,7 @@ int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;
+  prm.dbias = dkey_bias;
   const size_t BH = (size_t)s.B * s.H;
   prm.delta = reinterpret_cast<float*>(ws);
   const long long rows = (long long)BH * s.Sq;

@@ -76,8 +76,9 @@ enum {
  * Element-level mask and score modifiers, shared by every call.
  * Score of pair (i,j): s = scale * q_i.k_j; if softcap > 0, s = softcap *
  * tanh(s / softcap); then s += rel_bias_slope * (i - j) + key_bias[b,h,j].
- * The biases are constants (no gradient flows to them): the rel-bias
- * score_mod backward of [FA2C] returns the incoming gradient unchanged.
+ * The rel-bias is a constant: the rel-bias score_mod backward of [FA2C]
+ * returns the incoming gradient unchanged and nothing flows to the slope.
+ * attn_bwd can return the gradient of the key bias on request (dkey_bias).
  */
 typedef struct {
   int kind;             /* GBATTN_MASK_*                                        */
@@ -115,6 +116,14 @@ typedef struct {
   uint32_t* keep_bits;  /* [B,H,ceil(Sk/32)]: DYNAMIC_TOPK keep set, bit j%32 of word
                            j/32; written by build_block_mask, read by the kernels.
                            NULL allowed for the other kinds.                      */
+  int32_t* keep_idx;    /* [B,H,Sk] or NULL: DYNAMIC_TOPK kept-key index list, the
+                           min(topk,Sk) kept key indices of each (b,h) ascending,
+                           then 0 up to Sk; written by build_block_mask when not
+                           NULL. With it, the bf16 attn_fwd / attn_bwd gather only
+                           the kept keys into compact 128-key tiles (TMA row
+                           gathers) instead of walking the lists with the keep
+                           bits; the results are the same. Ignored for the other
+                           kinds and by the fp32 path.                             */
 } gbattn_blocks;
 
 /* Byte sizes of the block-list arrays for this shape (any of the out pointers
@@ -122,14 +131,15 @@ typedef struct {
 int gbattn_block_mask_sizes(int B, int H, int Sq, int Sk, int sparse_m, int sparse_n,
                             size_t* q_cnt_bytes, size_t* q_idx_bytes,
                             size_t* k_cnt_bytes, size_t* k_idx_bytes,
-                            size_t* keep_bits_bytes);
+                            size_t* keep_bits_bytes, size_t* keep_idx_bytes);
 
 /*
  * build_block_mask - classify every sparse block as absent / mask / full and
  * write the forward and backward lists into `out` ([FA2C]
  * `_build_block_sparse_masks_for_bwd`, restated for C). For DYNAMIC_TOPK it
- * first selects the keep set per (b,h) on the GPU and writes out->keep_bits.
- * The result is exact (integer work; the top-k compares fp32 biases).
+ * first selects the keep set per (b,h) on the GPU and writes out->keep_bits
+ * (and out->keep_idx when it is not NULL). The result is exact (integer work;
+ * the top-k compares fp32 biases).
  */
 int build_block_mask(int B, int H, int Sq, int Sk, const gbattn_mask* mask,
                      gbattn_blocks* out, gbattn_stream stream);
@@ -164,13 +174,19 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk
  * GBATTN_ERR_ARG). o and lse must be the outputs of attn_fwd for the same
  * inputs. workspace is device memory of at least attn_bwd_workspace_bytes();
  * its contents on entry do not matter.
+ * dkey_bias: NULL, or device [B,H,Sk] fp32 (4-byte aligned) that receives the
+ * gradient of the loss with respect to key_bias: dkey_bias[b,h,j] =
+ * sum_i P_ij (dP_ij - D_i) over the allowed pairs (the softcap factor does not
+ * apply: the bias is added after the cap). The dynamic keep set is held fixed
+ * (it changes only where two biases cross). Written for every key, 0 for keys
+ * no query sees; also defined when key_bias is NULL (the gradient at zero).
  */
 int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
              const void* q, const void* k, const void* v, const void* o,
              const void* dout, const float* lse, float scale,
              const gbattn_mask* mask, const gbattn_blocks* blocks, int deterministic,
-             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-             gbattn_stream stream);
+             void* dq, void* dk, void* dv, float* dkey_bias,
+             void* workspace, size_t workspace_bytes, gbattn_stream stream);
 
 /* Workspace bytes attn_fwd_splitkv needs: num_splits partial outputs
  * [n,B,H,Sq,Dv] fp32 and partial LSEs [n,B,H,Sq] fp32 (0 when num_splits == 1). */

@@ -223,17 +223,11 @@ class Problem:
         allk = np.arange(self.sk)
 
         def ds_block(rr, cc):
-            r0, s = self.scores(rr, cc)
-            m = self.mask(rr, cc)
-            lse = lse_all[rr]
-            live = np.isfinite(lse)
-            use = m & live[:, None]
-            p = np.exp(np.where(use, s - np.where(live, lse, 0.0)[:, None], -np.inf))
-            dp = do[rr] @ self.v[cc].T
-            ds = p * (dp - d_all[rr][:, None])
+            p, ds_s, r0 = self._p_ds(do, d_all, lse_all, rr, cc)
+            ds = ds_s
             if self.softcap > 0.0:
                 t = np.tanh(r0 / self.softcap)
-                ds = ds * (1.0 - t * t)
+                ds = ds_s * (1.0 - t * t)
             return p, ds
 
         dq = np.zeros((rows.shape[0], self.dqk))
@@ -249,6 +243,37 @@ class Problem:
             dk[c0:c0 + chunk] = self.scale * (ds.T @ self.q)
             dv[c0:c0 + chunk] = p.T @ do
         return dq, dk, dv, d_all
+
+    def _p_ds(self, do, d_all, lse_all, rr, cc):
+        """P and dL/ds (s = the score after the softcap and the biases) on
+        rows rr x cols cc, with the raw scaled score r0 for the softcap factor:
+        dL/ds_ij = P_ij (dP_ij - D_i)."""
+        r0, s = self.scores(rr, cc)
+        m = self.mask(rr, cc)
+        lse = lse_all[rr]
+        live = np.isfinite(lse)
+        use = m & live[:, None]
+        p = np.exp(np.where(use, s - np.where(live, lse, 0.0)[:, None], -np.inf))
+        dp = do[rr] @ self.v[cc].T
+        return p, p * (dp - d_all[rr][:, None]), r0
+
+    def dkey_bias(self, do, cols=None, chunk=2048):
+        """Gradient of L = <dO, O> with respect to the key bias:
+        dL/dkb_j = sum_i dL/ds_ij, because kb_j enters every score s_ij of key
+        j with coefficient 1 and is added after the softcap (so the tanh
+        factor does not apply). The dynamic keep set is held fixed (it is
+        piecewise constant in the bias). Returns dkb[cols]."""
+        do = np.asarray(do, dtype=np.float64)
+        cols = np.arange(self.sk) if cols is None else np.asarray(cols)
+        all_rows = np.arange(self.sq)
+        o_all, lse_all = self.forward(all_rows, chunk=chunk)
+        d_all = np.sum(do * o_all, axis=1)
+        out = np.zeros(cols.shape[0])
+        for c0 in range(0, cols.shape[0], chunk):
+            cc = cols[c0:c0 + chunk]
+            _, ds_s, _ = self._p_ds(do, d_all, lse_all, all_rows, cc)
+            out[c0:c0 + chunk] = ds_s.sum(axis=0)
+        return out
 
     # ---- split-KV ([FSA] split-KV forward; [PCB] merge algebra) ----
     @staticmethod
@@ -392,6 +417,19 @@ def keep_bits(key_bias, topk: int):
             keep = topk_keep(np.asarray(key_bias[b, h], dtype=np.float64), topk)
             for j in np.nonzero(keep)[0]:
                 out[b, h, j // 32] |= np.uint32(1) << np.uint32(j % 32)
+    return out
+
+
+def keep_index(key_bias, topk: int):
+    """Kept-key index list [B, H, Sk] int32: per (b, h) the indices of the
+    kept keys in ascending order, then 0 up to Sk (the library's gathered
+    dynamic path streams exactly these keys)."""
+    B, H, sk = key_bias.shape
+    out = np.zeros((B, H, sk), dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            kept = np.nonzero(topk_keep(np.asarray(key_bias[b, h], dtype=np.float64), topk))[0]
+            out[b, h, : kept.size] = kept
     return out
 
 

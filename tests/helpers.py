@@ -48,7 +48,7 @@ class Case:
     """Inputs on host and device, the GPU spec and lists, and the oracle spec."""
 
     def __init__(self, B, H, Sq, Sk, Dqk, Dv, kind="none", dtype="bf16", seed=42, sparse=(256, 512),
-                 use_bias=False, lists=True, **kw):
+                 use_bias=False, lists=True, gather=True, **kw):
         need_bias = use_bias or KIND[kind] == orc.DYNAMIC_TOPK
         self.shape = (B, H, Sq, Sk, Dqk, Dv)
         self.x = make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype, seed=seed, bias=need_bias)
@@ -58,7 +58,7 @@ class Case:
         self.lists = None
         if lists and (self.d["kind"] != orc.NONE or sparse is not None):
             sm, sn = sparse
-            self.lists = ga.alloc_block_lists(B, H, Sq, Sk, sm, sn)
+            self.lists = ga.alloc_block_lists(B, H, Sq, Sk, sm, sn, gather=gather)
             ga.build_block_mask(B, H, Sq, Sk, self.spec, self.lists)
         od = dict(self.d)
         if need_bias:
@@ -69,9 +69,14 @@ class Case:
     def fwd(self):
         return ga.attn_fwd(self.dev["q"], self.dev["k"], self.dev["v"], 0.0, self.spec, self.lists)
 
-    def bwd(self, o, lse, deterministic=False):
+    def bwd(self, o, lse, deterministic=False, dkey_bias=None):
         return ga.attn_bwd(self.dev["q"], self.dev["k"], self.dev["v"], o, self.dev["do"], lse, 0.0, self.spec,
-                           self.lists, deterministic=deterministic)
+                           self.lists, deterministic=deterministic, dkey_bias=dkey_bias)
+
+    def dbias_buffer(self):
+        B, H, Sq, Sk = self.shape[:4]
+        # filled with NaN so that a key the kernels skip shows up
+        return torch.full((B, H, Sk), float("nan"), dtype=torch.float32, device="cuda")
 
     def problem(self, b, h):
         kb = self.od.get("key_bias")
@@ -96,6 +101,13 @@ def check_lse(lg, l_ref, fp32=False):
     if (~inf_r).any():
         err = np.max(np.abs(lg[~inf_r] - l_ref[~inf_r]))
         assert err <= (1e-4 if fp32 else 2e-2), f"LSE err {err:.3e}"
+
+
+def check_dbias(g, r, fp32=False):
+    """Key-bias gradient: same bar as dQ/dK/dV (relative to max), and no NaN
+    (every key is written)."""
+    assert np.all(np.isfinite(g)), "dkey_bias has unwritten (NaN) entries"
+    return check_grad(g, r, "dkey_bias", fp32=fp32)
 
 
 def check_grad(g, r, name, fp32=False):

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         assert hasattr(lib, n), n
     assert set(bd.EXPORTS) >= set(declared_functions())
-    assert lib.gbattn_version() == 100
+    assert lib.gbattn_version() == 101
 
 
 def test_strerror_covers_codes():
@@ -45,12 +45,13 @@ def test_strerror_covers_codes():
 
 def test_block_mask_sizes():
     lib = ga.load_library()
-    sz = [ctypes.c_size_t() for _ in range(5)]
+    sz = [ctypes.c_size_t() for _ in range(6)]
     rc = lib.gbattn_block_mask_sizes(1, 16, 16384, 16384, 256, 512, *[ctypes.byref(s) for s in sz])
     assert rc == 0
-    assert [s.value for s in sz] == [16 * 64 * 4, 16 * 64 * 32 * 4, 16 * 32 * 4, 16 * 32 * 64 * 4, 16 * 512 * 4]
-    assert lib.gbattn_block_mask_sizes(1, 1, 100, 100, 100, 128, *[None] * 5) == bd.ERR_ARG
-    assert lib.gbattn_block_mask_sizes(0, 1, 100, 100, 128, 128, *[None] * 5) == bd.ERR_ARG
+    assert [s.value for s in sz] == [16 * 64 * 4, 16 * 64 * 32 * 4, 16 * 32 * 4, 16 * 32 * 64 * 4, 16 * 512 * 4,
+                                     16 * 16384 * 4]
+    assert lib.gbattn_block_mask_sizes(1, 1, 100, 100, 100, 128, *[None] * 6) == bd.ERR_ARG
+    assert lib.gbattn_block_mask_sizes(0, 1, 100, 100, 128, 128, *[None] * 6) == bd.ERR_ARG
 
 
 def test_workspace_queries():
@@ -105,9 +106,10 @@ def test_valid_call_without_gpu_reports_unsupported_device():
 def test_bwd_and_splitkv_argument_checks():
     lib = ga.load_library()
     args = [0, 1, 1, 128, 128, 64, 64] + [FAKE] * 6 + [0.0, None, None]
-    assert lib.attn_bwd(*args, 2, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == bd.ERR_ARG   # deterministic flag
-    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, 1 << 30, None) == bd.ERR_WORKSPACE
-    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE, 16, None) == bd.ERR_WORKSPACE
+    assert lib.attn_bwd(*args, 2, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, None) == bd.ERR_ARG   # deterministic flag
+    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, None, 1 << 30, None) == bd.ERR_WORKSPACE
+    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, FAKE, 16, None) == bd.ERR_WORKSPACE
+    assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 1 << 30, None) == bd.ERR_ALIGN  # dkey_bias
     sk = [0, 32, 32, 1, 65536, 128, 128, FAKE, FAKE, FAKE, 0.0, None]
     assert lib.attn_fwd_splitkv(*sk, 0, FAKE, FAKE, None, 0, None) == bd.ERR_ARG          # 0 splits
     assert lib.attn_fwd_splitkv(*sk, 4, FAKE, FAKE, None, 0, None) == bd.ERR_WORKSPACE

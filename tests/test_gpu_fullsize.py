@@ -8,7 +8,7 @@ import torch
 
 import block_sparse_attention_tma_gb300 as ga
 from block_sparse_attention_tma_gb300.synth import make_device_inputs
-from helpers import Case, check_grad, check_lse, check_out, f64, assert_no_device_error
+from helpers import Case, check_dbias, check_grad, check_lse, check_out, f64, assert_no_device_error
 from oracle import attention as orc
 
 pytestmark = pytest.mark.gpu
@@ -94,13 +94,20 @@ def test_dynamic_topk_1x16x8192(D):
     bits = orc.keep_bits(c.od["key_bias"], 2048)
     got = c.lists.tensors["keep_bits"].cpu().numpy().view(np.uint32).reshape(bits.shape)
     assert np.array_equal(got, bits)
+    idx = orc.keep_index(c.od["key_bias"], 2048)
+    got = c.lists.tensors["keep_idx"].cpu().numpy().reshape(idx.shape)
+    assert np.array_equal(got, idx)
+    # the gathered path (kept keys only), as bench.py runs it
     o, lse = c.fwd()
-    dq, dk, dv = c.bwd(o, lse)
+    db = c.dbias_buffer()
+    dq, dk, dv = c.bwd(o, lse, dkey_bias=db)
     torch.cuda.synchronize()
     assert_no_device_error()
     rows, cols = sample_idx(S, seed=1), sample_idx(S, seed=2)
     for h in (0, 9):
         check_rows_cols(c, 0, h, rows, cols, o, lse, (dq, dk, dv) if h == 0 else None)
+    check_dbias(f64(db[0, 0])[cols], c.problem(0, 0).dkey_bias(c.h["do"][0, 0], cols))
+    assert np.all(np.isfinite(f64(db)))
 
 
 @pytest.mark.parametrize("kind,extra", [("causal", {}), ("sliding", {}), ("block_diag", dict(block_size=1024)),

@@ -7,7 +7,7 @@ import torch
 
 import block_sparse_attention_tma_gb300 as ga
 from conftest import read_golden
-from helpers import Case, check_grad, check_lse, check_out, f64, assert_no_device_error
+from helpers import Case, check_dbias, check_grad, check_lse, check_out, f64, assert_no_device_error
 from oracle import attention as orc
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +25,10 @@ def lists_equal(c, B, H, Sq, Sk, sm, sn):
         bits = orc.keep_bits(c.od["key_bias"], c.od["topk"])
         g = c.lists.tensors["keep_bits"].cpu().numpy().view(np.uint32).reshape(bits.shape)
         assert np.array_equal(g, bits)
+        if "keep_idx" in c.lists.tensors:
+            idx = orc.keep_index(c.od["key_bias"], c.od["topk"])
+            g = c.lists.tensors["keep_idx"].cpu().numpy().reshape(idx.shape)
+            assert np.array_equal(g, idx)
 
 
 # ------------------------------------------------------------------ a1 build_block_mask
@@ -36,6 +40,13 @@ def test_block_mask_bit_exact(kind, Sq, Sk, sm, sn):
     torch.cuda.synchronize()
     lists_equal(c, 1, 2, Sq, Sk, sm, sn)
     assert_no_device_error()
+
+
+@pytest.mark.parametrize("topk", [0, 1, 33, 699, 700, 5000])
+def test_keep_index_bit_exact(topk):
+    c = Case(2, 2, 64, 700, 64, 64, "dynamic", topk=topk, sparse=(128, 128))
+    torch.cuda.synchronize()
+    lists_equal(c, 2, 2, 64, 700, 128, 128)
 
 
 def test_topk_ties_and_signed_zeros():
@@ -139,6 +150,80 @@ def test_gradients_are_bitwise_reproducible():
         assert torch.equal(x, y) and torch.equal(x, z)
 
 
+# ------------------------------------------------------------------ gathered dynamic path + key-bias gradient
+GATHER_CASES = [
+    # B, H, Sq, Sk, D, topk, extras
+    (1, 2, 900, 900, 64, 200, {}),
+    (1, 2, 1000, 1000, 32, 300, {}),
+    (2, 1, 700, 1000, 128, 300, dict(slope=0.01)),        # Sq < Sk
+    (1, 1, 1000, 700, 64, 650, {}),                       # Sq > Sk: leading rows see few keys
+    (1, 1, 640, 640, 64, 1, {}),                          # one kept key
+    (1, 1, 513, 513, 64, 600, {}),                        # topk >= Sk: every key kept
+    (1, 1, 777, 777, 128, 260, dict(softcap=2.0, slope=0.02)),
+    (1, 1, 640, 900, 192, 333, dict(slope=0.01)),         # MLA head dims
+]
+
+
+@pytest.mark.parametrize("gather", [True, False])
+@pytest.mark.parametrize("case", GATHER_CASES, ids=lambda c: f"{c[2]}x{c[3]}-d{c[4]}-k{c[5]}")
+def test_dynamic_forward_backward_dkey_bias(case, gather):
+    # gather=True streams only the kept keys (TMA row gathers); gather=False
+    # walks the block lists and tests the keep bits: both against the oracle
+    B, H, Sq, Sk, D, topk, ex = case
+    Dv = 128 if D == 192 else D
+    c = Case(B, H, Sq, Sk, D, Dv, "dynamic", topk=topk, sparse=(128, 128), gather=gather, **ex)
+    o, lse = c.fwd()
+    db = c.dbias_buffer()
+    dq, dk, dv = c.bwd(o, lse, dkey_bias=db)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for b in range(B):
+        for h in range(H):
+            p = c.problem(b, h)
+            o_ref, l_ref = p.forward()
+            check_out(f64(o[b, h]), o_ref)
+            check_lse(f64(lse[b, h]), l_ref)
+            dq_r, dk_r, dv_r, _ = p.backward(c.h["do"][b, h])
+            check_grad(f64(dq[b, h]), dq_r, "dQ")
+            check_grad(f64(dk[b, h]), dk_r, "dK")
+            check_grad(f64(dv[b, h]), dv_r, "dV")
+            check_dbias(f64(db[b, h]), p.dkey_bias(c.h["do"][b, h]))
+            # keys outside the keep set get exactly zero gradients
+            keep = orc.topk_keep(c.od["key_bias"][b, h], topk)
+            assert np.all(f64(dk[b, h])[~keep] == 0) and np.all(f64(dv[b, h])[~keep] == 0)
+            assert np.all(f64(db[b, h])[~keep] == 0)
+
+
+@pytest.mark.parametrize("case", [(1, 2, 600, 600, 64, "causal", {}),
+                                  (1, 1, 513, 769, 192, "sliding", dict(slope=0.01)),
+                                  (1, 1, 384, 384, 128, "none", dict(softcap=2.0)),
+                                  (1, 1, 600, 600, 32, "prefix_lm", dict(prefix_len=200)),
+                                  (1, 1, 512, 512, 64, "block_diag", dict(block_size=128))],
+                         ids=lambda c: c[5])
+def test_key_bias_gradient_bf16(case):
+    B, H, Sq, Sk, D, kind, ex = case
+    Dv = 128 if D == 192 else D
+    c = Case(B, H, Sq, Sk, D, Dv, kind, use_bias=True, sparse=(128, 256), **ex)
+    o, lse = c.fwd()
+    db = c.dbias_buffer()
+    c.bwd(o, lse, dkey_bias=db)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for h in range(H):
+        check_dbias(f64(db[0, h]), c.problem(0, h).dkey_bias(c.h["do"][0, h]))
+
+
+def test_gathered_gradients_are_bitwise_reproducible():
+    c = Case(1, 2, 900, 900, 64, 64, "dynamic", topk=300, sparse=(128, 128))
+    o, lse = c.fwd()
+    d1, d2 = c.dbias_buffer(), c.dbias_buffer()
+    a = c.bwd(o, lse, dkey_bias=d1)
+    b = c.bwd(o, lse, dkey_bias=d2)
+    torch.cuda.synchronize()
+    for x, y in zip(a + (d1,), b + (d2,)):
+        assert torch.equal(x, y)
+
+
 # ------------------------------------------------------------------ fp32 path
 @pytest.mark.parametrize("case", [(1, 1, 128, 128, 64, 64, "causal", {}),
                                   (1, 2, 200, 333, 48, 24, "sliding", dict(window=50, slope=0.02)),
@@ -161,6 +246,17 @@ def test_fp32_forward_backward(case):
         check_grad(f64(dq[0, h]), dq_r, "dQ", fp32=True)
         check_grad(f64(dk[0, h]), dk_r, "dK", fp32=True)
         check_grad(f64(dv[0, h]), dv_r, "dV", fp32=True)
+
+
+@pytest.mark.parametrize("kind,ex", [("dynamic", dict(topk=40)), ("causal", dict(softcap=1.5, slope=0.02))])
+def test_fp32_key_bias_gradient(kind, ex):
+    c = Case(1, 2, 150, 170, 32, 16, kind, dtype="fp32", use_bias=True, sparse=(128, 128), **ex)
+    o, lse = c.fwd()
+    db = c.dbias_buffer()
+    c.bwd(o, lse, dkey_bias=db)
+    torch.cuda.synchronize()
+    for h in range(2):
+        check_dbias(f64(db[0, h]), c.problem(0, h).dkey_bias(c.h["do"][0, h]), fp32=True)
 
 
 # ------------------------------------------------------------------ a6-a7 split-KV decode

@@ -139,6 +139,76 @@ def test_gradients_match_finite_differences(name, extras, shape):
 
 
 @pytest.mark.parametrize("name", list(KINDS))
+@pytest.mark.parametrize("extras", [dict(), dict(slope=0.05, softcap=2.0)])
+def test_key_bias_gradient_matches_finite_differences(name, extras):
+    # L = <dO, O> as a function of each key bias (the dynamic keep set is fixed
+    # at construction, so the perturbation moves the scores only)
+    rng = np.random.default_rng(17)
+    p = _problem(rng, 6, 9, 4, 3, KINDS[name], bias=True, **extras)
+    do = _rand(rng, p.sq, p.dv)
+    g = p.dkey_bias(do)
+    h = 1e-6
+    num = np.zeros(p.sk)
+    for j in range(p.sk):
+        x0 = p.key_bias[j]
+        p.key_bias[j] = x0 + h
+        lp = _loss(p, do)
+        p.key_bias[j] = x0 - h
+        lm = _loss(p, do)
+        p.key_bias[j] = x0
+        num[j] = (lp - lm) / (2 * h)
+    assert np.abs(num - g).max() / max(1.0, np.abs(num).max()) < 1e-6
+    # a subset of columns is the same numbers
+    cols = np.array([0, 4, 8])
+    assert np.array_equal(p.dkey_bias(do, cols), g[cols])
+
+
+@pytest.mark.parametrize("name", list(KINDS))
+def test_key_bias_gradient_sums_to_zero_and_matches_autograd(name):
+    # sum_j dL/dkb_j = sum_i sum_j P_ij (dP_ij - D_i) = 0 for every live row,
+    # softcap or not (the cap acts before the bias); keys no query sees get 0
+    rng = np.random.default_rng(18)
+    p = _problem(rng, 23, 31, 8, 5, KINDS[name], bias=True, slope=0.03, softcap=1.5)
+    do = _rand(rng, p.sq, p.dv)
+    g = p.dkey_bias(do)
+    assert abs(g.sum()) < 1e-12
+    unused = ~p.mask(np.arange(p.sq), np.arange(p.sk)).any(0)
+    assert np.all(g[unused] == 0.0)
+    # torch float64 autograd through an explicit softmax with the bias as a leaf
+    rows, cols = np.arange(p.sq), np.arange(p.sk)
+    m = torch.tensor(p.mask(rows, cols))
+    kb = torch.tensor(p.key_bias, requires_grad=True)
+    r = p.scale * torch.tensor(p.q) @ torch.tensor(p.k).T
+    r = p.softcap * torch.tanh(r / p.softcap)
+    s = r + p.rel_bias_slope * torch.tensor(rows[:, None] - cols[None, :], dtype=torch.float64) + kb[None, :]
+    s = torch.where(m, s, torch.tensor(-math.inf, dtype=torch.float64))
+    live = m.any(1)
+    pr = torch.where(live[:, None], torch.softmax(torch.where(live[:, None], s, torch.zeros_like(s)), 1)
+                     * m, torch.zeros_like(s))
+    out = pr @ torch.tensor(p.v)
+    out.backward(torch.tensor(do))
+    assert np.allclose(g, kb.grad.numpy(), atol=1e-11)
+
+
+def test_keep_index_lists_kept_keys_ascending():
+    rng = np.random.default_rng(19)
+    kb = np.round(rng.standard_normal((2, 2, 45)) * 2) / 2  # ties
+    for k in (0, 1, 10, 45, 60):
+        idx = A.keep_index(kb, k)
+        assert idx.shape == (2, 2, 45) and idx.dtype == np.int32
+        for b in range(2):
+            for h in range(2):
+                row = kb[b, h]
+                # brute-force rank count, independent of the lexsort in topk_keep
+                kept = [j for j in range(45)
+                        if sum(1 for i in range(45) if row[i] > row[j] or (row[i] == row[j] and i < j)) < k]
+                n = len(kept)
+                assert n == min(k, 45)
+                assert idx[b, h, :n].tolist() == kept  # ascending by construction of the list above
+                assert np.all(idx[b, h, n:] == 0)
+
+
+@pytest.mark.parametrize("name", list(KINDS))
 def test_backward_invariants(name):
     rng = np.random.default_rng(8)
     p = _problem(rng, 21, 33, 8, 6, KINDS[name], bias=True)

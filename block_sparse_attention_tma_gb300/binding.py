@@ -18,7 +18,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgbattn.so")
 
-NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK = range(6)
+NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL = range(7)
 BF16, FP32 = 0, 1
 _DT = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -54,20 +54,24 @@ _SIGS = [
     ("gbattn_block_mask_sizes", ctypes.c_int, [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_size_t)] * 6),
     ("build_block_mask", ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.POINTER(_Mask), ctypes.POINTER(_Blocks),
                                                               ctypes.c_void_p]),
-    ("attn_fwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.POINTER(_Mask),
+    ("attn_fwd", ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.POINTER(_Mask),
                                                                               ctypes.POINTER(_Blocks),
                                                                               ctypes.c_void_p, ctypes.c_void_p,
                                                                               ctypes.c_void_p]),
     ("attn_bwd_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 7),
-    ("attn_bwd", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.POINTER(_Mask),
+    ("attn_bwd", ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.POINTER(_Mask),
                                                                               ctypes.POINTER(_Blocks), ctypes.c_int]
      + [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p]),
     ("attn_fwd_splitkv_workspace_bytes", ctypes.c_size_t, [ctypes.c_int] * 5),
-    ("attn_fwd_splitkv", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3 + [ctypes.c_float,
+    ("attn_fwd_splitkv", ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p] * 3 + [ctypes.c_float,
                                                                                       ctypes.POINTER(_Mask),
                                                                                       ctypes.c_int]
      + [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
-    ("attn_fwd_splitkv_noalloc", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3
+    ("attn_fwd_splitkv_paged", ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p] * 3
+     + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+        ctypes.POINTER(_Mask), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p]),
+    ("attn_fwd_splitkv_noalloc", ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p] * 3
      + [ctypes.c_float, ctypes.POINTER(_Mask), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("gbattn_last_device_error", ctypes.c_int, [ctypes.c_void_p]),
 ]
@@ -175,9 +179,11 @@ def build_block_mask(B, H, Sq, Sk, mask: MaskSpec, lists: BlockLists, stream=Non
 
 def attn_fwd(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, lists: Optional[BlockLists] = None,
              o=None, lse=None, stream=None):
+    """q [B, H, Sq, Dqk]; k, v [B, Hkv, Sk, D] (Hkv divides H: grouped-query
+    attention when Hkv < H)."""
     lib = load_library()
     B, H, Sq, Dqk = q.shape
-    Sk, Dv = k.shape[2], v.shape[3]
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
@@ -185,7 +191,7 @@ def attn_fwd(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, lists: Optiona
     mask = mask or MaskSpec()
     cm = mask.c()
     cb = lists.c() if lists is not None else None
-    _check(lib.attn_fwd(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), float(scale),
+    _check(lib.attn_fwd(_DT.get(q.dtype, -1), B, H, Hkv, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), float(scale),
                         ctypes.byref(cm), ctypes.byref(cb) if cb is not None else None, _ptr(o), _ptr(lse),
                         _stream(stream)), "attn_fwd")
     return o, lse
@@ -202,7 +208,7 @@ def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
     given it receives the gradient of the key bias."""
     lib = load_library()
     B, H, Sq, Dqk = q.shape
-    Sk, Dv = k.shape[2], v.shape[3]
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -212,7 +218,8 @@ def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
     mask = mask or MaskSpec()
     cm = mask.c()
     cb = lists.c() if lists is not None else None
-    _check(lib.attn_bwd(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+    _check(lib.attn_bwd(_DT.get(q.dtype, -1), B, H, Hkv, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                        _ptr(dout),
                         _ptr(lse), float(scale), ctypes.byref(cm), ctypes.byref(cb) if cb is not None else None,
                         int(bool(deterministic)), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkey_bias), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)), "attn_bwd")
@@ -227,7 +234,7 @@ def attn_fwd_splitkv(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_sp
                      workspace=None, stream=None):
     lib = load_library()
     B, H, Sq, Dqk = q.shape
-    Sk, Dv = k.shape[2], v.shape[3]
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
@@ -237,10 +244,37 @@ def attn_fwd_splitkv(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_sp
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     mask = mask or MaskSpec()
     cm = mask.c()
-    _check(lib.attn_fwd_splitkv(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v), float(scale),
-                                ctypes.byref(cm), int(num_splits), _ptr(o), _ptr(lse), _ptr(workspace),
+    _check(lib.attn_fwd_splitkv(_DT.get(q.dtype, -1), B, H, Hkv, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v),
+                                float(scale), ctypes.byref(cm), int(num_splits), _ptr(o), _ptr(lse), _ptr(workspace),
                                 0 if workspace is None else workspace.numel() * workspace.element_size(),
                                 _stream(stream)), "attn_fwd_splitkv")
+    return o, lse
+
+
+def attn_fwd_splitkv_paged(q, k_cache, v_cache, page_table, seqlens_k, scale=0.0, mask: Optional[MaskSpec] = None,
+                           num_splits=1, o=None, lse=None, workspace=None, stream=None):
+    """Split-KV decode over a paged cache: k_cache / v_cache [num_pages, Hkv,
+    page_size, D] bf16, page_table [B, max_pages] int32 and seqlens_k [B]
+    int32 on the GPU."""
+    lib = load_library()
+    B, H, Sq, Dqk = q.shape
+    num_pages, Hkv, page_size, Dv = v_cache.shape
+    max_pages = page_table.shape[1]
+    if o is None:
+        o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    need = attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    mask = mask or MaskSpec()
+    cm = mask.c()
+    _check(lib.attn_fwd_splitkv_paged(_DT.get(q.dtype, -1), B, H, Hkv, Sq, Dqk, Dv, _ptr(q), _ptr(k_cache),
+                                      _ptr(v_cache), num_pages, page_size, _ptr(page_table), max_pages,
+                                      _ptr(seqlens_k), float(scale), ctypes.byref(cm), int(num_splits), _ptr(o),
+                                      _ptr(lse), _ptr(workspace),
+                                      0 if workspace is None else workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "attn_fwd_splitkv_paged")
     return o, lse
 
 
@@ -257,14 +291,14 @@ def attn_fwd_splitkv_noalloc(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None
     nothing here either."""
     lib = load_library()
     B, H, Sq, Dqk = q.shape
-    Sk, Dv = k.shape[2], v.shape[3]
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     mask = mask or MaskSpec()
     cm = mask.c()
-    _check(lib.attn_fwd_splitkv_noalloc(_DT.get(q.dtype, -1), B, H, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v),
+    _check(lib.attn_fwd_splitkv_noalloc(_DT.get(q.dtype, -1), B, H, Hkv, Sq, Sk, Dqk, Dv, _ptr(q), _ptr(k), _ptr(v),
                                         float(scale), ctypes.byref(cm), int(num_splits), _ptr(o), _ptr(lse),
                                         _stream(stream)), "attn_fwd_splitkv_noalloc")
     return o, lse

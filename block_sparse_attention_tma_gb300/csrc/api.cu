@@ -35,6 +35,9 @@ bool dims_ok(int B, int H, int Sq, int Sk) {
   return true;
 }
 
+// Grouped-query attention: H query heads share Hkv key/value heads.
+bool heads_ok(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
+
 bool bf16_dims_ok(int Dqk, int Dv) {
   return (Dqk == 32 && Dv == 32) || (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128) ||
          (Dqk == 192 && Dv == 128);
@@ -74,8 +77,9 @@ int check_mask(const gbattn_mask* mask, HostMask* hm) {
   hm->kind = GBATTN_MASK_NONE;
   hm->window_left = -1;
   if (!mask) return GBATTN_OK;
-  if (mask->kind < GBATTN_MASK_NONE || mask->kind > GBATTN_MASK_DYNAMIC_TOPK) return GBATTN_ERR_ARG;
-  if (mask->kind == GBATTN_MASK_BLOCK_DIAG && mask->block_size <= 0) return GBATTN_ERR_ARG;
+  if (mask->kind < GBATTN_MASK_NONE || mask->kind > GBATTN_MASK_MINI_CAUSAL) return GBATTN_ERR_ARG;
+  if ((mask->kind == GBATTN_MASK_BLOCK_DIAG || mask->kind == GBATTN_MASK_MINI_CAUSAL) && mask->block_size <= 0)
+    return GBATTN_ERR_ARG;
   if (mask->kind == GBATTN_MASK_PREFIX_LM && mask->prefix_len < 0) return GBATTN_ERR_ARG;
   if (mask->kind == GBATTN_MASK_DYNAMIC_TOPK && (mask->topk < 0 || !mask->key_bias)) return GBATTN_ERR_ARG;
   if (!isfinite(mask->softcap) || mask->softcap < 0.f || !isfinite(mask->rel_bias_slope)) return GBATTN_ERR_ARG;
@@ -134,6 +138,7 @@ void choose_gather(int dtype, const Shape& s, HostMask* hm) {
   hm->gather = 0;
   hm->kept = s.Sk;
   if (dtype != GBATTN_BF16 || hm->kind != GBATTN_MASK_DYNAMIC_TOPK || !hm->has_lists || !hm->keep_idx) return;
+  if (s.Hkv != s.H) return;  // compact key tiles are per query head
   if ((long long)s.B * s.H * s.Sk >= (1ll << 31)) return;
   hm->gather = 1;
   hm->kept = hm->topk < s.Sk ? hm->topk : s.Sk;
@@ -195,7 +200,7 @@ using namespace gb;
 
 extern "C" {
 
-int gbattn_version(void) { return 101; }
+int gbattn_version(void) { return 102; }
 
 const char* gbattn_strerror(int status) {
   switch (status) {
@@ -245,10 +250,10 @@ int build_block_mask(int B, int H, int Sq, int Sk, const gbattn_mask* mask, gbat
   return blockmask_launch(B, H, Sq, Sk, hm, out, static_cast<cudaStream_t>(stream));
 }
 
-int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k, const void* v,
-             float scale, const gbattn_mask* mask, const gbattn_blocks* blocks, void* o, float* lse,
+int attn_fwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k,
+             const void* v, float scale, const gbattn_mask* mask, const gbattn_blocks* blocks, void* o, float* lse,
              gbattn_stream stream) {
-  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
+  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1 || !heads_ok(H, Hkv)) return GBATTN_ERR_ARG;
   if (!q || !k || !v || !o) return GBATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
     return GBATTN_ERR_ALIGN;
@@ -266,7 +271,7 @@ int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
   if (rc) return rc;
   rc = device_check();
   if (rc) return rc;
-  const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  const Shape s{B, H, Sq, Sk, Dqk, Dv, Hkv};
   choose_gather(dtype, s, &hm);
   const float sc = resolve_scale(scale, Dqk);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -278,14 +283,14 @@ int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
 size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv) {
   if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return 0;
   if (dtype != GBATTN_BF16 && dtype != GBATTN_FP32) return 0;
-  return bwd_workspace_bytes(Shape{B, H, Sq, Sk, Dqk, Dv});
+  return bwd_workspace_bytes(Shape{B, H, Sq, Sk, Dqk, Dv, H});
 }
 
-int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k, const void* v,
-             const void* o, const void* dout, const float* lse, float scale, const gbattn_mask* mask,
+int attn_bwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k,
+             const void* v, const void* o, const void* dout, const float* lse, float scale, const gbattn_mask* mask,
              const gbattn_blocks* blocks, int deterministic, void* dq, void* dk, void* dv, float* dkey_bias,
              void* workspace, size_t workspace_bytes, gbattn_stream stream) {
-  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
+  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1 || !heads_ok(H, Hkv)) return GBATTN_ERR_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return GBATTN_ERR_ARG;
   if (deterministic != 0 && deterministic != 1) return GBATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
@@ -303,7 +308,13 @@ int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const voi
   if (rc) return rc;
   rc = check_blocks(blocks, Sq, Sk, true, true, &hm);
   if (rc) return rc;
-  const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  const Shape s{B, H, Sq, Sk, Dqk, Dv, Hkv};
+  if (Hkv != H) {
+    // the key-bias gradient is per query head; a group's dK/dV kernel walks
+    // G heads' tiles under one 15-bit tile index
+    if (dkey_bias) return GBATTN_ERR_UNSUPPORTED;
+    if (H / Hkv > kMaxGroup || (long long)(H / Hkv) * ((Sq + 127) / 128) >= 32768) return GBATTN_ERR_UNSUPPORTED;
+  }
   if (!workspace || workspace_bytes < bwd_workspace_bytes(s)) return GBATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return GBATTN_ERR_ALIGN;
   rc = device_check();
@@ -326,10 +337,10 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Dv, int num_sp
   return align_up(rows * Dv * sizeof(float), 256) + align_up(rows * sizeof(float), 256);
 }
 
-int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k,
-                     const void* v, float scale, const gbattn_mask* mask, int num_splits, void* o, float* lse,
-                     void* workspace, size_t workspace_bytes, gbattn_stream stream) {
-  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
+int attn_fwd_splitkv(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, const void* q,
+                     const void* k, const void* v, float scale, const gbattn_mask* mask, int num_splits, void* o,
+                     float* lse, void* workspace, size_t workspace_bytes, gbattn_stream stream) {
+  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1 || !heads_ok(H, Hkv)) return GBATTN_ERR_ARG;
   if (!q || !k || !v || !o) return GBATTN_ERR_ARG;
   if (num_splits < 1 || num_splits > 64) return GBATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
@@ -348,15 +359,50 @@ int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, c
   }
   rc = device_check();
   if (rc) return rc;
-  const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  const Shape s{B, H, Sq, Sk, Dqk, Dv, Hkv};
   return splitkv_launch(s, q, k, v, resolve_scale(scale, Dqk), hm.kind == GBATTN_MASK_CAUSAL, num_splits, o, lse,
-                        workspace, static_cast<cudaStream_t>(stream));
+                        workspace, static_cast<cudaStream_t>(stream), nullptr);
 }
 
-int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv, const void* q, const void* k,
-                             const void* v, float scale, const gbattn_mask* mask, int num_splits, void* o, float* lse,
-                             gbattn_stream stream) {
-  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1) return GBATTN_ERR_ARG;
+int attn_fwd_splitkv_paged(int dtype, int B, int H, int Hkv, int Sq, int Dqk, int Dv, const void* q,
+                           const void* k_cache, const void* v_cache, int num_pages, int page_size,
+                           const int32_t* page_table, int max_pages_per_seq, const int32_t* seqlens_k, float scale,
+                           const gbattn_mask* mask, int num_splits, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, gbattn_stream stream) {
+  if (B < 1 || H < 1 || Sq < 1 || Dqk < 1 || Dv < 1 || !heads_ok(H, Hkv)) return GBATTN_ERR_ARG;
+  if ((long long)B * H > (1ll << 24) || Sq > kMaxSeq) return GBATTN_ERR_ARG;
+  if (!q || !k_cache || !v_cache || !o || !page_table || !seqlens_k) return GBATTN_ERR_ARG;
+  if (num_pages < 1 || page_size < 64 || page_size % 64 || max_pages_per_seq < 1) return GBATTN_ERR_ARG;
+  if ((long long)max_pages_per_seq * page_size > kMaxSeq) return GBATTN_ERR_ARG;
+  if ((long long)num_pages * Hkv * page_size >= (1ll << 31)) return GBATTN_ERR_ARG;
+  if (num_splits < 1 || num_splits > 64) return GBATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || (lse && !aligned4(lse)) ||
+      !aligned4(page_table) || !aligned4(seqlens_k))
+    return GBATTN_ERR_ALIGN;
+  if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+  if (!(Dqk == Dv && (Dqk == 64 || Dqk == 128))) return GBATTN_ERR_UNSUPPORTED;
+  HostMask hm;
+  int rc = check_mask(mask, &hm);
+  if (rc) return rc;
+  if (hm.kind != GBATTN_MASK_NONE && hm.kind != GBATTN_MASK_CAUSAL) return GBATTN_ERR_UNSUPPORTED;
+  if (hm.softcap != 0.f || hm.slope != 0.f || hm.key_bias) return GBATTN_ERR_UNSUPPORTED;
+  if (num_splits > 1) {
+    if (!workspace || workspace_bytes < attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits))
+      return GBATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GBATTN_ERR_ALIGN;
+  }
+  rc = device_check();
+  if (rc) return rc;
+  const Shape s{B, H, Sq, max_pages_per_seq * page_size, Dqk, Dv, Hkv};
+  const PagedKV pk{seqlens_k, page_table, page_size, max_pages_per_seq, num_pages};
+  return splitkv_launch(s, q, k_cache, v_cache, resolve_scale(scale, Dqk), hm.kind == GBATTN_MASK_CAUSAL,
+                        num_splits, o, lse, workspace, static_cast<cudaStream_t>(stream), &pk);
+}
+
+int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, const void* q,
+                             const void* k, const void* v, float scale, const gbattn_mask* mask, int num_splits,
+                             void* o, float* lse, gbattn_stream stream) {
+  if (!dims_ok(B, H, Sq, Sk) || Dqk < 1 || Dv < 1 || !heads_ok(H, Hkv)) return GBATTN_ERR_ARG;
   if (!q || !k || !v || !o) return GBATTN_ERR_ARG;
   if (num_splits < 1 || num_splits > 64) return GBATTN_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
@@ -372,7 +418,7 @@ int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Sq, int Sk, int Dqk, i
   if (need > (size_t)GBATTN_NOALLOC_SCRATCH_BYTES) return GBATTN_ERR_WORKSPACE;
   rc = device_check();
   if (rc) return rc;
-  const Shape s{B, H, Sq, Sk, Dqk, Dv};
+  const Shape s{B, H, Sq, Sk, Dqk, Dv, Hkv};
   return splitkv_noalloc_launch(s, q, k, v, resolve_scale(scale, Dqk), hm.kind == GBATTN_MASK_CAUSAL, num_splits,
                                 need, o, lse, static_cast<cudaStream_t>(stream));
 }

@@ -36,6 +36,7 @@ namespace gb {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   int B, H, Sq, Sk, sq_pad;
+  int Hkv, G;          // key/value heads and query heads per key/value head (GQA)
   float scale_log2, cap_pre, cap_post, scale;
   MaskParams mask;
   int has_lists, sub_q, sub_k, nqb, nkb, sparse_m, sparse_n;
@@ -128,7 +129,8 @@ struct DkdvCfg {
          B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, B_FIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
-      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 + TCAP * 2 + NBAR * 8 + 32 + 2048;
+      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 + 4 * (kMaxGroup + 4) + TCAP * 2 +
+      NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
   static constexpr uint32_t ID_DV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
@@ -146,7 +148,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   uint8_t* sG = sQ + C::QST * C::QTILE;         // [GST]
   float* sLD = reinterpret_cast<float*>(sG + C::GST * C::VTILE);  // [QST][lse2 128 | delta 128]
   float* sDB = sLD + C::QST * 256;                                  // [128] key-bias partial sums
-  uint16_t* tlist = reinterpret_cast<uint16_t*>(sDB + 128);         // [TCAP]
+  int* soff = reinterpret_cast<int*>(sDB + 128);                    // [G + 1] slot offsets of the query heads
+  uint16_t* tlist = reinterpret_cast<uint16_t*>(soff + kMaxGroup + 4);  // [TCAP]
   uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -154,29 +157,82 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   int* gpos = reinterpret_cast<int*>(tmem_slot + 4);  // [2] first / last key of a gathered tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int k0 = (blockIdx.x / BH) * 128;
+  const int BHkv = p.B * p.Hkv;
+  const int bkv = blockIdx.x % BHkv;  // key/value head of this CTA
+  const int k0 = (blockIdx.x / BHkv) * 128;
+  // query heads bq0 .. bq0 + G - 1 share this key/value head (GQA); their
+  // tiles are walked one head after the other and accumulate into the same
+  // dK / dV. A walked tile's start is g * SqP + q0 (g = query head in the group).
+  const int bq0 = (bkv / p.Hkv) * p.H + (bkv % p.Hkv) * p.G;
+  const int nqt = (p.Sq + 127) / 128;
+  const int SqP = nqt * 128;
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
   const int Skv = p.Skv;
   const int delta = p.Sk - p.Sq;
-  const int32_t* pos_h = gat ? p.kidx + (size_t)bh * p.Sk : nullptr;
+  const int32_t* pos_h = gat ? p.kidx + (size_t)bq0 * p.Sk : nullptr;
 
   TileWalk walk;
   int nslots;
   int p_first = 0, p_last = 0;
   if (gat) {
-    nslots = (p.Sq + 127) / 128;
+    nslots = nqt;
+  } else if (p.G == 1) {
+    if (p.has_lists) {
+      walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bq0 * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
+      nslots = walk.nslots;
+    } else {
+      nslots = nqt;
+    }
   } else if (p.has_lists) {
-    walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
-    nslots = walk.nslots;
+    // per-head slot counts of the group, prefix-summed into soff by warp 0
+    if (warp == 0) {
+      int tot = 0;
+      for (int g0 = 0; g0 < p.G; g0 += 32) {
+        const int g = g0 + lane;
+        int ns = 0;
+        if (g < p.G) ns = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, (bq0 + g) * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q,
+                                    p.Sq).nslots;
+        int incl = ns;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (g < p.G) soff[g] = tot + incl - ns;
+        tot += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) soff[p.G] = tot;
+      __syncwarp();
+    }
+    nslots = 0;  // set from soff[G] (after the block-wide barrier for roles other than warp 0)
+    if (warp == 0) nslots = soff[p.G];
   } else {
-    nslots = (p.Sq + 127) / 128;
+    nslots = p.G * nqt;
   }
-  auto slot = [&](int s, int* q0, bool* masked) -> bool {
-    if (gat) return gathered_slot_cols(s, p_first, p_last, k0 + 128 <= Skv, delta, p.Sq, q0, masked);
-    return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, q0, masked)
-                       : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, q0, masked);
+  auto slot = [&](int s, int* st, bool* masked) -> bool {
+    if (gat) return gathered_slot_cols(s, p_first, p_last, k0 + 128 <= Skv, delta, p.Sq, st, masked);
+    if (p.G == 1)
+      return p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, st, masked)
+                         : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, st, masked);
+    int g, q0;
+    bool ok;
+    if (p.has_lists) {
+      int lo = 0, hi = p.G - 1;  // last g with soff[g] <= s
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (soff[mid] <= s) lo = mid;
+        else hi = mid - 1;
+      }
+      g = lo;
+      const TileWalk w =
+          make_walk(p.kmc, p.kmi, p.kfc, p.kfi, (bq0 + g) * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
+      ok = walk_slot(w, s - soff[g], p.mask, false, k0, p.Sq, p.Sk, &q0, masked);
+    } else {
+      g = s / nqt;
+      ok = dense_slot(s - g * nqt, p.mask, false, k0, p.Sq, p.Sk, &q0, masked);
+    }
+    *st = g * SqP + q0;
+    return ok;
   };
   if (warp == 0) {
     if (gat) {
@@ -207,6 +263,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
     p_first = gpos[0];
     p_last = gpos[1];
   }
+  if (!gat && p.G > 1 && p.has_lists && warp != 0) nslots = soff[p.G];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -215,29 +272,31 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         int n = 0, nq = 0, ng = 0;
         bool ok = true;
         auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
-        int q0;
+        int st;
         bool masked;
-        while (ok && it.next(&q0, &masked)) {
+        while (ok && it.next(&st, &masked)) {
+          const int g = st / SqP, q0 = st - g * SqP;
+          const int bq = bq0 + g;  // query head of this tile
           if (n == 0) {
             mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
             for (int j = 0; j < C::NQSLAB; ++j)
-              tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bh);
+              tma_load_3d(sK + j * C::QSLAB, &p.tm_k, bar + C::B_KV, j * (C::SWQ / 2), k0, bkv);
             for (int j = 0; j < C::NVSLAB; ++j)
-              tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bh);
+              tma_load_3d(sV + j * C::VSLAB, &p.tm_v, bar + C::B_KV, j * (C::SWV / 2), k0, bkv);
           }
           const int qs = n % C::QST;
           if (n >= C::QST && !(ok = mbar_wait(bar + C::B_QE + qs, ((n / C::QST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
           for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
-          bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
-          bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+            tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bq);
+          bulk_load(sLD + qs * 256, p.lse2 + (size_t)bq * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+          bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bq * p.sq_pad + q0, 512, bar + C::B_QF + qs);
           ++nq;
           const int gs = n % C::GST;
           if (n >= C::GST && !(ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
           for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bh);
+            tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bq);
           ++ng;
           ++n;
         }
@@ -262,7 +321,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
           if (lane == 0) mbar_expect_tx(bar + C::B_KV, C::QTILE + C::VTILE);
           int gr[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(k0 + 4 * lane + e, Skv - 1));
+          for (int e = 0; e < 4; ++e) gr[e] = bkv * p.Sk + __ldg(pos_h + min(k0 + 4 * lane + e, Skv - 1));
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < C::NQSLAB; ++j)
@@ -279,9 +338,9 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
           if (ok) {
             mbar_expect_tx(bar + C::B_QF + qs, C::QTILE + 1024);
             for (int j = 0; j < C::NQSLAB; ++j)
-              tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bh);
-            bulk_load(sLD + qs * 256, p.lse2 + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
-            bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bh * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+              tma_load_3d(sQ + qs * C::QTILE + j * C::QSLAB, &p.tm_q, bar + C::B_QF + qs, j * (C::SWQ / 2), q0, bq0);
+            bulk_load(sLD + qs * 256, p.lse2 + (size_t)bq0 * p.sq_pad + q0, 512, bar + C::B_QF + qs);
+            bulk_load(sLD + qs * 256 + 128, p.delta + (size_t)bq0 * p.sq_pad + q0, 512, bar + C::B_QF + qs);
             ++nq;
             const int gs = n % C::GST;
             if (n >= C::GST) ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag);
@@ -289,7 +348,7 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
               mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
               for (int j = 0; j < C::NVSLAB; ++j)
                 tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0,
-                            bh);
+                            bq0);
               ++ng;
             }
           }
@@ -403,27 +462,40 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     int ilo, ihi;
     float kt;  // per-key score term, log2 units
-    bool kept = j < Skv;
-    {
+    bool kept;
+    // the keep bit and the key-bias term belong to the query head (bq)
+    auto head_terms = [&](int bq) {
       const int jo = orig();
-      if (gat) {
-        ilo = max(0, jo - delta);
-        ihi = p.Sq - 1;
-      } else {
-        col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
-      }
+      kept = j < Skv;
       if (kept && p.mask.keep && !gat)
-        kept = (__ldg(p.mask.keep + (size_t)bh * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
-      const float kb = (j < Skv && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bh * p.Sk + jo) : 0.f;
+        kept = (__ldg(p.mask.keep + (size_t)bq * p.mask.nkw + (j >> 5)) >> (j & 31)) & 1u;
+      const float kb = (j < Skv && p.mask.key_bias) ? __ldg(p.mask.key_bias + (size_t)bq * p.Sk + jo) : 0.f;
       kt = (kb - p.mask.slope * (float)jo) * kLog2e;
+    };
+    if (gat) {
+      ilo = max(0, orig() - delta);
+      ihi = p.Sq - 1;
+    } else {
+      col_interval(p.mask, j, p.Sq, p.Sk, ilo, ihi);
     }
+    head_terms(bq0);
+    int g_cur = 0;
     float dbs = 0.f;  // key-bias gradient: this half's sum of dS^T (before the softcap factor)
     int n = 0;
     bool ok = true;
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
-    int q0;
+    int st;
     bool masked;
-    while (ok && it.next(&q0, &masked)) {
+    while (ok && it.next(&st, &masked)) {
+      int q0 = st;
+      if (p.G > 1) {
+        const int g = st / SqP;
+        q0 = st - g * SqP;
+        if (g != g_cur) {
+          g_cur = g;
+          head_terms(bq0 + g);
+        }
+      }
       const int qs = n % C::QST;
       ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
       if (ok) ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag);  // lse2 / delta landed
@@ -558,12 +630,12 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
           sDB[row] = dbs;
           mbar_arrive(bar + C::B_FIN);
         } else if (ok && mbar_wait(bar + C::B_FIN, 0, abort_flag) && jin) {
-          p.dbias[(size_t)bh * p.Sk + jo] = dbs + sDB[row];
+          p.dbias[(size_t)bq0 * p.Sk + jo] = dbs + sDB[row];
         }
       }
       if (ok) {
-        __nv_bfloat16* dvrow = p.dv + ((size_t)bh * p.Sk + jo) * DV;
-        __nv_bfloat16* dkrow = p.dk + ((size_t)bh * p.Sk + jo) * DQK;
+        __nv_bfloat16* dvrow = p.dv + ((size_t)bkv * p.Sk + jo) * DV;
+        __nv_bfloat16* dkrow = p.dk + ((size_t)bkv * p.Sk + jo) * DQK;
 #pragma unroll 1
         for (int c0 = grp * 32; c0 < DV + DQK; c0 += 64) {
           const bool isv = c0 < DV;
@@ -645,6 +717,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   const int BH = p.B * p.H;
   const int nqt = (p.Sq + 127) / 128;
   const int bh = blockIdx.x % BH;
+  const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
   const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * 128;
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
   const int Skv = p.Skv;
@@ -715,13 +788,13 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
           if (n >= C::KST && !(ok = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bh);
+            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bkv);
           ++nk;
           const int vs = n % C::VST;
           if (n >= C::VST && !(ok = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
           for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, bar + C::B_VF + vs, j * (C::SWV / 2), kv0, bh);
+            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, bar + C::B_VF + vs, j * (C::SWV / 2), kv0, bkv);
           ++nv;
           ++n;
         }
@@ -751,7 +824,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         }
         int gr[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
+        for (int e = 0; e < 4; ++e) gr[e] = bkv * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
         const int ks = n % C::KST;
         bool w = true;
         if (lane == 0 && n >= C::KST) w = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag);
@@ -1030,12 +1103,12 @@ static int set_smem_once(K kern, int bytes, bool* flag) {
 
 template <int DQK, int DV, bool CAP, bool GAT, bool DB>
 static int launch_bwd_main(const BwdParams& prm, const Shape& s, cudaStream_t st) {
-  const int BH = s.B * s.H;
+  const int BH = s.B * s.H, BHkv = s.B * s.Hkv;
   static bool f1 = false, f2 = false;
   if (set_smem_once(dkdv_kernel<DQK, DV, CAP, GAT, DB>, DkdvCfg<DQK, DV>::SMEM, &f1)) return GBATTN_ERR_CUDA;
   const int nkt = (prm.Skv + 127) / 128;  // key tiles (compact tiles when gathered)
   if (nkt > 0) {
-    dkdv_kernel<DQK, DV, CAP, GAT, DB><<<nkt * BH, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
+    dkdv_kernel<DQK, DV, CAP, GAT, DB><<<nkt * BHkv, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
   }
   if (set_smem_once(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV>::SMEM, &f2)) return GBATTN_ERR_CUDA;
@@ -1064,13 +1137,16 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
+  const int BHkv = s.B * s.Hkv;
   if (m.gather) {
-    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BH * s.Sk, swq)) return GBATTN_ERR_CUDA;
-    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BH * s.Sk, swv)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BHkv * s.Sk, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BHkv * s.Sk, swv)) return GBATTN_ERR_CUDA;
   } else {
-    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
-    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, swv)) return GBATTN_ERR_CUDA;
   }
+  prm.Hkv = s.Hkv;
+  prm.G = s.H / s.Hkv;
   if (!make_tmap_bf16_3d(&prm.tm_do, dout, s.Dv, s.Sq, BH, swv)) return GBATTN_ERR_CUDA;
   prm.gather = m.gather;
   prm.Skv = m.gather ? m.kept : s.Sk;

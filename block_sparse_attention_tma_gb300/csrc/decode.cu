@@ -9,6 +9,13 @@
 // output over its keys (online softmax); the warps are merged at the end and
 // the split partials are merged by a combine kernel using the rule of the
 // POPCORNBENCH "Kimi-K2.6 l1_p97" trace: m = max_s m_s, weights exp(m_s - m).
+//
+// The key/value rows come from a dense cache [B, Hkv, Sk, D] or from a paged
+// cache (pages of page_size keys of one key/value head, [num_pages, Hkv,
+// page_size, D], mapped per sequence by a page table), optionally with a
+// per-sequence key count. Query heads share key/value heads in groups of
+// G = H / Hkv (GQA); the G CTAs of a group stream the same rows close in time,
+// so the repeats are served by L2.
 #include <mutex>
 
 #include "kernels.h"
@@ -27,9 +34,25 @@ struct DecParams {
   float* lse;
   float* o_part;     // [n][BH][Sq][D]
   float* lse_part;   // [n][BH][Sq]
-  int BH, Sq, Sk, nsplit, per, causal;
+  int BH, Sq, Sk, nsplit, causal;
+  int H, Hkv, G;     // query heads, key/value heads, H / Hkv
+  const int32_t* seqlens;     // [B] keys per sequence, or nullptr (all Sk)
+  const int32_t* page_table;  // [B][max_pages], or nullptr (dense cache)
+  int page_size, max_pages, num_pages;
   float scale_log2;
 };
+
+// Address of the key/value row `key` of sequence b, key/value head hkv.
+template <int D>
+__device__ __forceinline__ size_t kv_row(const DecParams& p, int b, int hkv, int key) {
+  if (!p.page_table) return ((size_t)(b * p.Hkv + hkv) * p.Sk + key) * D;
+  int page = __ldg(p.page_table + (size_t)b * p.max_pages + key / p.page_size);
+  if (page < 0 || page >= p.num_pages) {
+    raise_dev_error(GBATTN_ERR_BLOCKS);  // read page 0 instead; the output is invalid
+    page = 0;
+  }
+  return ((size_t)(page * p.Hkv + hkv) * p.page_size + key % p.page_size) * D;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams p) {
@@ -48,9 +71,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
   const int split = blockIdx.x % p.nsplit;
   const int rowid = blockIdx.x / p.nsplit;  // bh * Sq + i
   const int bh = rowid / p.Sq, i = rowid % p.Sq;
-  int kb = split * p.per;
-  int ke = min(kb + p.per, p.Sk);
-  if (p.causal) ke = min(ke, i + (p.Sk - p.Sq) + 1);
+  const int b = bh / p.H, hkv = (bh % p.H) / p.G;
+  int skb = p.Sk;  // keys of this sequence
+  if (p.seqlens) {
+    skb = __ldg(p.seqlens + b);
+    const int cap = p.page_table ? p.max_pages * p.page_size : p.Sk;
+    if (skb < 0 || skb > cap) {
+      if (threadIdx.x == 0) raise_dev_error(GBATTN_ERR_BLOCKS);
+      skb = max(0, min(skb, cap));
+    }
+  }
+  // split s covers keys [s L, (s + 1) L), L = ceil(keys / n) rounded up to 128
+  const int per = ((skb + p.nsplit - 1) / p.nsplit + 127) / 128 * 128;
+  int kb = split * per;
+  int ke = min(kb + per, skb);
+  if (p.causal) ke = min(ke, i + (skb - p.Sq) + 1);
   const int nkeys = max(0, ke - kb);
   const int nchunks = (nkeys + kDecChunk - 1) / kDecChunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -65,8 +100,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
   }
   __syncthreads();
 
-  const __nv_bfloat16* Kg = p.k + ((size_t)bh * p.Sk + kb) * D;
-  const __nv_bfloat16* Vg = p.v + ((size_t)bh * p.Sk + kb) * D;
 
   if (warp == kDecWarps) {
     // ------------------------------------------------------------ producer
@@ -77,9 +110,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
         if (c >= kDecStages && !mbar_wait(empty + s, ((c / kDecStages) + 1) & 1, abort_flag)) break;
         const int rows = min(kDecChunk, nkeys - c * kDecChunk);
         const uint32_t bytes = (uint32_t)rows * ROWB;
+        // a chunk never crosses a page: kb is a multiple of 128 and pages hold a
+        // multiple of 64 keys
+        const size_t off = kv_row<D>(p, b, hkv, kb + c * kDecChunk);
         mbar_expect_tx(full + s, 2 * bytes);
-        bulk_load(sK + s * CHB, Kg + (size_t)c * kDecChunk * D, bytes, full + s);
-        bulk_load(sV + s * CHB, Vg + (size_t)c * kDecChunk * D, bytes, full + s);
+        bulk_load(sK + s * CHB, p.k + off, bytes, full + s);
+        bulk_load(sV + s * CHB, p.v + off, bytes, full + s);
         ++issued;
       }
       if (*abort_flag)
@@ -271,9 +307,19 @@ static int launch_dec(const DecParams& prm, cudaStream_t st) {
 }
 
 int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
-                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st) {
+                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st, const PagedKV* paged) {
   DecParams prm;
   memset(&prm, 0, sizeof(prm));
+  prm.H = s.H;
+  prm.Hkv = s.Hkv;
+  prm.G = s.H / s.Hkv;
+  if (paged) {
+    prm.seqlens = paged->seqlens;
+    prm.page_table = paged->page_table;
+    prm.page_size = paged->page_size;
+    prm.max_pages = paged->max_pages;
+    prm.num_pages = paged->num_pages;
+  }
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k = static_cast<const __nv_bfloat16*>(k);
   prm.v = static_cast<const __nv_bfloat16*>(v);
@@ -283,9 +329,6 @@ int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, 
   prm.Sq = s.Sq;
   prm.Sk = s.Sk;
   prm.nsplit = num_splits;
-  int per = (s.Sk + num_splits - 1) / num_splits;
-  per = (per + 127) / 128 * 128;
-  prm.per = per;
   prm.causal = causal;
   prm.scale_log2 = scale * kLog2e;
   if (num_splits > 1) {
@@ -334,7 +377,7 @@ int splitkv_noalloc_launch(const Shape& s, const void* q, const void* k, const v
     scratch = noalloc_scratch_address();
     if (!scratch) return GBATTN_ERR_CUDA;
   }
-  return splitkv_launch(s, q, k, v, scale, causal, num_splits, o, lse, scratch, st);
+  return splitkv_launch(s, q, k, v, scale, causal, num_splits, o, lse, scratch, st, nullptr);
 }
 
 GB_DEFINE_ERROR_READER(decode_take_error)

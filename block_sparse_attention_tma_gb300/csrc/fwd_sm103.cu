@@ -40,6 +40,7 @@ namespace gb {
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;
   int B, H, Sq, Sk;
+  int Hkv, G;          // key/value heads and query heads per key/value head (GQA)
   int nqt;             // query tiles per head
   float scale_log2;    // scale * log2(e)
   float cap_pre;       // scale / softcap (softcap on)
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   const int L = blockIdx.x;
   const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
   const int bh = L % BH;
+  const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
   const int q0 = qt * 128;
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
   const int Skv = p.Skv;
@@ -212,13 +214,13 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
           if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(k_full + ks, C::QTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bh);
+            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bkv);
           ++nk;
           const int vs = n % C::VST;
           if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(v_full + vs, C::VTILE);
           for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bh);
+            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bkv);
           ++nv;
           ++n;
         }
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       while (ok && it.next(&kv0, &masked)) {
         int gr[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) gr[e] = bh * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
+        for (int e = 0; e < 4; ++e) gr[e] = bkv * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
         const int ks = n % C::KST;
         bool w = true;
         if (lane == 0 && n >= C::KST) w = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag);
@@ -589,13 +591,16 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
+  const int BHkv = s.B * s.Hkv;
   if (m.gather) {
-    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BH * s.Sk, swq)) return GBATTN_ERR_CUDA;
-    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BH * s.Sk, swv)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BHkv * s.Sk, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BHkv * s.Sk, swv)) return GBATTN_ERR_CUDA;
   } else {
-    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BH, swq)) return GBATTN_ERR_CUDA;
-    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BH, swv)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, swq)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, swv)) return GBATTN_ERR_CUDA;
   }
+  prm.Hkv = s.Hkv;
+  prm.G = s.H / s.Hkv;
   prm.gather = m.gather;
   prm.Skv = m.gather ? m.kept : s.Sk;
   prm.kidx = m.gather ? m.keep_idx : nullptr;

@@ -11,8 +11,13 @@
 
 namespace gb {
 
+// Largest number of query heads per key/value head (GQA group) the
+// tensor-core backward accepts.
+constexpr int kMaxGroup = 128;
+
 struct Shape {
   int B, H, Sq, Sk, Dqk, Dv;
+  int Hkv;  // key/value heads (H % Hkv == 0; Hkv == H without GQA)
 };
 
 // Validated, device-ready view of the mask and lists of one call.
@@ -49,8 +54,16 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
                     const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
                     float* dv, float* dkey_bias, void* ws, cudaStream_t st);
+// Paged key/value cache of the decode path: pages of page_size keys of one
+// key/value head ([num_pages, Hkv, page_size, D]); seqlens may be given
+// without a page table (a dense cache with per-sequence key counts).
+struct PagedKV {
+  const int32_t* seqlens;     // [B] or nullptr
+  const int32_t* page_table;  // [B][max_pages] or nullptr
+  int page_size, max_pages, num_pages;
+};
 int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
-                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st);
+                   int num_splits, void* o, float* lse, void* ws, cudaStream_t st, const PagedKV* paged);
 // Split-KV forward with its split partials in the library's static scratch
 // array (no allocation); workspace_bytes is what attn_fwd_splitkv would need.
 int splitkv_noalloc_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,

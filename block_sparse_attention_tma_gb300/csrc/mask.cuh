@@ -3,7 +3,9 @@
 // lists shared by every attention kernel.
 //
 // Mask kinds follow "Enable 2CTA for SM100 block-sparse backward" (fuzz
-// tester mask names: causal, sliding_window, block_diagonal, prefix_lm) and
+// tester mask names: causal, sliding_window, block_diagonal, mini_causal,
+// prefix_lm; mini_causal, which the page does not define, is read as causal
+// inside each block of block_size keys) and
 // the dynamic (bias-ranked) mask of "Optimize Flash Dynamic Mask Attention
 // Kernel Configurations". With the diagonal aligned bottom-right
 // (a = i + Sk - Sq), every closed-form kind allows, for query i, one interval
@@ -122,6 +124,12 @@ __device__ __forceinline__ void row_interval(const MaskParams& m, int i, int Sq,
       hi = min(Sk - 1, blk + m.block_size - 1);
       break;
     }
+    case GBATTN_MASK_MINI_CAUSAL: {
+      const int blk = floor_div(a, m.block_size) * m.block_size;
+      lo = max(0, blk);
+      hi = min(Sk - 1, a);
+      break;
+    }
     case GBATTN_MASK_PREFIX_LM:
       hi = min(max(m.prefix_len - 1, a), Sk - 1);
       break;
@@ -149,6 +157,12 @@ __device__ __forceinline__ void col_interval(const MaskParams& m, int j, int Sq,
     case GBATTN_MASK_BLOCK_DIAG: {
       const int blk = floor_div(j, m.block_size) * m.block_size;
       lo = max(0, blk - d);
+      hi = min(Sq - 1, blk + m.block_size - 1 - d);
+      break;
+    }
+    case GBATTN_MASK_MINI_CAUSAL: {  // rows with j <= i + d inside key j's block
+      const int blk = floor_div(j, m.block_size) * m.block_size;
+      lo = max(0, j - d);
       hi = min(Sq - 1, blk + m.block_size - 1 - d);
       break;
     }

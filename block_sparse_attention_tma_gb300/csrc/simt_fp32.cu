@@ -17,6 +17,7 @@ constexpr int kChunk = 32;
 
 struct SimtParams {
   int B, H, Sq, Sk, Dqk, Dv;
+  int Hkv, G;  // key/value heads, query heads per key/value head (GQA)
   float scale;
   float softcap;
   MaskParams mask;
@@ -64,8 +65,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_fwd_kernel(const SimtParams
   const int q0 = (blockIdx.x / (p.B * p.H)) * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* Q = p.q + (size_t)bh * p.Sq * DQ;
-  const float* K = p.k + (size_t)bh * p.Sk * DQ;
-  const float* V = p.v + (size_t)bh * p.Sk * DV;
+  const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head
+  const float* K = p.k + (size_t)bkv * p.Sk * DQ;
+  const float* V = p.v + (size_t)bkv * p.Sk * DV;
   const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
   const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
 
@@ -183,8 +185,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dq_kernel(const SimtParams 
   const int bh = blockIdx.x % (p.B * p.H);
   const int q0 = (blockIdx.x / (p.B * p.H)) * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float* K = p.k + (size_t)bh * p.Sk * DQ;
-  const float* V = p.v + (size_t)bh * p.Sk * DV;
+  const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head
+  const float* K = p.k + (size_t)bkv * p.Sk * DQ;
+  const float* V = p.v + (size_t)bkv * p.Sk * DV;
   const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
   const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
   for (int e = threadIdx.x; e < 128 * DQ; e += blockDim.x) {
@@ -266,7 +269,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dq_kernel(const SimtParams 
   }
 }
 
-// dK, dV: CTA = (b, h, 128-key tile), walking the backward lists over query
+// dK, dV: CTA = (b, key/value head, 128-key tile), walking, for each query
+// head of the group (GQA; one head without it), its backward list over query
 // tiles; warp w owns keys 16 w .. 16 w + 15; lanes map to 32 query rows.
 __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParams p) {
   extern __shared__ float sm[];
@@ -275,20 +279,18 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
   float* sV = sK + 128 * DQ;               // [128][DV]
   float* sQ = sV + 128 * DV;               // [32][DQ + 1]
   float* sG = sQ + kChunk * (DQ + 1);      // [32][DV + 1]
-  const int bh = blockIdx.x % (p.B * p.H);
-  const int k0 = (blockIdx.x / (p.B * p.H)) * 128;
+  const int BHkv = p.B * p.Hkv;
+  const int bkv = blockIdx.x % BHkv;
+  const int k0 = (blockIdx.x / BHkv) * 128;
+  const int bq0 = (bkv / p.Hkv) * p.H + (bkv % p.Hkv) * p.G;  // first query head of the group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float* Q = p.q + (size_t)bh * p.Sq * DQ;
-  const float* G = p.dout + (size_t)bh * p.Sq * DV;
-  const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
-  const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
   for (int e = threadIdx.x; e < 128 * DQ; e += blockDim.x) {
     const int r = e / DQ, d = e % DQ;
-    sK[e] = (k0 + r < p.Sk) ? p.k[((size_t)bh * p.Sk + k0 + r) * DQ + d] : 0.f;
+    sK[e] = (k0 + r < p.Sk) ? p.k[((size_t)bkv * p.Sk + k0 + r) * DQ + d] : 0.f;
   }
   for (int e = threadIdx.x; e < 128 * DV; e += blockDim.x) {
     const int r = e / DV, d = e % DV;
-    sV[e] = (k0 + r < p.Sk) ? p.v[((size_t)bh * p.Sk + k0 + r) * DV + d] : 0.f;
+    sV[e] = (k0 + r < p.Sk) ? p.v[((size_t)bkv * p.Sk + k0 + r) * DV + d] : 0.f;
   }
   float ak[16][4], av[16][4];
   float dbk[16];  // key-bias gradient: this lane's rows' sum of dS (before the softcap factor)
@@ -301,57 +303,68 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
     for (int t = 0; t < 4; ++t) ak[kk][t] = av[kk][t] = 0.f;
     const int j = k0 + warp * 16 + kk;
     col_interval(p.mask, j, p.Sq, p.Sk, lo[kk], hi[kk]);
-    kept[kk] = (j < p.Sk) && (!keep || ((__ldg(keep + (j >> 5)) >> (j & 31)) & 1u));
   }
-  TileWalk walk;
-  int nslots;
-  if (p.has_lists) {
-    walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
-    nslots = walk.nslots;
-  } else {
-    nslots = (p.Sq + 127) / 128;
-  }
-  for (int s = 0; s < nslots; ++s) {
-    int qs;
-    bool masked;
-    const bool ok = p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, &qs, &masked)
-                                : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, &qs, &masked);
-    if (!ok) continue;
-    for (int r0 = qs; r0 < qs + 128 && r0 < p.Sq; r0 += kChunk) {
-      __syncthreads();
-      for (int e = threadIdx.x; e < kChunk * DQ; e += blockDim.x) {
-        const int r = e / DQ, d = e % DQ;
-        sQ[r * (DQ + 1) + d] = (r0 + r < p.Sq) ? Q[(size_t)(r0 + r) * DQ + d] : 0.f;
-      }
-      for (int e = threadIdx.x; e < kChunk * DV; e += blockDim.x) {
-        const int r = e / DV, d = e % DV;
-        sG[r * (DV + 1) + d] = (r0 + r < p.Sq) ? G[(size_t)(r0 + r) * DV + d] : 0.f;
-      }
-      __syncthreads();
-      const int i = r0 + lane;
-      const float lse = (i < p.Sq) ? p.lse[(size_t)bh * p.Sq + i] : -INFINITY;
-      const float dl = (i < p.Sq) ? p.delta[(size_t)bh * p.Sq + i] : 0.f;
-#pragma unroll 1
-      for (int kk = 0; kk < 16; ++kk) {
-        const int kr = warp * 16 + kk, j = k0 + kr;
-        float dot = 0.f, dp = 0.f;
-        for (int d = 0; d < DQ; ++d) dot = fmaf(sQ[lane * (DQ + 1) + d], sK[kr * DQ + d], dot);
-        for (int d = 0; d < DV; ++d) dp = fmaf(sG[lane * (DV + 1) + d], sV[kr * DV + d], dp);
-        float dcap;
-        const float sc = simt_score(p, dot, i, j, kb, &dcap);
-        const bool al = kept[kk] && i >= lo[kk] && i <= hi[kk] && i < p.Sq && lse != -INFINITY;
-        const float pj = al ? expf(sc - lse) : 0.f;
-        const float ds0 = pj * (dp - dl);
-        dbk[kk] += ds0;
-        const float ds = ds0 * dcap;
-        for (int ii = 0; ii < kChunk; ++ii) {
-          const float pb = __shfl_sync(0xffffffffu, pj, ii);
-          const float db = __shfl_sync(0xffffffffu, ds, ii);
+  for (int g = 0; g < p.G; ++g) {
+    const int bh = bq0 + g;  // query head
+    const float* Q = p.q + (size_t)bh * p.Sq * DQ;
+    const float* G = p.dout + (size_t)bh * p.Sq * DV;
+    const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
+    const uint32_t* keep = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int d = lane + 32 * t;
-            if (d < DV) av[kk][t] = fmaf(pb, sG[ii * (DV + 1) + d], av[kk][t]);
-            if (d < DQ) ak[kk][t] = fmaf(db, sQ[ii * (DQ + 1) + d], ak[kk][t]);
+    for (int kk = 0; kk < 16; ++kk) {
+      const int j = k0 + warp * 16 + kk;
+      kept[kk] = (j < p.Sk) && (!keep || ((__ldg(keep + (j >> 5)) >> (j & 31)) & 1u));
+    }
+    TileWalk walk;
+    int nslots;
+    if (p.has_lists) {
+      walk = make_walk(p.kmc, p.kmi, p.kfc, p.kfi, bh * p.nkb + k0 / p.sparse_n, p.nqb, p.sub_q, p.Sq);
+      nslots = walk.nslots;
+    } else {
+      nslots = (p.Sq + 127) / 128;
+    }
+    for (int s = 0; s < nslots; ++s) {
+      int qs;
+      bool masked;
+      const bool ok = p.has_lists ? walk_slot(walk, s, p.mask, false, k0, p.Sq, p.Sk, &qs, &masked)
+                                  : dense_slot(s, p.mask, false, k0, p.Sq, p.Sk, &qs, &masked);
+      if (!ok) continue;
+      for (int r0 = qs; r0 < qs + 128 && r0 < p.Sq; r0 += kChunk) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kChunk * DQ; e += blockDim.x) {
+          const int r = e / DQ, d = e % DQ;
+          sQ[r * (DQ + 1) + d] = (r0 + r < p.Sq) ? Q[(size_t)(r0 + r) * DQ + d] : 0.f;
+        }
+        for (int e = threadIdx.x; e < kChunk * DV; e += blockDim.x) {
+          const int r = e / DV, d = e % DV;
+          sG[r * (DV + 1) + d] = (r0 + r < p.Sq) ? G[(size_t)(r0 + r) * DV + d] : 0.f;
+        }
+        __syncthreads();
+        const int i = r0 + lane;
+        const float lse = (i < p.Sq) ? p.lse[(size_t)bh * p.Sq + i] : -INFINITY;
+        const float dl = (i < p.Sq) ? p.delta[(size_t)bh * p.Sq + i] : 0.f;
+#pragma unroll 1
+        for (int kk = 0; kk < 16; ++kk) {
+          const int kr = warp * 16 + kk, j = k0 + kr;
+          float dot = 0.f, dp = 0.f;
+          for (int d = 0; d < DQ; ++d) dot = fmaf(sQ[lane * (DQ + 1) + d], sK[kr * DQ + d], dot);
+          for (int d = 0; d < DV; ++d) dp = fmaf(sG[lane * (DV + 1) + d], sV[kr * DV + d], dp);
+          float dcap;
+          const float sc = simt_score(p, dot, i, j, kb, &dcap);
+          const bool al = kept[kk] && i >= lo[kk] && i <= hi[kk] && i < p.Sq && lse != -INFINITY;
+          const float pj = al ? expf(sc - lse) : 0.f;
+          const float ds0 = pj * (dp - dl);
+          dbk[kk] += ds0;
+          const float ds = ds0 * dcap;
+          for (int ii = 0; ii < kChunk; ++ii) {
+            const float pb = __shfl_sync(0xffffffffu, pj, ii);
+            const float db = __shfl_sync(0xffffffffu, ds, ii);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int d = lane + 32 * t;
+              if (d < DV) av[kk][t] = fmaf(pb, sG[ii * (DV + 1) + d], av[kk][t]);
+              if (d < DQ) ak[kk][t] = fmaf(db, sQ[ii * (DQ + 1) + d], ak[kk][t]);
+            }
           }
         }
       }
@@ -364,12 +377,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
     if (j >= p.Sk) continue;
-    if (p.dbias && lane == 0) p.dbias[(size_t)bh * p.Sk + j] = db;
+    // key-bias gradient: one query head per key/value head (the host rejects it with GQA)
+    if (p.dbias && lane == 0) p.dbias[(size_t)bq0 * p.Sk + j] = db;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int d = lane + 32 * t;
-      if (d < DV) p.dv[((size_t)bh * p.Sk + j) * DV + d] = av[kk][t];
-      if (d < DQ) p.dk[((size_t)bh * p.Sk + j) * DQ + d] = ak[kk][t] * p.scale;
+      if (d < DV) p.dv[((size_t)bkv * p.Sk + j) * DV + d] = av[kk][t];
+      if (d < DQ) p.dk[((size_t)bkv * p.Sk + j) * DQ + d] = ak[kk][t] * p.scale;
     }
   }
 }
@@ -382,6 +396,8 @@ static void fill_simt(SimtParams& prm, const Shape& s, float scale, const HostMa
   prm.Sk = s.Sk;
   prm.Dqk = s.Dqk;
   prm.Dv = s.Dv;
+  prm.Hkv = s.Hkv;
+  prm.G = s.H / s.Hkv;
   prm.scale = scale;
   prm.softcap = m.softcap;
   prm.mask.kind = m.kind;
@@ -459,7 +475,7 @@ int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float*
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
   const size_t smk = sizeof(float) * (128 * s.Dqk + 128 * s.Dv + kChunk * (s.Dqk + 1) + kChunk * (s.Dv + 1));
   if (set_smem((const void*)simt_dkdv_kernel, smk)) return GBATTN_ERR_CUDA;
-  simt_dkdv_kernel<<<(unsigned)(((s.Sk + 127) / 128) * BH), kSimtThreads, smk, st>>>(prm);
+  simt_dkdv_kernel<<<(unsigned)(((s.Sk + 127) / 128) * s.B * s.Hkv), kSimtThreads, smk, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

@@ -15,13 +15,15 @@ import torch
 DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 
-def make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype="bf16", seed=42, dout=True, bias=False):
+def make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype="bf16", seed=42, dout=True, bias=False, Hkv=None):
+    """Hkv (default H): key/value heads, for grouped-query inputs."""
     g = torch.Generator().manual_seed(int(seed))
     td = DTYPES[dtype]
+    Hkv = H if Hkv is None else Hkv
     out = {
         "q": torch.randn(B, H, Sq, Dqk, generator=g).to(td),
-        "k": torch.randn(B, H, Sk, Dqk, generator=g).to(td),
-        "v": torch.randn(B, H, Sk, Dv, generator=g).to(td),
+        "k": torch.randn(B, Hkv, Sk, Dqk, generator=g).to(td),
+        "v": torch.randn(B, Hkv, Sk, Dv, generator=g).to(td),
     }
     if dout:
         out["do"] = torch.randn(B, H, Sq, Dv, generator=g).to(td)
@@ -31,13 +33,14 @@ def make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype="bf16", seed=42, dout=True, bias=Fa
 
 
 def make_device_inputs(B, H, Sq, Sk, Dqk, Dv, dtype="bf16", seed=42, device="cuda",
-                       dout=True):
+                       dout=True, Hkv=None):
     """Same recipe drawn by a CUDA generator, for inputs too large to build on
     the host (the 65536-key decode workload holds 34 GB of K/V)."""
     g = torch.Generator(device=device).manual_seed(int(seed))
     td = DTYPES[dtype]
+    Hkv = H if Hkv is None else Hkv
     out = {}
-    for name, shape in (("q", (B, H, Sq, Dqk)), ("k", (B, H, Sk, Dqk)), ("v", (B, H, Sk, Dv))):
+    for name, shape in (("q", (B, H, Sq, Dqk)), ("k", (B, Hkv, Sk, Dqk)), ("v", (B, Hkv, Sk, Dv))):
         t = torch.empty(shape, dtype=td, device=device)
         # draw in fp32 slices so the peak extra memory stays small
         flat = t.view(-1, shape[-1])

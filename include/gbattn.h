@@ -14,8 +14,13 @@
  *          attention and the online-softmax merge of partial results.
  *
  * Conventions shared by every entry point
- *   - Layout: Q [B,H,Sq,Dqk], K [B,H,Sk,Dqk], V [B,H,Sk,Dv], O/dO [B,H,Sq,Dv],
- *     each contiguous with the head dim innermost; LSE [B,H,Sq] fp32.
+ *   - Layout: Q [B,H,Sq,Dqk], K [B,Hkv,Sk,Dqk], V [B,Hkv,Sk,Dv], O/dO
+ *     [B,H,Sq,Dv], each contiguous with the head dim innermost; LSE [B,H,Sq]
+ *     fp32. Grouped-query attention ([FA2C]'s reference runs flex_attention
+ *     with enable_gqa and the kernel call carries pack_gqa): query head h
+ *     reads key/value head h / (H / Hkv); H % Hkv == 0; Hkv == H is plain
+ *     multi-head attention. Masks, key biases and block lists are per query
+ *     head.
  *   - Every pointer is a DEVICE pointer of the current CUDA device, owned by
  *     the caller. The library allocates nothing, frees nothing and keeps no
  *     pointer after the call returns. Tensor pointers must be 16-byte aligned.
@@ -56,8 +61,12 @@ enum {
                                 /* unbounded, i.e. causal)                                    */
   GBATTN_MASK_BLOCK_DIAG = 3,   /* floor((i + Sk - Sq) / block_size) == floor(j / block_size) */
   GBATTN_MASK_PREFIX_LM = 4,    /* j < prefix_len, or causal                                  */
-  GBATTN_MASK_DYNAMIC_TOPK = 5  /* j among the topk keys of (b,h) ranked by key_bias          */
+  GBATTN_MASK_DYNAMIC_TOPK = 5, /* j among the topk keys of (b,h) ranked by key_bias          */
                                 /* (descending, ties: lower index first), and causal          */
+  GBATTN_MASK_MINI_CAUSAL = 6   /* causal inside blocks: j <= i + (Sk - Sq) and               */
+                                /* floor((i + Sk - Sq) / block_size) == floor(j / block_size) */
+                                /* ([FA2C] names mini_causal without defining it; this is the */
+                                /* reading taken)                                              */
 };
 
 /* status codes */
@@ -83,7 +92,7 @@ enum {
 typedef struct {
   int kind;             /* GBATTN_MASK_*                                        */
   int window_left;      /* SLIDING                                               */
-  int block_size;       /* BLOCK_DIAG, > 0                                       */
+  int block_size;       /* BLOCK_DIAG and MINI_CAUSAL, > 0                       */
   int prefix_len;       /* PREFIX_LM, >= 0                                       */
   int topk;             /* DYNAMIC_TOPK, >= 0                                    */
   float rel_bias_slope; /* 0 = off                                               */
@@ -152,7 +161,7 @@ int build_block_mask(int B, int H, int Sq, int Sk, const gbattn_mask* mask,
  * block_sparse_tensors and return_lse). `blocks` may be NULL only for
  * GBATTN_MASK_NONE. o has the dtype of q; lse may be NULL.
  */
-int attn_fwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+int attn_fwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
              const void* q, const void* k, const void* v, float scale,
              const gbattn_mask* mask, const gbattn_blocks* blocks,
              void* o, float* lse, gbattn_stream stream);
@@ -173,7 +182,11 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk
  * `deterministic` says (0 or 1 are both accepted; any other value is
  * GBATTN_ERR_ARG). o and lse must be the outputs of attn_fwd for the same
  * inputs. workspace is device memory of at least attn_bwd_workspace_bytes();
- * its contents on entry do not matter.
+ * its contents on entry do not matter. With GQA (Hkv < H), dk / dv are
+ * [B,Hkv,Sk,D] and sum the contributions of the H / Hkv query heads of each
+ * group (one CTA walks all of them, still without atomics); bf16 accepts
+ * groups of up to 128 heads with (H/Hkv) * ceil(Sq/128) < 32768, and
+ * dkey_bias is not supported with GQA (GBATTN_ERR_UNSUPPORTED).
  * dkey_bias: NULL, or device [B,H,Sk] fp32 (4-byte aligned) that receives the
  * gradient of the loss with respect to key_bias: dkey_bias[b,h,j] =
  * sum_i P_ij (dP_ij - D_i) over the allowed pairs (the softcap factor does not
@@ -181,7 +194,7 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk
  * (it changes only where two biases cross). Written for every key, 0 for keys
  * no query sees; also defined when key_bias is NULL (the gradient at zero).
  */
-int attn_bwd(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+int attn_bwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
              const void* q, const void* k, const void* v, const void* o,
              const void* dout, const float* lse, float scale,
              const gbattn_mask* mask, const gbattn_blocks* blocks, int deterministic,
@@ -199,12 +212,39 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Dv, int num_sp
  * its K/V range once with 16-byte vector loads and writes a partial output and
  * LSE; a combine kernel merges them with the LSE-weighted rule of [PCB]
  * (num_splits == 1 writes O directly). bf16 only; mask kind NONE or CAUSAL,
- * no softcap or biases. 1 <= num_splits <= 64.
+ * no softcap or biases. 1 <= num_splits <= 64. With GQA the CTAs of the
+ * H / Hkv query heads of a group read the same key/value rows (L2 serves the
+ * repeats).
  */
-int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+int attn_fwd_splitkv(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
                      const void* q, const void* k, const void* v, float scale,
                      const gbattn_mask* mask, int num_splits, void* o, float* lse,
                      void* workspace, size_t workspace_bytes, gbattn_stream stream);
+
+/*
+ * attn_fwd_splitkv_paged - attn_fwd_splitkv over a paged key/value cache
+ * with a key count per sequence (the `page_table` / `seqused_k` arguments of
+ * [FA2C]'s `_flash_attn_fwd`; the page layout is this library's choice).
+ *   - k_cache, v_cache: [num_pages, Hkv, page_size, D] bf16: a page holds
+ *     page_size consecutive keys of one sequence for every key/value head,
+ *     each head's rows contiguous. page_size is a multiple of 64.
+ *   - page_table: device [B, max_pages_per_seq] int32; key t of sequence b
+ *     is row t % page_size of page page_table[b][t / page_size].
+ *   - seqlens_k: device [B] int32, keys of sequence b (0 ..
+ *     max_pages_per_seq * page_size). CAUSAL aligns query i with key
+ *     i + seqlens_k[b] - Sq.
+ *   - Splits cut each sequence's own keys (L = ceil(seqlens_k[b]/num_splits)
+ *     rounded up to 128). A page index outside [0, num_pages) or a key count
+ *     outside its range is not read: the kernel raises GBATTN_ERR_BLOCKS
+ *     (gbattn_last_device_error) and the affected outputs are invalid.
+ * Other arguments, workspace and status codes as attn_fwd_splitkv.
+ */
+int attn_fwd_splitkv_paged(int dtype, int B, int H, int Hkv, int Sq, int Dqk, int Dv,
+                           const void* q, const void* k_cache, const void* v_cache,
+                           int num_pages, int page_size, const int32_t* page_table,
+                           int max_pages_per_seq, const int32_t* seqlens_k, float scale,
+                           const gbattn_mask* mask, int num_splits, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, gbattn_stream stream);
 
 /*
  * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot
@@ -235,7 +275,7 @@ int attn_fwd_splitkv(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
  * attn_fwd_splitkv.
  */
 #define GBATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
-int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Sq, int Sk, int Dqk, int Dv,
+int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
                              const void* q, const void* k, const void* v, float scale,
                              const gbattn_mask* mask, int num_splits, void* o, float* lse,
                              gbattn_stream stream);

@@ -32,6 +32,9 @@ Readings where the pages are silent (each is also listed in the design doc):
   * sliding window keeps keys j with 0 <= (i + delta) - j <= window_left
     (window_left + 1 keys, self included); window_left < 0 = unbounded.
   * block_diagonal is bidirectional inside a block of the given size.
+  * mini_causal ([FA2C] lists it among the fuzz tester's mask names without
+    defining it) is causal inside each block of the given size: the
+    block-diagonal mask AND the causal mask.
   * prefix_lm allows j < prefix_len or the causal keys.
   * dynamic_topk: per (b, h), keep the first k keys in the order
     (key_bias descending, index ascending), AND causal; the bias is also
@@ -47,7 +50,7 @@ import math
 import numpy as np
 
 # Mask kinds (numbering is the C ABI's; the oracle keeps its own copy).
-NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK = range(6)
+NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL = range(7)
 
 
 def default_scale(dqk: int) -> float:
@@ -102,6 +105,10 @@ def allowed(kind: int, sq: int, sk: int, rows: np.ndarray, cols: np.ndarray, *,
         m = np.floor_divide(a, block_size) == np.floor_divide(j, block_size)
     elif kind == PREFIX_LM:
         m = (j < prefix_len) | (j <= a)
+    elif kind == MINI_CAUSAL:
+        if block_size <= 0:
+            raise ValueError("block_size must be positive")
+        m = (np.floor_divide(a, block_size) == np.floor_divide(j, block_size)) & (j <= a)
     elif kind == DYNAMIC_TOPK:
         if keep is None:
             raise ValueError("dynamic mask needs the keep set")

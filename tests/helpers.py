@@ -15,7 +15,7 @@ from oracle import attention as orc
 
 KIND = {"none": orc.NONE, "causal": orc.CAUSAL, "sliding": orc.SLIDING, "sliding_window": orc.SLIDING,
         "block_diag": orc.BLOCK_DIAG, "block_diagonal": orc.BLOCK_DIAG, "prefix_lm": orc.PREFIX_LM,
-        "dynamic": orc.DYNAMIC_TOPK}
+        "dynamic": orc.DYNAMIC_TOPK, "mini_causal": orc.MINI_CAUSAL}
 
 
 def spec_dicts(kind, Sq, Sk, window=None, block_size=256, prefix_len=64, topk=None, slope=0.0, softcap=0.0,
@@ -24,7 +24,7 @@ def spec_dicts(kind, Sq, Sk, window=None, block_size=256, prefix_len=64, topk=No
     d = dict(kind=k, rel_bias_slope=slope, softcap=softcap)
     if k == orc.SLIDING:
         d["window_left"] = max(64, min(Sq, Sk) // 3) if window is None else window
-    if k == orc.BLOCK_DIAG:
+    if k in (orc.BLOCK_DIAG, orc.MINI_CAUSAL):
         d["block_size"] = block_size
     if k == orc.PREFIX_LM:
         d["prefix_len"] = prefix_len
@@ -48,10 +48,12 @@ class Case:
     """Inputs on host and device, the GPU spec and lists, and the oracle spec."""
 
     def __init__(self, B, H, Sq, Sk, Dqk, Dv, kind="none", dtype="bf16", seed=42, sparse=(256, 512),
-                 use_bias=False, lists=True, gather=True, **kw):
+                 use_bias=False, lists=True, gather=True, Hkv=None, **kw):
         need_bias = use_bias or KIND[kind] == orc.DYNAMIC_TOPK
         self.shape = (B, H, Sq, Sk, Dqk, Dv)
-        self.x = make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype, seed=seed, bias=need_bias)
+        self.Hkv = H if Hkv is None else Hkv
+        self.G = H // self.Hkv
+        self.x = make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype, seed=seed, bias=need_bias, Hkv=self.Hkv)
         self.dev = {n: t.cuda() for n, t in self.x.items()}
         self.d = spec_dicts(kind, Sq, Sk, **kw)
         self.spec = to_gpu_spec(self.d, self.dev.get("key_bias"))
@@ -79,8 +81,10 @@ class Case:
         return torch.full((B, H, Sk), float("nan"), dtype=torch.float32, device="cuda")
 
     def problem(self, b, h):
+        """Oracle problem of query head h (it reads key/value head h // G)."""
         kb = self.od.get("key_bias")
-        return orc.Problem(self.h["q"][b, h], self.h["k"][b, h], self.h["v"][b, h], kind=self.od["kind"],
+        hk = h // self.G
+        return orc.Problem(self.h["q"][b, h], self.h["k"][b, hk], self.h["v"][b, hk], kind=self.od["kind"],
                            window_left=self.od.get("window_left", -1), block_size=self.od.get("block_size", 0),
                            prefix_len=self.od.get("prefix_len", 0), topk=self.od.get("topk", 0),
                            rel_bias_slope=self.od.get("rel_bias_slope", 0.0), softcap=self.od.get("softcap", 0.0),

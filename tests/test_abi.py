@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         assert hasattr(lib, n), n
     assert set(bd.EXPORTS) >= set(declared_functions())
-    assert lib.gbattn_version() == 101
+    assert lib.gbattn_version() == 102
 
 
 def test_strerror_covers_codes():
@@ -69,15 +69,19 @@ FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
 
 
 def _fwd(dtype=0, B=1, H=1, Sq=128, Sk=128, Dqk=64, Dv=64, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE,
-         mask=None, blocks=None):
+         mask=None, blocks=None, Hkv=None):
     lib = ga.load_library()
     m = mask.c() if mask is not None else None
-    return lib.attn_fwd(dtype, B, H, Sq, Sk, Dqk, Dv, q, k, v, 0.0, ctypes.byref(m) if m else None,
+    return lib.attn_fwd(dtype, B, H, H if Hkv is None else Hkv, Sq, Sk, Dqk, Dv, q, k, v, 0.0,
+                        ctypes.byref(m) if m else None,
                         ctypes.byref(blocks) if blocks else None, o, lse, None)
 
 
 def test_fwd_argument_checks():
     assert _fwd(B=0) == bd.ERR_ARG
+    assert _fwd(H=4, Hkv=3) == bd.ERR_ARG   # Hkv must divide H
+    assert _fwd(H=4, Hkv=0) == bd.ERR_ARG
+    assert _fwd(H=4, Hkv=8) == bd.ERR_ARG
     assert _fwd(Sk=-1) == bd.ERR_ARG
     assert _fwd(q=0) == bd.ERR_ARG
     assert _fwd(q=FAKE + 8) == bd.ERR_ALIGN
@@ -105,20 +109,34 @@ def test_valid_call_without_gpu_reports_unsupported_device():
 
 def test_bwd_and_splitkv_argument_checks():
     lib = ga.load_library()
-    args = [0, 1, 1, 128, 128, 64, 64] + [FAKE] * 6 + [0.0, None, None]
+    args = [0, 1, 1, 1, 128, 128, 64, 64] + [FAKE] * 6 + [0.0, None, None]
     assert lib.attn_bwd(*args, 2, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, None) == bd.ERR_ARG   # deterministic flag
     assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, None, 1 << 30, None) == bd.ERR_WORKSPACE
     assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, None, FAKE, 16, None) == bd.ERR_WORKSPACE
     assert lib.attn_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE + 2, FAKE, 1 << 30, None) == bd.ERR_ALIGN  # dkey_bias
-    sk = [0, 32, 32, 1, 65536, 128, 128, FAKE, FAKE, FAKE, 0.0, None]
+    gqa = [0, 1, 4, 2] + args[4:]
+    assert lib.attn_bwd(*gqa, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == bd.ERR_UNSUPPORTED  # dkey_bias + GQA
+    sk = [0, 32, 32, 32, 1, 65536, 128, 128, FAKE, FAKE, FAKE, 0.0, None]
     assert lib.attn_fwd_splitkv(*sk, 0, FAKE, FAKE, None, 0, None) == bd.ERR_ARG          # 0 splits
     assert lib.attn_fwd_splitkv(*sk, 4, FAKE, FAKE, None, 0, None) == bd.ERR_WORKSPACE
     m = bd.MaskSpec(kind=bd.SLIDING, window_left=3).c()
-    sk2 = sk[:11] + [ctypes.byref(m)]
+    sk2 = sk[:12] + [ctypes.byref(m)]
     assert lib.attn_fwd_splitkv(*sk2, 1, FAKE, FAKE, None, 0, None) == bd.ERR_UNSUPPORTED
     sk3 = list(sk)
     sk3[0] = 1
     assert lib.attn_fwd_splitkv(*sk3, 1, FAKE, FAKE, None, 0, None) == bd.ERR_UNSUPPORTED  # fp32 decode
+    # paged decode: page size a multiple of 64, page table and key counts required
+    pg = lambda **kw: lib.attn_fwd_splitkv_paged(  # noqa: E731
+        0, 2, 8, kw.get("Hkv", 2), 1, 128, 128, FAKE, FAKE, FAKE, kw.get("num_pages", 16), kw.get("page_size", 256),
+        kw.get("table", FAKE), 8, kw.get("seqlens", FAKE), 0.0, None, kw.get("splits", 1), FAKE, FAKE, None, 0, None)
+    assert pg(page_size=100) == bd.ERR_ARG
+    assert pg(page_size=32) == bd.ERR_ARG
+    assert pg(table=None) == bd.ERR_ARG
+    assert pg(seqlens=None) == bd.ERR_ARG
+    assert pg(num_pages=0) == bd.ERR_ARG
+    assert pg(Hkv=3) == bd.ERR_ARG
+    assert pg(table=FAKE + 2) == bd.ERR_ALIGN
+    assert pg(splits=4) == bd.ERR_WORKSPACE
 
 
 def test_build_block_mask_argument_checks():

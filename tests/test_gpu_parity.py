@@ -32,7 +32,7 @@ def lists_equal(c, B, H, Sq, Sk, sm, sn):
 
 
 # ------------------------------------------------------------------ a1 build_block_mask
-@pytest.mark.parametrize("kind", ["causal", "sliding", "block_diag", "prefix_lm", "dynamic", "none"])
+@pytest.mark.parametrize("kind", ["causal", "sliding", "block_diag", "prefix_lm", "dynamic", "none", "mini_causal"])
 @pytest.mark.parametrize("Sq,Sk,sm,sn", [(1000, 1000, 256, 512), (383, 769, 256, 256), (1025, 511, 128, 128),
                                          (640, 512, 256, 512), (129, 257, 128, 256)])
 def test_block_mask_bit_exact(kind, Sq, Sk, sm, sn):
@@ -76,6 +76,8 @@ FWD_CASES = [
     (1, 2, 900, 900, 64, 64, "dynamic", dict(topk=200)),
     (1, 1, 256, 384, 128, 128, "causal", dict(softcap=2.0, use_bias=True)),
     (1, 1, 1025, 511, 128, 128, "sliding", {}),
+    (1, 2, 1000, 1000, 64, 64, "mini_causal", dict(block_size=192)),
+    (1, 1, 513, 769, 192, 128, "mini_causal", dict(block_size=128, slope=0.01)),
 ]
 
 
@@ -96,8 +98,6 @@ def test_forward_bf16(case):
 @pytest.mark.parametrize("row", read_golden("fa_pr2661_fuzz_cases.txt"), ids=lambda r: r[0])
 def test_forward_fuzz_shapes(row):
     seed, sq, sk, dqk, dv, stm, stn, name = row
-    if name == "mini_causal":
-        pytest.skip("mini_causal is out of scope")
     c = Case(1, 1, int(sq), int(sk), int(dqk), int(dv), name, seed=int(seed), sparse=(int(stm), int(stn)),
              slope=0.01, block_size=256)
     o, lse = c.fwd()
@@ -117,6 +117,7 @@ BWD_CASES = [
     (1, 1, 700, 700, 64, 64, "dynamic", dict(topk=150)),
     (1, 1, 512, 512, 192, 128, "block_diag", dict(block_size=256)),
     (1, 1, 300, 260, 128, 128, "causal", dict(softcap=2.0, use_bias=True)),
+    (1, 2, 700, 640, 64, 64, "mini_causal", dict(block_size=200)),
 ]
 
 
@@ -224,11 +225,127 @@ def test_gathered_gradients_are_bitwise_reproducible():
         assert torch.equal(x, y)
 
 
+# ------------------------------------------------------------------ grouped-query attention (GQA)
+GQA_CASES = [
+    # B, H, Hkv, Sq, Sk, Dqk, Dv, kind, extras, dtype
+    (1, 4, 2, 640, 700, 128, 128, "causal", dict(slope=0.01), "bf16"),
+    (2, 8, 1, 513, 513, 64, 64, "sliding", {}, "bf16"),
+    (1, 6, 2, 512, 640, 192, 128, "block_diag", dict(block_size=256), "bf16"),
+    (1, 4, 2, 700, 700, 64, 64, "dynamic", dict(topk=250), "bf16"),       # per-head keep sets, shared K/V
+    (1, 4, 1, 384, 300, 32, 32, "prefix_lm", dict(prefix_len=100, softcap=2.0, use_bias=True), "bf16"),
+    (1, 4, 2, 150, 170, 32, 16, "causal", dict(slope=0.02), "fp32"),
+]
+
+
+@pytest.mark.parametrize("case", GQA_CASES, ids=lambda c: f"{c[7]}-h{c[1]}kv{c[2]}-{c[9]}")
+def test_gqa_forward_backward(case):
+    # dK / dV of a key/value head are the sums over its query heads
+    B, H, Hkv, Sq, Sk, Dqk, Dv, kind, ex, dt = case
+    c = Case(B, H, Sq, Sk, Dqk, Dv, kind, dtype=dt, Hkv=Hkv, sparse=(128, 256), **ex)
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    assert dk.shape == (B, Hkv, Sk, Dqk) and dv.shape == (B, Hkv, Sk, Dv)
+    fp32 = dt == "fp32"
+    G = H // Hkv
+    for b in range(B):
+        for hk in range(Hkv):
+            dk_r = np.zeros((Sk, Dqk))
+            dv_r = np.zeros((Sk, Dv))
+            for h in range(hk * G, (hk + 1) * G):
+                p = c.problem(b, h)
+                o_ref, l_ref = p.forward()
+                check_out(f64(o[b, h]), o_ref, fp32=fp32)
+                check_lse(f64(lse[b, h]), l_ref, fp32=fp32)
+                dq_r, dkh, dvh, _ = p.backward(c.h["do"][b, h])
+                check_grad(f64(dq[b, h]), dq_r, "dQ", fp32=fp32)
+                dk_r += dkh
+                dv_r += dvh
+            check_grad(f64(dk[b, hk]), dk_r, "dK", fp32=fp32)
+            check_grad(f64(dv[b, hk]), dv_r, "dV", fp32=fp32)
+
+
+@pytest.mark.parametrize("n", [1, 4])
+@pytest.mark.parametrize("Hkv", [1, 2])
+def test_gqa_splitkv_decode(n, Hkv):
+    c = Case(2, 4, 2, 1500, 128, 128, "causal", Hkv=Hkv, lists=False, sparse=None)
+    o, lse = ga.attn_fwd_splitkv(c.dev["q"], c.dev["k"], c.dev["v"], 0.0, c.spec, n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for b in range(2):
+        for h in range(4):
+            o_ref, l_ref = c.problem(b, h).forward()
+            check_out(f64(o[b, h]), o_ref)
+            check_lse(f64(lse[b, h]), l_ref)
+
+
+def _paged_cache(k, v, page_size, seqlens, extra_pages, seed):
+    """Scatter dense per-sequence K/V [B, Hkv, S, D] into a shuffled page pool
+    [num_pages, Hkv, page_size, D] and its page table (test set-up only)."""
+    B, Hkv, S, D = k.shape
+    need = [-(-int(n) // page_size) for n in seqlens]
+    max_pages = max(1, max(need))
+    num_pages = sum(need) + extra_pages
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(num_pages)
+    kc = torch.zeros(num_pages, Hkv, page_size, D, dtype=k.dtype)
+    vc = torch.zeros_like(kc)
+    table = np.full((B, max_pages), 10 ** 6, dtype=np.int32)  # unused entries: never read
+    t = 0
+    for b in range(B):
+        for pgi in range(need[b]):
+            pg = int(order[t])
+            t += 1
+            table[b, pgi] = pg
+            r0, r1 = pgi * page_size, min((pgi + 1) * page_size, int(seqlens[b]))
+            kc[pg, :, : r1 - r0] = k[b, :, r0:r1]
+            vc[pg, :, : r1 - r0] = v[b, :, r0:r1]
+    return kc, vc, torch.from_numpy(table)
+
+
+@pytest.mark.parametrize("page_size,n,kind,Hkv", [(64, 1, "none", 2), (128, 4, "causal", 1), (256, 16, "none", 4),
+                                                   (192, 2, "causal", 2)])
+def test_paged_splitkv_decode(page_size, n, kind, Hkv):
+    B, H, Sq, S, D = 4, 4, 2, 1100, 128
+    c = Case(B, H, Sq, S, D, D, kind, Hkv=Hkv, lists=False, sparse=None)
+    seqlens = np.array([1100, 0, 1, 777])
+    kc, vc, table = _paged_cache(c.x["k"], c.x["v"], page_size, seqlens, extra_pages=3, seed=page_size)
+    o, lse = ga.attn_fwd_splitkv_paged(c.dev["q"], kc.cuda(), vc.cuda(), table.cuda(),
+                                       torch.from_numpy(seqlens.astype(np.int32)).cuda(), 0.0, c.spec, n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    G = H // Hkv
+    for b in range(B):
+        L = int(seqlens[b])
+        for h in range(H):
+            if L == 0:
+                assert np.all(f64(o[b, h]) == 0) and np.all(np.isneginf(f64(lse[b, h])))
+                continue
+            p = orc.Problem(c.h["q"][b, h], c.h["k"][b, h // G][:L], c.h["v"][b, h // G][:L], kind=c.od["kind"])
+            o_ref, l_ref = p.forward()
+            check_out(f64(o[b, h]), o_ref)
+            check_lse(f64(lse[b, h]), l_ref)
+
+
+def test_paged_decode_bad_page_index_raises_device_error():
+    # a page index outside the pool is not read: the kernel flags it
+    B, H, D = 1, 2, 64
+    q = torch.randn(B, H, 1, D).to(torch.bfloat16).cuda()
+    kc = torch.zeros(2, H, 64, D, dtype=torch.bfloat16).cuda()
+    table = torch.tensor([[0, 5]], dtype=torch.int32).cuda()
+    seqlens = torch.tensor([100], dtype=torch.int32).cuda()
+    ga.attn_fwd_splitkv_paged(q, kc, kc, table, seqlens, 0.0, None, 1)
+    torch.cuda.synchronize()
+    assert ga.load_library().gbattn_last_device_error(None) == ga.binding.ERR_BLOCKS
+
+
 # ------------------------------------------------------------------ fp32 path
 @pytest.mark.parametrize("case", [(1, 1, 128, 128, 64, 64, "causal", {}),
                                   (1, 2, 200, 333, 48, 24, "sliding", dict(window=50, slope=0.02)),
                                   (1, 1, 150, 150, 64, 64, "dynamic", dict(topk=40)),
-                                  (1, 1, 130, 100, 16, 16, "block_diag", dict(block_size=64, softcap=1.5))],
+                                  (1, 1, 130, 100, 16, 16, "block_diag", dict(block_size=64, softcap=1.5)),
+                                  (1, 1, 150, 130, 32, 32, "mini_causal", dict(block_size=48))],
                          ids=lambda c: c[6])
 def test_fp32_forward_backward(case):
     B, H, Sq, Sk, Dqk, Dv, kind, ex = case

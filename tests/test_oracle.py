@@ -21,6 +21,7 @@ KINDS = {
     "block_diag": dict(kind=A.BLOCK_DIAG, block_size=8),
     "prefix_lm": dict(kind=A.PREFIX_LM, prefix_len=6),
     "dynamic": dict(kind=A.DYNAMIC_TOPK, topk=9),
+    "mini_causal": dict(kind=A.MINI_CAUSAL, block_size=4),
 }
 
 
@@ -256,6 +257,55 @@ def test_matches_torch_float64_sdpa_and_autograd(name):
     assert np.allclose(lse, ref_lse, atol=1e-12)
 
 
+def test_grouped_query_reading_matches_torch_enable_gqa():
+    # GQA reading: query head h reads key/value head h // (H / Hkv), and the
+    # gradient of a key/value head sums over its query heads. Pinned against
+    # torch's float64 SDPA with enable_gqa=True and autograd (a library routine).
+    rng = np.random.default_rng(21)
+    H, Hkv, sq, sk, d = 6, 2, 19, 23, 8
+    G = H // Hkv
+    q, k, v = _rand(rng, H, sq, d), _rand(rng, Hkv, sk, d), _rand(rng, Hkv, sk, d)
+    do = _rand(rng, H, sq, d)
+    rows, cols = np.arange(sq), np.arange(sk)
+    m = A.allowed(A.CAUSAL, sq, sk, rows, cols)
+    tq = torch.tensor(q, requires_grad=True)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], tk[None], tv[None], attn_mask=torch.tensor(m)[None, None], enable_gqa=True)[0]
+    out.backward(torch.tensor(do))
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(H):
+        p = A.Problem(q[h], k[h // G], v[h // G], kind=A.CAUSAL)
+        o, _ = p.forward()
+        assert np.allclose(o, out[h].detach().numpy(), atol=1e-12)
+        dq_h, dk_h, dv_h, _ = p.backward(do[h])
+        assert np.allclose(dq_h, tq.grad[h].numpy(), atol=1e-11)
+        dk[h // G] += dk_h
+        dv[h // G] += dv_h
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-11)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+def test_mini_causal_reading():
+    # causal inside blocks: a per-element brute force of the reading, its
+    # closed-form pair count, and the two limits (one block = causal; blocks
+    # of one key = the diagonal only)
+    for sq, sk, bs in ((16, 16, 4), (13, 21, 5), (21, 13, 3)):
+        m = A.allowed(A.MINI_CAUSAL, sq, sk, np.arange(sq), np.arange(sk), block_size=bs)
+        for i in range(sq):
+            a = i + sk - sq
+            for j in range(sk):
+                assert m[i, j] == (j <= a and a // bs == j // bs)
+    S, bs = 1024, 128
+    assert A.pair_count(S, S, dict(kind=A.MINI_CAUSAL, block_size=bs)) == (S // bs) * bs * (bs + 1) // 2
+    rows, cols = np.arange(40), np.arange(40)
+    assert np.array_equal(A.allowed(A.MINI_CAUSAL, 40, 40, rows, cols, block_size=64),
+                          A.allowed(A.CAUSAL, 40, 40, rows, cols))
+    assert np.array_equal(A.allowed(A.MINI_CAUSAL, 40, 40, rows, cols, block_size=1), np.eye(40, dtype=bool))
+
+
 def test_topk_matches_brute_force_ranks_with_ties():
     rng = np.random.default_rng(10)
     for sk, k in ((40, 7), (64, 64), (33, 50), (50, 0), (1, 1)):
@@ -374,13 +424,14 @@ def test_block_lists_block_diag_and_ragged_edge():
     assert list(lists["q_mask_cnt"][0, 0]) == [1, 1, 1, 4]
 
 
-@pytest.mark.parametrize("row", read_golden("fa_pr2661_fuzz_cases.txt")[:10])
+@pytest.mark.parametrize("row", read_golden("fa_pr2661_fuzz_cases.txt"))
 def test_fwd_and_bwd_lists_describe_the_same_blocks(row):
     seed, sq, sk, dqk, dv, stm, stn, name = row
     sq, sk, stm, stn = int(sq), int(sk), int(stm), int(stn)
     spec = {"causal": dict(kind=A.CAUSAL),
             "sliding_window": dict(kind=A.SLIDING, window_left=max(64, min(sq, sk) // 3)),
-            "block_diagonal": dict(kind=A.BLOCK_DIAG, block_size=256)}[name]
+            "block_diagonal": dict(kind=A.BLOCK_DIAG, block_size=256),
+            "mini_causal": dict(kind=A.MINI_CAUSAL, block_size=256)}[name]
     L = A.block_lists(1, 1, sq, sk, spec, stm, stn)
     fwd = {(r, int(L["q_mask_idx"][0, 0, r, t]), "m") for r in range(L["q_mask_cnt"].shape[2])
            for t in range(L["q_mask_cnt"][0, 0, r])}

@@ -25,7 +25,8 @@ def _call_noalloc(q, k, v, n, o, lse):
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
     m = bd.MaskSpec().c()
-    return lib.attn_fwd_splitkv_noalloc(bd.BF16, B, H, Sq, Sk, D, D, q.data_ptr(), k.data_ptr(), v.data_ptr(), 0.0,
+    return lib.attn_fwd_splitkv_noalloc(bd.BF16, B, H, k.shape[1], Sq, Sk, D, D, q.data_ptr(), k.data_ptr(),
+                                        v.data_ptr(), 0.0,
                                         ctypes.byref(m), n, o.data_ptr(), lse.data_ptr(),
                                         torch.cuda.current_stream().cuda_stream)
 
@@ -39,7 +40,7 @@ def _call_with_workspace(q, k, v, n):
     need = lib.attn_fwd_splitkv_workspace_bytes(B, H, Sq, D, n)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     m = bd.MaskSpec().c()
-    rc = lib.attn_fwd_splitkv(bd.BF16, B, H, Sq, Sk, D, D, q.data_ptr(), k.data_ptr(), v.data_ptr(), 0.0,
+    rc = lib.attn_fwd_splitkv(bd.BF16, B, H, k.shape[1], Sq, Sk, D, D, q.data_ptr(), k.data_ptr(), v.data_ptr(), 0.0,
                               ctypes.byref(m), n, o.data_ptr(), lse.data_ptr(), ws.data_ptr(), need,
                               torch.cuda.current_stream().cuda_stream)
     assert rc == 0
@@ -50,7 +51,7 @@ def test_rejects_problems_larger_than_the_scratch():
     lib = bd.load_library()
     fake = 1 << 20
     # 64 splits x 64 x 64 rows x 128 fp32 partials = 128 MiB > 16 MiB
-    rc = lib.attn_fwd_splitkv_noalloc(bd.BF16, 64, 64, 1, 65536, 128, 128, fake, fake, fake, 0.0, None, 64,
+    rc = lib.attn_fwd_splitkv_noalloc(bd.BF16, 64, 64, 64, 1, 65536, 128, 128, fake, fake, fake, 0.0, None, 64,
                                       fake, fake, None)
     assert rc == bd.ERR_WORKSPACE
     assert lib.attn_fwd_splitkv_workspace_bytes(64, 64, 1, 128, 64) > SCRATCH

@@ -18,7 +18,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgbattn.so")
 
-NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL = range(7)
+NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL, TABLE = range(8)
 BF16, FP32 = 0, 1
 _DT = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -35,7 +35,8 @@ class GbattnError(RuntimeError):
 class _Mask(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("window_left", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("prefix_len", ctypes.c_int), ("topk", ctypes.c_int), ("rel_bias_slope", ctypes.c_float),
-                ("softcap", ctypes.c_float), ("key_bias", ctypes.c_void_p)]
+                ("softcap", ctypes.c_float), ("key_bias", ctypes.c_void_p), ("table", ctypes.c_void_p),
+                ("table_per_head", ctypes.c_int)]
 
 
 class _Blocks(ctypes.Structure):
@@ -130,11 +131,28 @@ class MaskSpec:
     rel_bias_slope: float = 0.0
     softcap: float = 0.0
     key_bias: Optional[torch.Tensor] = None  # [B, H, Sk] fp32 on the GPU
+    table: Optional[torch.Tensor] = None     # TABLE: int32 bits [Sq, ceil(Sk/32)] or [B, H, Sq, ceil(Sk/32)]
 
     def c(self) -> _Mask:
         return _Mask(self.kind, self.window_left, self.block_size, self.prefix_len, self.topk,
                      float(self.rel_bias_slope), float(self.softcap),
-                     None if self.key_bias is None else self.key_bias.data_ptr())
+                     None if self.key_bias is None else self.key_bias.data_ptr(),
+                     None if self.table is None else self.table.data_ptr(),
+                     0 if self.table is None or self.table.dim() == 2 else 1)
+
+
+def pack_mask_table(allowed: torch.Tensor) -> torch.Tensor:
+    """Packs a boolean element mask [..., Sq, Sk] into the TABLE kind's bits:
+    int32 words [..., Sq, ceil(Sk/32)], bit j % 32 of word j // 32 = pair
+    (i, j) allowed. Runs on the tensor's device (torch ops, no attention
+    arithmetic)."""
+    *lead, sq, sk = allowed.shape
+    nw = (sk + 31) // 32
+    pad = torch.zeros(*lead, sq, nw * 32, dtype=torch.int64, device=allowed.device)
+    pad[..., :sk] = allowed.to(torch.int64)
+    w = pad.view(*lead, sq, nw, 32) << torch.arange(32, device=allowed.device, dtype=torch.int64)
+    packed = w.sum(-1)  # < 2^32
+    return (packed - (packed >= 2 ** 31).to(torch.int64) * 2 ** 32).to(torch.int32).contiguous()
 
 
 @dataclass

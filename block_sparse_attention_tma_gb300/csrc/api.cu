@@ -77,7 +77,9 @@ int check_mask(const gbattn_mask* mask, HostMask* hm) {
   hm->kind = GBATTN_MASK_NONE;
   hm->window_left = -1;
   if (!mask) return GBATTN_OK;
-  if (mask->kind < GBATTN_MASK_NONE || mask->kind > GBATTN_MASK_MINI_CAUSAL) return GBATTN_ERR_ARG;
+  if (mask->kind < GBATTN_MASK_NONE || mask->kind > GBATTN_MASK_TABLE) return GBATTN_ERR_ARG;
+  if (mask->kind == GBATTN_MASK_TABLE && !mask->table) return GBATTN_ERR_ARG;
+  if (mask->table && !aligned4(mask->table)) return GBATTN_ERR_ALIGN;
   if ((mask->kind == GBATTN_MASK_BLOCK_DIAG || mask->kind == GBATTN_MASK_MINI_CAUSAL) && mask->block_size <= 0)
     return GBATTN_ERR_ARG;
   if (mask->kind == GBATTN_MASK_PREFIX_LM && mask->prefix_len < 0) return GBATTN_ERR_ARG;
@@ -92,6 +94,8 @@ int check_mask(const gbattn_mask* mask, HostMask* hm) {
   hm->slope = mask->rel_bias_slope;
   hm->softcap = mask->softcap;
   hm->key_bias = mask->key_bias;
+  hm->table = mask->kind == GBATTN_MASK_TABLE ? mask->table : nullptr;
+  hm->table_per_head = mask->table_per_head != 0;
   return GBATTN_OK;
 }
 
@@ -426,7 +430,8 @@ int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Hkv, int Sq, int Sk, i
 int gbattn_last_device_error(gbattn_stream stream) {
   if (device_check() != GBATTN_OK) return GBATTN_ERR_UNSUPPORTED;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GBATTN_ERR_CUDA;
-  int errs[5] = {fwd_take_error(), bwd_take_error(), simt_take_error(), decode_take_error(), blockmask_take_error()};
+  int errs[6] = {fwd_take_error(),    bwd_take_error(),    dkdv_take_error(),
+                 simt_take_error(),   decode_take_error(), blockmask_take_error()};
   for (int e : errs)
     if (e == GBATTN_ERR_CUDA) return e;
   for (int e : errs)

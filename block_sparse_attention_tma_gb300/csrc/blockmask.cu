@@ -161,9 +161,11 @@ __device__ long long block_pairs(const ListArgs& a, int bh, int r, int c) {
     row_interval(a.mask, i, a.Sq, a.Sk, lo, hi);
     const int s = max(lo, c0), e = min(hi, c1 - 1);
     if (e < s) continue;
-    if (a.mask.kind == GBATTN_MASK_DYNAMIC_TOPK) {
+    // dynamic: the head's keep bits; element table: this row's bits
+    const uint32_t* bitsrc = a.mask.table ? table_row(a.mask, bh, a.Sq, i) : keep;
+    if (bitsrc) {
       for (int w = s >> 5; w <= (e >> 5); ++w) {
-        uint32_t bits = __ldg(keep + w);
+        uint32_t bits = __ldg(bitsrc + w);
         const int wb = w << 5;
         if (s > wb) bits &= ~((1u << (s - wb)) - 1u);
         if (e < wb + 31) bits &= (1u << (e - wb + 1)) - 1u;
@@ -245,6 +247,8 @@ int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbat
   a.mask.block_size = m.block_size;
   a.mask.prefix_len = m.prefix_len;
   a.mask.nkw = (Sk + 31) / 32;
+  a.mask.table = m.kind == GBATTN_MASK_TABLE ? m.table : nullptr;
+  a.mask.table_per_head = m.table_per_head;
   a.Sq = Sq;
   a.Sk = Sk;
   a.sm = out->sparse_m;

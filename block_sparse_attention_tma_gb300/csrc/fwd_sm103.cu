@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     else row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
     const uint32_t* keep = GAT ? nullptr : keep_h;  // gathered keys are all kept
+    if (p.mask.table) keep = i < p.Sq ? table_row(p.mask, bh, p.Sq, i) : nullptr;  // this row's element bits
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0;
     bool ok = true;
@@ -622,6 +623,8 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.mask.slope = m.slope;
   prm.mask.key_bias = m.key_bias;
   prm.mask.keep = m.kind == GBATTN_MASK_DYNAMIC_TOPK ? m.keep : nullptr;
+  prm.mask.table = m.kind == GBATTN_MASK_TABLE ? m.table : nullptr;
+  prm.mask.table_per_head = m.table_per_head;
   prm.mask.nkw = (s.Sk + 31) / 32;
   prm.has_lists = m.gather ? 0 : m.has_lists;
   if (prm.has_lists) {

@@ -26,6 +26,8 @@ struct HostMask {
   float slope, softcap;
   const float* key_bias;
   const uint32_t* keep;
+  const uint32_t* table;  // element table (mask kind TABLE)
+  int table_per_head;
   int has_lists;
   int sparse_m, sparse_n, nqb, nkb;
   const int32_t *q_mask_cnt, *q_mask_idx, *q_full_cnt, *q_full_idx;
@@ -74,6 +76,7 @@ int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbat
 // Device error words, one per translation unit (read and cleared).
 int fwd_take_error();
 int bwd_take_error();
+int dkdv_take_error();
 int simt_take_error();
 int decode_take_error();
 int blockmask_take_error();

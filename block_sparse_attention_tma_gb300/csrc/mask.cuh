@@ -31,8 +31,15 @@ struct MaskParams {
   float slope;             // rel-bias slope (score += slope * (i - j))
   const float* key_bias;   // [B*H, Sk] or nullptr
   const uint32_t* keep;    // [B*H, nkw] (dynamic) or nullptr
-  int nkw;                 // words per (b,h) in keep
+  int nkw;                 // words per (b,h) in keep; words per row of table
+  const uint32_t* table;   // element table: [Sq, nkw] or [B*H, Sq, nkw] bits, or nullptr
+  int table_per_head;      // 1: one table per (b, h)
 };
+
+// Row i's words of the element table (mask kind TABLE) of head bh.
+__device__ __forceinline__ const uint32_t* table_row(const MaskParams& m, int bh, int Sq, int i) {
+  return m.table + ((m.table_per_head ? (size_t)bh * Sq : 0) + (size_t)i) * m.nkw;
+}
 
 // ---- gathered keys ----------------------------------------------------------
 // Number of kept keys with index <= a among the keep bits of one head (nkw
@@ -189,7 +196,7 @@ __device__ __forceinline__ int tile_class(const MaskParams& m, int q0, int k0, i
   row_interval(m, q0, Sq, Sk, lo_f, hi_f);
   row_interval(m, q1 - 1, Sq, Sk, lo_l, hi_l);
   if (hi_l < k0 || lo_f > k1 - 1) return TILE_EMPTY;
-  if (m.kind == GBATTN_MASK_DYNAMIC_TOPK) return TILE_PARTIAL;
+  if (m.kind == GBATTN_MASK_DYNAMIC_TOPK || m.kind == GBATTN_MASK_TABLE) return TILE_PARTIAL;
   const bool whole = (k1 - k0 == 128) && (!rows_whole || q1 - q0 == 128);
   if (whole && lo_l <= k0 && hi_f >= k1 - 1) return TILE_FULL;
   return TILE_PARTIAL;

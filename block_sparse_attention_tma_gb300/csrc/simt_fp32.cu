@@ -46,10 +46,11 @@ __device__ __forceinline__ float simt_score(const SimtParams& p, float dot, int 
   return s;
 }
 
-__device__ __forceinline__ bool simt_allowed(const SimtParams& p, int i, int j, int lo, int hi,
+__device__ __forceinline__ bool simt_allowed(const SimtParams& p, int bh, int i, int j, int lo, int hi,
                                              const uint32_t* keep) {
   if (j < lo || j > hi || j >= p.Sk || i >= p.Sq) return false;
   if (keep) return (__ldg(keep + (j >> 5)) >> (j & 31)) & 1u;
+  if (p.mask.table) return (__ldg(table_row(p.mask, bh, p.Sq, i) + (j >> 5)) >> (j & 31)) & 1u;
   return true;
 }
 
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_fwd_kernel(const SimtParams
         for (int d = 0; d < DQ; ++d) dot = fmaf(sQ[row * DQ + d], sK[lane * (DQ + 1) + d], dot);
         float dcap;
         float sc = simt_score(p, dot, i, j, kb, &dcap);
-        if (!simt_allowed(p, i, j, lo[rr], hi[rr], keep)) sc = -INFINITY;
+        if (!simt_allowed(p, bh, i, j, lo[rr], hi[rr], keep)) sc = -INFINITY;
         float mx = sc;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dq_kernel(const SimtParams 
         for (int d = 0; d < DV; ++d) dp = fmaf(sG[row * DV + d], sV[lane * (DV + 1) + d], dp);
         float dcap;
         const float sc = simt_score(p, dot, i, j, kb, &dcap);
-        const bool al = simt_allowed(p, i, j, lo[rr], hi[rr], keep) && lse[rr] != -INFINITY;
+        const bool al = simt_allowed(p, bh, i, j, lo[rr], hi[rr], keep) && lse[rr] != -INFINITY;
         const float pj = al ? expf(sc - lse[rr]) : 0.f;
         const float ds = pj * (dp - dl[rr]) * dcap;
         for (int jj = 0; jj < kChunk; ++jj) {
@@ -351,7 +352,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_dkdv_kernel(const SimtParam
           for (int d = 0; d < DV; ++d) dp = fmaf(sG[lane * (DV + 1) + d], sV[kr * DV + d], dp);
           float dcap;
           const float sc = simt_score(p, dot, i, j, kb, &dcap);
-          const bool al = kept[kk] && i >= lo[kk] && i <= hi[kk] && i < p.Sq && lse != -INFINITY;
+          const bool al = kept[kk] && i >= lo[kk] && i <= hi[kk] && i < p.Sq && lse != -INFINITY &&
+                          (!p.mask.table || ((__ldg(table_row(p.mask, bh, p.Sq, i) + (j >> 5)) >> (j & 31)) & 1u));
           const float pj = al ? expf(sc - lse) : 0.f;
           const float ds0 = pj * (dp - dl);
           dbk[kk] += ds0;
@@ -407,6 +409,8 @@ static void fill_simt(SimtParams& prm, const Shape& s, float scale, const HostMa
   prm.mask.slope = m.slope;
   prm.mask.key_bias = m.key_bias;
   prm.mask.keep = m.kind == GBATTN_MASK_DYNAMIC_TOPK ? m.keep : nullptr;
+  prm.mask.table = m.kind == GBATTN_MASK_TABLE ? m.table : nullptr;
+  prm.mask.table_per_head = m.table_per_head;
   prm.mask.nkw = (s.Sk + 31) / 32;
   prm.has_lists = m.has_lists;
   if (m.has_lists) {

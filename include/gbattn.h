@@ -63,10 +63,15 @@ enum {
   GBATTN_MASK_PREFIX_LM = 4,    /* j < prefix_len, or causal                                  */
   GBATTN_MASK_DYNAMIC_TOPK = 5, /* j among the topk keys of (b,h) ranked by key_bias          */
                                 /* (descending, ties: lower index first), and causal          */
-  GBATTN_MASK_MINI_CAUSAL = 6   /* causal inside blocks: j <= i + (Sk - Sq) and               */
+  GBATTN_MASK_MINI_CAUSAL = 6,  /* causal inside blocks: j <= i + (Sk - Sq) and               */
                                 /* floor((i + Sk - Sq) / block_size) == floor(j / block_size) */
                                 /* ([FA2C] names mini_causal without defining it; this is the */
                                 /* reading taken)                                              */
+  GBATTN_MASK_TABLE = 7         /* any element predicate: pair (i, j) allowed iff bit j % 32   */
+                                /* of word j / 32 of row i of `table` is set (the caller      */
+                                /* evaluates its predicate, e.g. a flex_attention mask_mod,   */
+                                /* into the table once; [FA2C] builds block lists from such a */
+                                /* predicate)                                                  */
 };
 
 /* status codes */
@@ -99,6 +104,11 @@ typedef struct {
   float softcap;        /* 0 = off                                               */
   const float* key_bias;/* device [B,H,Sk] fp32 additive key bias, or NULL; required */
                         /* for DYNAMIC_TOPK (it is also the ranking key)          */
+  const uint32_t* table;/* TABLE: device bits, ceil(Sk/32) uint32 words per query row: */
+                        /* [Sq, ceil(Sk/32)] shared by every (b,h), or             */
+                        /* [B,H,Sq, ceil(Sk/32)] when table_per_head; bits past Sk */
+                        /* are ignored. NULL for the other kinds.                  */
+  int table_per_head;   /* 0: one table for all heads; 1: one per (b,h)           */
 } gbattn_mask;
 
 /*

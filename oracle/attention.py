@@ -35,6 +35,9 @@ Readings where the pages are silent (each is also listed in the design doc):
   * mini_causal ([FA2C] lists it among the fuzz tester's mask names without
     defining it) is causal inside each block of the given size: the
     block-diagonal mask AND the causal mask.
+  * table: an arbitrary element predicate given as a boolean matrix
+    [Sq, Sk] (the stand-in for flex_attention's mask_mod, from which [FA2C]
+    builds its block lists).
   * prefix_lm allows j < prefix_len or the causal keys.
   * dynamic_topk: per (b, h), keep the first k keys in the order
     (key_bias descending, index ascending), AND causal; the bias is also
@@ -50,7 +53,7 @@ import math
 import numpy as np
 
 # Mask kinds (numbering is the C ABI's; the oracle keeps its own copy).
-NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL = range(7)
+NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL, TABLE = range(8)
 
 
 def default_scale(dqk: int) -> float:
@@ -79,7 +82,7 @@ def topk_keep(bias_row: np.ndarray, k: int) -> np.ndarray:
 
 def allowed(kind: int, sq: int, sk: int, rows: np.ndarray, cols: np.ndarray, *,
             window_left: int = -1, block_size: int = 0, prefix_len: int = 0,
-            keep: np.ndarray | None = None) -> np.ndarray:
+            keep: np.ndarray | None = None, table: np.ndarray | None = None) -> np.ndarray:
     """Element mask m_ij (True = the pair (i, j) takes part), rows x cols.
 
     Mask names follow [FA2C] (`get_mask_pair` names: causal, sliding_window,
@@ -105,6 +108,12 @@ def allowed(kind: int, sq: int, sk: int, rows: np.ndarray, cols: np.ndarray, *,
         m = np.floor_divide(a, block_size) == np.floor_divide(j, block_size)
     elif kind == PREFIX_LM:
         m = (j < prefix_len) | (j <= a)
+    elif kind == TABLE:
+        if table is None:
+            raise ValueError("table mask needs the element table")
+        ii = np.clip(i, 0, sq - 1)
+        jj = np.clip(j, 0, sk - 1)
+        m = np.asarray(table, dtype=bool)[ii, jj]
     elif kind == MINI_CAUSAL:
         if block_size <= 0:
             raise ValueError("block_size must be positive")
@@ -162,7 +171,7 @@ class Problem:
 
     def __init__(self, q, k, v, *, kind=NONE, scale=None, window_left=-1,
                  block_size=0, prefix_len=0, topk=0, rel_bias_slope=0.0,
-                 softcap=0.0, key_bias=None):
+                 softcap=0.0, key_bias=None, table=None):
         self.q = np.asarray(q, dtype=np.float64)
         self.k = np.asarray(k, dtype=np.float64)
         self.v = np.asarray(v, dtype=np.float64)
@@ -177,6 +186,7 @@ class Problem:
         self.rel_bias_slope = float(rel_bias_slope)
         self.softcap = float(softcap)
         self.key_bias = None if key_bias is None else np.asarray(key_bias, dtype=np.float64)
+        self.table = None if table is None else np.asarray(table, dtype=bool)
         self.keep = None
         if kind == DYNAMIC_TOPK:
             if self.key_bias is None:
@@ -186,7 +196,7 @@ class Problem:
     def mask(self, rows, cols):
         return allowed(self.kind, self.sq, self.sk, rows, cols,
                        window_left=self.window_left, block_size=self.block_size,
-                       prefix_len=self.prefix_len, keep=self.keep)
+                       prefix_len=self.prefix_len, keep=self.keep, table=self.table)
 
     def scores(self, rows, cols):
         return _raw_and_scores(self.q[rows], self.k, rows, cols, self.sq, self.sk,
@@ -335,7 +345,7 @@ def _head_problem(q, k, v, b, h, spec):
                    block_size=spec.get("block_size", 0),
                    prefix_len=spec.get("prefix_len", 0), topk=spec.get("topk", 0),
                    rel_bias_slope=spec.get("rel_bias_slope", 0.0),
-                   softcap=spec.get("softcap", 0.0),
+                   softcap=spec.get("softcap", 0.0), table=_head_table(spec, b, h),
                    key_bias=None if kb is None else kb[b, h])
 
 
@@ -356,6 +366,16 @@ def backward(q, k, v, do, spec: dict, heads=None, rows=None, cols=None):
     for (b, h) in heads:
         out[(b, h)] = _head_problem(q, k, v, b, h, spec).backward(do[b, h], rows, cols)
     return out
+
+
+def _head_table(spec: dict, b: int, h: int):
+    """The element table of head (b, h): spec["table"] is [Sq, Sk] (shared)
+    or [B, H, Sq, Sk]."""
+    t = spec.get("table")
+    if t is None:
+        return None
+    t = np.asarray(t, dtype=bool)
+    return t if t.ndim == 2 else t[b, h]
 
 
 def block_lists(B, H, sq, sk, spec: dict, sparse_m: int, sparse_n: int):
@@ -388,7 +408,7 @@ def block_lists(B, H, sq, sk, spec: dict, sparse_m: int, sparse_n: int):
             m = allowed(spec.get("kind", NONE), sq, sk, rows, cols,
                         window_left=spec.get("window_left", -1),
                         block_size=spec.get("block_size", 0),
-                        prefix_len=spec.get("prefix_len", 0), keep=keep)
+                        prefix_len=spec.get("prefix_len", 0), keep=keep, table=_head_table(spec, b, h))
             pad = np.zeros((nqb * sparse_m, nkb * sparse_n), dtype=bool)
             pad[:sq, :sk] = m
             cnt = pad.reshape(nqb, sparse_m, nkb, sparse_n).sum(axis=(1, 3), dtype=np.int64)
@@ -453,5 +473,6 @@ def pair_count(sq, sk, spec: dict, key_bias=None) -> int:
         total += int(allowed(spec.get("kind", NONE), sq, sk, rows, cols,
                              window_left=spec.get("window_left", -1),
                              block_size=spec.get("block_size", 0),
-                             prefix_len=spec.get("prefix_len", 0), keep=keep).sum())
+                             prefix_len=spec.get("prefix_len", 0), keep=keep,
+                             table=_head_table(spec, 0, 0)).sum())
     return total

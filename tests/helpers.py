@@ -15,7 +15,7 @@ from oracle import attention as orc
 
 KIND = {"none": orc.NONE, "causal": orc.CAUSAL, "sliding": orc.SLIDING, "sliding_window": orc.SLIDING,
         "block_diag": orc.BLOCK_DIAG, "block_diagonal": orc.BLOCK_DIAG, "prefix_lm": orc.PREFIX_LM,
-        "dynamic": orc.DYNAMIC_TOPK, "mini_causal": orc.MINI_CAUSAL}
+        "dynamic": orc.DYNAMIC_TOPK, "mini_causal": orc.MINI_CAUSAL, "table": orc.TABLE}
 
 
 def spec_dicts(kind, Sq, Sk, window=None, block_size=256, prefix_len=64, topk=None, slope=0.0, softcap=0.0,
@@ -33,11 +33,32 @@ def spec_dicts(kind, Sq, Sk, window=None, block_size=256, prefix_len=64, topk=No
     return d
 
 
-def to_gpu_spec(d, key_bias_gpu=None):
+def to_gpu_spec(d, key_bias_gpu=None, table_gpu=None):
     return ga.MaskSpec(kind=d["kind"], window_left=d.get("window_left", -1), block_size=d.get("block_size", 0),
                        prefix_len=d.get("prefix_len", 0), topk=d.get("topk", 0),
                        rel_bias_slope=d.get("rel_bias_slope", 0.0), softcap=d.get("softcap", 0.0),
-                       key_bias=key_bias_gpu)
+                       key_bias=key_bias_gpu, table=table_gpu)
+
+
+def make_table(B, H, Sq, Sk, pattern="random", per_head=False, seed=7):
+    """A boolean element table for the TABLE kind (test set-up): "random"
+    (35% of pairs), "dilated" (causal, every other key), or "documents"
+    (causal inside documents of random lengths)."""
+    rng = np.random.default_rng(seed)
+    shape = (B, H, Sq, Sk) if per_head else (Sq, Sk)
+    i = np.arange(Sq)[:, None] + (Sk - Sq)
+    j = np.arange(Sk)[None, :]
+    if pattern == "random":
+        return rng.random(shape) < 0.35
+    if pattern == "dilated":
+        t = (j <= i) & ((i - j) % 2 == 0)
+    elif pattern == "documents":
+        cuts = np.sort(rng.choice(np.arange(1, Sk), size=min(6, Sk - 1), replace=False))
+        doc = np.searchsorted(cuts, np.arange(Sk), side="right")
+        t = (j <= i) & (doc[np.clip(i, 0, Sk - 1)] == doc[j[0]][None, :])
+    else:
+        raise ValueError(pattern)
+    return np.broadcast_to(t, shape).copy()
 
 
 def f64(t):
@@ -48,7 +69,7 @@ class Case:
     """Inputs on host and device, the GPU spec and lists, and the oracle spec."""
 
     def __init__(self, B, H, Sq, Sk, Dqk, Dv, kind="none", dtype="bf16", seed=42, sparse=(256, 512),
-                 use_bias=False, lists=True, gather=True, Hkv=None, **kw):
+                 use_bias=False, lists=True, gather=True, Hkv=None, table=None, **kw):
         need_bias = use_bias or KIND[kind] == orc.DYNAMIC_TOPK
         self.shape = (B, H, Sq, Sk, Dqk, Dv)
         self.Hkv = H if Hkv is None else Hkv
@@ -56,13 +77,20 @@ class Case:
         self.x = make_inputs(B, H, Sq, Sk, Dqk, Dv, dtype, seed=seed, bias=need_bias, Hkv=self.Hkv)
         self.dev = {n: t.cuda() for n, t in self.x.items()}
         self.d = spec_dicts(kind, Sq, Sk, **kw)
-        self.spec = to_gpu_spec(self.d, self.dev.get("key_bias"))
+        self.table = table
+        tab_gpu = None
+        if table is not None:
+            tab_gpu = ga.pack_mask_table(torch.from_numpy(np.ascontiguousarray(table)).cuda())
+            self.dev["table"] = tab_gpu
+        self.spec = to_gpu_spec(self.d, self.dev.get("key_bias"), tab_gpu)
         self.lists = None
         if lists and (self.d["kind"] != orc.NONE or sparse is not None):
             sm, sn = sparse
             self.lists = ga.alloc_block_lists(B, H, Sq, Sk, sm, sn, gather=gather)
             ga.build_block_mask(B, H, Sq, Sk, self.spec, self.lists)
         od = dict(self.d)
+        if table is not None:
+            od["table"] = table
         if need_bias:
             od["key_bias"] = self.x["key_bias"].double().numpy()
         self.od = od
@@ -88,7 +116,9 @@ class Case:
                            window_left=self.od.get("window_left", -1), block_size=self.od.get("block_size", 0),
                            prefix_len=self.od.get("prefix_len", 0), topk=self.od.get("topk", 0),
                            rel_bias_slope=self.od.get("rel_bias_slope", 0.0), softcap=self.od.get("softcap", 0.0),
-                           key_bias=None if kb is None else kb[b, h])
+                           key_bias=None if kb is None else kb[b, h],
+                           table=None if self.table is None else (self.table if self.table.ndim == 2
+                                                                  else self.table[b, h]))
 
 
 def check_out(og, o_ref, fp32=False):

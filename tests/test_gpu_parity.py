@@ -7,7 +7,7 @@ import torch
 
 import block_sparse_attention_tma_gb300 as ga
 from conftest import read_golden
-from helpers import Case, check_dbias, check_grad, check_lse, check_out, f64, assert_no_device_error
+from helpers import Case, check_dbias, check_grad, check_lse, check_out, f64, assert_no_device_error, make_table
 from oracle import attention as orc
 
 pytestmark = pytest.mark.gpu
@@ -338,6 +338,55 @@ def test_paged_decode_bad_page_index_raises_device_error():
     ga.attn_fwd_splitkv_paged(q, kc, kc, table, seqlens, 0.0, None, 1)
     torch.cuda.synchronize()
     assert ga.load_library().gbattn_last_device_error(None) == ga.binding.ERR_BLOCKS
+
+
+# ------------------------------------------------------------------ element-table masks (arbitrary predicates)
+@pytest.mark.parametrize("pattern,per_head,Sq,Sk,sm,sn", [("random", False, 700, 900, 128, 128),
+                                                          ("documents", True, 1000, 1000, 256, 512),
+                                                          ("dilated", False, 513, 769, 128, 256)])
+def test_table_block_lists_bit_exact(pattern, per_head, Sq, Sk, sm, sn):
+    t = make_table(1, 2, Sq, Sk, pattern, per_head)
+    c = Case(1, 2, Sq, Sk, 64, 64, "table", table=t, sparse=(sm, sn))
+    torch.cuda.synchronize()
+    lists_equal(c, 1, 2, Sq, Sk, sm, sn)
+    assert_no_device_error()
+
+
+TABLE_CASES = [
+    # B, H, Hkv, Sq, Sk, Dqk, Dv, pattern, per_head, sparse, extras, dtype
+    (1, 2, 2, 700, 900, 64, 64, "random", False, (128, 128), {}, "bf16"),
+    (1, 2, 2, 1000, 1000, 128, 128, "documents", True, (256, 512), dict(slope=0.01), "bf16"),
+    (1, 2, 2, 513, 769, 192, 128, "dilated", False, (128, 256), dict(softcap=2.0, use_bias=True), "bf16"),
+    (1, 4, 2, 640, 640, 64, 64, "random", True, (128, 128), {}, "bf16"),       # GQA with per-head tables
+    (1, 2, 2, 150, 170, 32, 16, "documents", True, (128, 128), {}, "fp32"),
+]
+
+
+@pytest.mark.parametrize("case", TABLE_CASES, ids=lambda c: f"{c[7]}-{'head' if c[8] else 'shared'}-d{c[5]}-{c[11]}")
+def test_table_forward_backward(case):
+    B, H, Hkv, Sq, Sk, Dqk, Dv, pattern, per_head, sparse, ex, dt = case
+    t = make_table(B, H, Sq, Sk, pattern, per_head)
+    c = Case(B, H, Sq, Sk, Dqk, Dv, "table", dtype=dt, Hkv=Hkv, table=t, sparse=sparse, **ex)
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    fp32 = dt == "fp32"
+    G = H // Hkv
+    for b in range(B):
+        for hk in range(Hkv):
+            dk_r, dv_r = 0.0, 0.0
+            for h in range(hk * G, (hk + 1) * G):
+                p = c.problem(b, h)
+                o_ref, l_ref = p.forward()
+                check_out(f64(o[b, h]), o_ref, fp32=fp32)
+                check_lse(f64(lse[b, h]), l_ref, fp32=fp32)
+                dq_r, dkh, dvh, _ = p.backward(c.h["do"][b, h])
+                check_grad(f64(dq[b, h]), dq_r, "dQ", fp32=fp32)
+                dk_r = dk_r + dkh
+                dv_r = dv_r + dvh
+            check_grad(f64(dk[b, hk]), dk_r, "dK", fp32=fp32)
+            check_grad(f64(dv[b, hk]), dv_r, "dV", fp32=fp32)
 
 
 # ------------------------------------------------------------------ fp32 path

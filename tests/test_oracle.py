@@ -22,6 +22,8 @@ KINDS = {
     "prefix_lm": dict(kind=A.PREFIX_LM, prefix_len=6),
     "dynamic": dict(kind=A.DYNAMIC_TOPK, topk=9),
     "mini_causal": dict(kind=A.MINI_CAUSAL, block_size=4),
+    # an arbitrary predicate: the allowed pairs of a fixed random table
+    "table": dict(kind=A.TABLE, table=np.random.default_rng(99).random((64, 64)) < 0.6),
 }
 
 
@@ -32,6 +34,8 @@ def _rand(rng, *shape):
 def _problem(rng, sq, sk, dqk, dv, spec, bias=False, slope=0.0, softcap=0.0):
     q, k, v = _rand(rng, sq, dqk), _rand(rng, sk, dqk), _rand(rng, sk, dv)
     kb = _rand(rng, sk) if (bias or spec["kind"] == A.DYNAMIC_TOPK) else None
+    if spec["kind"] == A.TABLE:  # the table's top-left Sq x Sk corner
+        spec = dict(spec, table=spec["table"][:sq, :sk])
     return A.Problem(q, k, v, key_bias=kb, rel_bias_slope=slope, softcap=softcap, **spec)
 
 
@@ -304,6 +308,34 @@ def test_mini_causal_reading():
     assert np.array_equal(A.allowed(A.MINI_CAUSAL, 40, 40, rows, cols, block_size=64),
                           A.allowed(A.CAUSAL, 40, 40, rows, cols))
     assert np.array_equal(A.allowed(A.MINI_CAUSAL, 40, 40, rows, cols, block_size=1), np.eye(40, dtype=bool))
+
+
+def test_table_mask_reproduces_the_closed_form_kinds():
+    # a table holding another kind's element mask gives that kind's result
+    # exactly (same mask matrix, same arithmetic), lists included
+    rng = np.random.default_rng(23)
+    sq, sk = 37, 45
+    q, k, v, do = _rand(rng, sq, 8), _rand(rng, sk, 8), _rand(rng, sk, 4), _rand(rng, sq, 4)
+    rows, cols = np.arange(sq), np.arange(sk)
+    for spec in (dict(kind=A.CAUSAL), dict(kind=A.SLIDING, window_left=6), dict(kind=A.MINI_CAUSAL, block_size=8)):
+        tab = A.allowed(spec["kind"], sq, sk, rows, cols, window_left=spec.get("window_left", -1),
+                        block_size=spec.get("block_size", 0))
+        p1 = A.Problem(q, k, v, **spec)
+        p2 = A.Problem(q, k, v, kind=A.TABLE, table=tab)
+        o1, l1 = p1.forward()
+        o2, l2 = p2.forward()
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+        g1, g2 = p1.backward(do), p2.backward(do)
+        for a, b in zip(g1, g2):
+            assert np.array_equal(a, b)
+        L1 = A.block_lists(1, 1, sq, sk, spec, 128, 128)
+        L2 = A.block_lists(1, 1, sq, sk, dict(kind=A.TABLE, table=tab), 128, 128)
+        for n in L1:
+            assert np.array_equal(L1[n], L2[n])
+    # per-head tables pick the head's own matrix
+    t = rng.random((1, 2, sq, sk)) < 0.5
+    L = A.block_lists(1, 2, sq, sk, dict(kind=A.TABLE, table=t), 128, 128)
+    assert L["q_mask_cnt"].shape == (1, 2, 1)
 
 
 def test_topk_matches_brute_force_ranks_with_ties():

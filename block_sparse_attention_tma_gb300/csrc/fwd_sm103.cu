@@ -72,8 +72,8 @@ struct FwdCfg {
   static constexpr int T_O = 256, T_Q = 384;
   static_assert(T_Q + DQK / 2 <= 512 && T_O + DV <= T_Q, "TMEM budget");
   // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
-  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2], fin
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 2 + 1;
+  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2][4 lane quarters], fin
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 8 + 1;
   static constexpr int THREADS = 320;
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
@@ -121,8 +121,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 1;
-  uint64_t* xbar = drain + 1;  // [2]
-  uint64_t* fin = xbar + 2;
+  uint64_t* xbar = drain + 1;  // [2][4]: the two warps of a lane quarter exchange row maxima
+  uint64_t* fin = xbar + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     mbar_init(q_tmem, 128);
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 256); mbar_init(xbar + i, 256); }
+    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 256); }
+    for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 64);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(fin, 256);
@@ -445,8 +446,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float* xm = xmax + sb * 256;
       xm[grp * 128 + row] = mt;
-      mbar_arrive(xbar + sb);
-      ok = mbar_wait(xbar + sb, (n >> 1) & 1, abort_flag);
+      mbar_arrive(xbar + sb * 4 + quarter);
+      ok = mbar_wait(xbar + sb * 4 + quarter, (n >> 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;

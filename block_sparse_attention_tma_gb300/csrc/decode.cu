@@ -254,6 +254,254 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
   }
 }
 
+// Grouped decode (GQA, pack-GQA): CTA = (b, key/value head, split, chunk of
+// RC = 4 RPG query rows of the group). The G query heads of a key/value head
+// (G x Sq rows, contiguous in Q, O and LSE) share every key/value row, so the
+// CTA streams each 64-key chunk once and all its rows use it: the four lane
+// groups of a warp take different rows of the same key, their shared-memory
+// reads of K and V are broadcasts, and each lane keeps 1/8 of the head dim of
+// its rows (scores reduced over the 8 lanes of a group). Each warp keeps its
+// own online softmax over its 8 keys of every chunk; the warps are merged at
+// the end and the splits by combine_kernel, as in splitkv_kernel. Nine warps
+// put three on one SM sub-partition, so a thread has at most 168 registers:
+// 16 rows per CTA fit at D = 64, 8 rows at D = 128.
+template <int D, int RPG>
+__global__ void __launch_bounds__(kDecThreads, 1) splitkv_group_kernel(const DecParams p, int nrch) {
+  constexpr int ROWB = D * 2;
+  constexpr int CHB = kDecChunk * ROWB;
+  constexpr int RC = 4 * RPG;     // query rows of this CTA
+  constexpr int SL = D / 8;       // head-dim elements of a lane: D/64 slabs of 8
+  constexpr int NS = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* sK = base;
+  uint8_t* sV = sK + kDecStages * CHB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sV + kDecStages * CHB);
+  uint64_t* empty = full + kDecStages;
+  float* red = reinterpret_cast<float*>(empty + kDecStages);  // [kDecWarps][RC][D + 2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kDecWarps * RC * (D + 2));
+
+  const int split = blockIdx.x % p.nsplit;
+  const int rest = blockIdx.x / p.nsplit;
+  const int rch = rest % nrch;
+  const int bkv = rest / nrch;
+  const int b = bkv / p.Hkv, hkv = bkv % p.Hkv;
+  const int R = p.G * p.Sq;                                 // query rows of the group
+  const int row0 = (b * p.H + hkv * p.G) * p.Sq;            // first row id of the group
+  const int rc0 = rch * RC;                                 // first group row of this CTA
+  int skb = p.Sk;
+  if (p.seqlens) {
+    skb = __ldg(p.seqlens + b);
+    const int cap = p.page_table ? p.max_pages * p.page_size : p.Sk;
+    if (skb < 0 || skb > cap) {
+      if (threadIdx.x == 0) raise_dev_error(GBATTN_ERR_BLOCKS);
+      skb = max(0, min(skb, cap));
+    }
+  }
+  const int per = ((skb + p.nsplit - 1) / p.nsplit + 127) / 128 * 128;
+  const int kb = split * per;
+  const int ke = min(kb + per, skb);
+  const int nkeys = max(0, ke - kb);
+  const int nchunks = (nkeys + kDecChunk - 1) / kDecChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kDecWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kDecStages;
+        if (c >= kDecStages && !mbar_wait(empty + s, ((c / kDecStages) + 1) & 1, abort_flag)) break;
+        const int rows = min(kDecChunk, nkeys - c * kDecChunk);
+        const uint32_t bytes = (uint32_t)rows * ROWB;
+        const size_t off = kv_row<D>(p, b, hkv, kb + c * kDecChunk);
+        mbar_expect_tx(full + s, 2 * bytes);
+        bulk_load(sK + s * CHB, p.k + off, bytes, full + s);
+        bulk_load(sV + s * CHB, p.v + off, bytes, full + s);
+        ++issued;
+      }
+      if (*abort_flag)
+        for (int c = (issued > kDecStages ? issued - kDecStages : 0); c < issued; ++c)
+          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int g = lane >> 3, sub = lane & 7;  // group: rows g*RPG.., sub: head-dim slice
+    float qv[RPG][SL];
+    int lim[RPG];  // last allowed key index of each row (-1: padding row)
+#pragma unroll
+    for (int t = 0; t < RPG; ++t) {
+      const int r = rc0 + g * RPG + t;
+      lim[t] = -1;
+#pragma unroll
+      for (int e = 0; e < SL; ++e) qv[t][e] = 0.f;
+      if (r < R) {
+        const int i = r % p.Sq;
+        lim[t] = p.causal ? i + (skb - p.Sq) : skb - 1;
+        const __nv_bfloat16* qrow = p.q + (size_t)(row0 + r) * D;
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(qrow + h * 64 + sub * 8);
+          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(b2[e]);
+            qv[t][h * 8 + 2 * e] = f.x * p.scale_log2;
+            qv[t][h * 8 + 2 * e + 1] = f.y * p.scale_log2;
+          }
+        }
+      }
+    }
+    float m[RPG], l[RPG], acc[RPG][SL];
+#pragma unroll
+    for (int t = 0; t < RPG; ++t) {
+      m[t] = -INFINITY;
+      l[t] = 0.f;
+#pragma unroll
+      for (int e = 0; e < SL; ++e) acc[t][e] = 0.f;
+    }
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kDecStages;
+      ok = mbar_wait(full + s, (c / kDecStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const int rows = min(kDecChunk, nkeys - c * kDecChunk);
+      const uint8_t* kc = sK + s * CHB;
+      const uint8_t* vc = sV + s * CHB;
+      const int key0 = kb + c * kDecChunk + warp * 8;  // index of this warp's first key
+      float sc[RPG][8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int key = warp * 8 + k;
+        float kf[SL];
+        if (key < rows) {
+#pragma unroll
+          for (int h = 0; h < NS; ++h) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(kc + key * ROWB + h * 128 + sub * 16);
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(b2[e]);
+              kf[h * 8 + 2 * e] = f.x;
+              kf[h * 8 + 2 * e + 1] = f.y;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < SL; ++e) kf[e] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < RPG; ++t) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < SL; ++e) dot = fmaf(kf[e], qv[t][e], dot);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+          dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+          sc[t][k] = (key < rows && key0 + k <= lim[t]) ? dot : -INFINITY;
+        }
+      }
+      // probabilities in place of the scores
+#pragma unroll
+      for (int t = 0; t < RPG; ++t) {
+        float mc = sc[t][0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mc = fmaxf(mc, sc[t][k]);
+        const float mn = fmaxf(m[t], mc);
+        const float msafe = (mn == -INFINITY) ? 0.f : mn;
+        const float alpha = ex2(m[t] - msafe);  // m = -inf -> 0
+        float ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          sc[t][k] = ex2(sc[t][k] - msafe);
+          ls += sc[t][k];
+        }
+        l[t] = l[t] * alpha + ls;
+        m[t] = mn;
+#pragma unroll
+        for (int e = 0; e < SL; ++e) acc[t][e] *= alpha;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int key = warp * 8 + k;
+        if (key >= rows) continue;  // stale shared memory beyond the chunk end
+        float vf[SL];
+#pragma unroll
+        for (int h = 0; h < NS; ++h) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(vc + key * ROWB + h * 128 + sub * 16);
+          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(b2[e]);
+            vf[h * 8 + 2 * e] = f.x;
+            vf[h * 8 + 2 * e + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < RPG; ++t)
+#pragma unroll
+          for (int e = 0; e < SL; ++e) acc[t][e] = fmaf(sc[t][k], vf[e], acc[t][e]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
+    }
+    // publish this warp's (m, l, acc) of each row for the merge
+#pragma unroll
+    for (int t = 0; t < RPG; ++t) {
+      float* rw = red + (warp * RC + g * RPG + t) * (D + 2);
+#pragma unroll
+      for (int h = 0; h < NS; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rw[h * 64 + sub * 8 + e] = acc[t][h * 8 + e];
+      if (sub == 0) {
+        rw[D] = m[t];
+        rw[D + 1] = l[t];
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) return;
+  // merge the warps: one output element per thread and step
+  for (int idx = threadIdx.x; idx < RC * D; idx += blockDim.x) {
+    const int rr = idx / D, d = idx % D;
+    const int r = rc0 + rr;
+    if (r >= R) continue;
+    float mx = -INFINITY;
+    for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, red[(w * RC + rr) * (D + 2) + D]);
+    float lt = 0.f, ot = 0.f;
+    if (mx != -INFINITY) {
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float* rw = red + (w * RC + rr) * (D + 2);
+        const float wgt = ex2(rw[D] - mx);
+        lt += wgt * rw[D + 1];
+        ot += wgt * rw[d];
+      }
+    }
+    const bool live = lt > 0.f;
+    const float val = live ? ot / lt : 0.f;
+    const float lse_nat = live ? (mx + __log2f(lt)) * kLn2 : -INFINITY;
+    const int rowid = row0 + r;
+    if (p.nsplit == 1) {
+      p.o[(size_t)rowid * D + d] = __float2bfloat16_rn(val);
+      if (d == 0 && p.lse) p.lse[rowid] = lse_nat;
+    } else {
+      const size_t prow = (size_t)split * p.BH * p.Sq + rowid;
+      p.o_part[prow * D + d] = val;
+      if (d == 0) p.lse_part[prow] = lse_nat;
+    }
+  }
+}
+
 // One warp per (b, h, query row): merge the split partials.
 template <int D>
 __global__ void combine_kernel(const DecParams p) {
@@ -284,6 +532,26 @@ __global__ void combine_kernel(const DecParams p) {
   if (lane == 0 && p.lse) p.lse[row] = live ? mx + __logf(tot) : -INFINITY;
 }
 
+template <int D, int RPG>
+static int launch_group(const DecParams& prm, cudaStream_t st) {
+  constexpr int CHB = kDecChunk * D * 2;
+  constexpr int RC = 4 * RPG;
+  constexpr int SMEM = 128 + 2 * kDecStages * CHB + 2 * kDecStages * 8 + kDecWarps * RC * (D + 2) * 4 + 16;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(splitkv_group_kernel<D, RPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
+        cudaSuccess)
+      return GBATTN_ERR_CUDA;
+    attr = true;
+  }
+  const int R = prm.G * prm.Sq;
+  const int nrch = (R + RC - 1) / RC;
+  const long long grid = (long long)(prm.BH / prm.G) * nrch * prm.nsplit;
+  if (grid >= (1ll << 31)) return GBATTN_ERR_ARG;
+  splitkv_group_kernel<D, RPG><<<(unsigned)grid, kDecThreads, SMEM, st>>>(prm, nrch);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
 template <int D>
 static int launch_dec(const DecParams& prm, cudaStream_t st) {
   constexpr int CHB = kDecChunk * D * 2;
@@ -294,10 +562,19 @@ static int launch_dec(const DecParams& prm, cudaStream_t st) {
       return GBATTN_ERR_CUDA;
     attr = true;
   }
-  const long long grid = (long long)prm.BH * prm.Sq * prm.nsplit;
-  if (grid >= (1ll << 31)) return GBATTN_ERR_ARG;
-  splitkv_kernel<D><<<(unsigned)grid, kDecThreads, SMEM, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  const int R = prm.G * prm.Sq;  // query rows per key/value head
+  if (prm.G > 1 && R >= 4) {
+    // query heads share key/value heads: one CTA streams each chunk for up to 8 (D=128) or 16 (D=64) rows
+    constexpr int RPG_MAX = D <= 64 ? 4 : 2;
+    const int rc = R <= 4 ? launch_group<D, 1>(prm, st) : (R <= 8 || RPG_MAX == 2) ? launch_group<D, 2>(prm, st)
+                                                                                   : launch_group<D, RPG_MAX>(prm, st);
+    if (rc != GBATTN_OK) return rc;
+  } else {
+    const long long grid = (long long)prm.BH * prm.Sq * prm.nsplit;
+    if (grid >= (1ll << 31)) return GBATTN_ERR_ARG;
+    splitkv_kernel<D><<<(unsigned)grid, kDecThreads, SMEM, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  }
   if (prm.nsplit > 1) {
     const long long rows = (long long)prm.BH * prm.Sq;
     combine_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(prm);

@@ -222,9 +222,10 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Sq, int Dv, int num_sp
  * its K/V range once with 16-byte vector loads and writes a partial output and
  * LSE; a combine kernel merges them with the LSE-weighted rule of [PCB]
  * (num_splits == 1 writes O directly). bf16 only; mask kind NONE or CAUSAL,
- * no softcap or biases. 1 <= num_splits <= 64. With GQA the CTAs of the
- * H / Hkv query heads of a group read the same key/value rows (L2 serves the
- * repeats).
+ * no softcap or biases. 1 <= num_splits <= 64. With GQA (H / Hkv query
+ * heads per key/value head) and at least 4 query rows per group, one CTA
+ * streams each key/value row once for up to 8 (D = 128) or 16 (D = 64) query
+ * rows of the group ([FA2C]'s pack_gqa).
  */
 int attn_fwd_splitkv(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
                      const void* q, const void* k, const void* v, float scale,

@@ -267,14 +267,18 @@ def test_gqa_forward_backward(case):
 
 
 @pytest.mark.parametrize("n", [1, 4])
-@pytest.mark.parametrize("Hkv", [1, 2])
-def test_gqa_splitkv_decode(n, Hkv):
-    c = Case(2, 4, 2, 1500, 128, 128, "causal", Hkv=Hkv, lists=False, sparse=None)
+@pytest.mark.parametrize("H,Hkv,Sq,D,kind", [(4, 2, 2, 128, "causal"),    # 4 rows per group: 1 row per lane group
+                                             (4, 1, 2, 128, "causal"),    # 8 rows
+                                             (16, 2, 3, 128, "causal"),   # 24 rows: two CTAs of 16 rows
+                                             (8, 1, 1, 64, "none"),       # MQA-style, D=64
+                                             (6, 3, 1, 128, "none")])     # 2 rows: one CTA per row
+def test_gqa_splitkv_decode(n, H, Hkv, Sq, D, kind):
+    c = Case(2, H, Sq, 1500, D, D, kind, Hkv=Hkv, lists=False, sparse=None)
     o, lse = ga.attn_fwd_splitkv(c.dev["q"], c.dev["k"], c.dev["v"], 0.0, c.spec, n)
     torch.cuda.synchronize()
     assert_no_device_error()
     for b in range(2):
-        for h in range(4):
+        for h in range(H):
             o_ref, l_ref = c.problem(b, h).forward()
             check_out(f64(o[b, h]), o_ref)
             check_lse(f64(lse[b, h]), l_ref)
@@ -304,10 +308,11 @@ def _paged_cache(k, v, page_size, seqlens, extra_pages, seed):
     return kc, vc, torch.from_numpy(table)
 
 
-@pytest.mark.parametrize("page_size,n,kind,Hkv", [(64, 1, "none", 2), (128, 4, "causal", 1), (256, 16, "none", 4),
-                                                   (192, 2, "causal", 2)])
-def test_paged_splitkv_decode(page_size, n, kind, Hkv):
-    B, H, Sq, S, D = 4, 4, 2, 1100, 128
+@pytest.mark.parametrize("page_size,n,kind,Hkv,H", [(64, 1, "none", 2, 4), (128, 4, "causal", 1, 4),
+                                                     (256, 16, "none", 4, 4), (192, 2, "causal", 2, 4),
+                                                     (128, 2, "causal", 1, 16)])
+def test_paged_splitkv_decode(page_size, n, kind, Hkv, H):
+    B, Sq, S, D = 4, 2, 1100, 128
     c = Case(B, H, Sq, S, D, D, kind, Hkv=Hkv, lists=False, sparse=None)
     seqlens = np.array([1100, 0, 1, 777])
     kc, vc, table = _paged_cache(c.x["k"], c.x["v"], page_size, seqlens, extra_pages=3, seed=page_size)

@@ -38,6 +38,9 @@ bool dims_ok(int B, int H, int Sq, int Sk) {
 // Grouped-query attention: H query heads share Hkv key/value heads.
 bool heads_ok(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
 
+// The tensor-core kernels keep 128-row / 128-key tile indices in 15 bits.
+bool bf16_seq_ok(int Sq, int Sk) { return (Sq + 127) / 128 < 32768 && (Sk + 127) / 128 < 32768; }
+
 bool bf16_dims_ok(int Dqk, int Dv) {
   return (Dqk == 32 && Dv == 32) || (Dqk == 64 && Dv == 64) || (Dqk == 128 && Dv == 128) ||
          (Dqk == 192 && Dv == 128);
@@ -262,7 +265,7 @@ int attn_fwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
     return GBATTN_ERR_ALIGN;
   if (dtype == GBATTN_BF16) {
-    if (!bf16_dims_ok(Dqk, Dv)) return GBATTN_ERR_UNSUPPORTED;
+    if (!bf16_dims_ok(Dqk, Dv) || !bf16_seq_ok(Sq, Sk)) return GBATTN_ERR_UNSUPPORTED;
   } else if (dtype == GBATTN_FP32) {
     if (!fp32_dims_ok(Dqk, Dv)) return GBATTN_ERR_UNSUPPORTED;
   } else {
@@ -301,7 +304,7 @@ int attn_bwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv, 
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (dkey_bias && !aligned4(dkey_bias)))
     return GBATTN_ERR_ALIGN;
   if (dtype == GBATTN_BF16) {
-    if (!bf16_dims_ok(Dqk, Dv)) return GBATTN_ERR_UNSUPPORTED;
+    if (!bf16_dims_ok(Dqk, Dv) || !bf16_seq_ok(Sq, Sk)) return GBATTN_ERR_UNSUPPORTED;
   } else if (dtype == GBATTN_FP32) {
     if (!fp32_dims_ok(Dqk, Dv)) return GBATTN_ERR_UNSUPPORTED;
   } else {

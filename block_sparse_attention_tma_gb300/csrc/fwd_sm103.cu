@@ -31,6 +31,11 @@
 // producer lane gathers 4 of the 128 rows); the bias and rel-bias terms use
 // each key's original index and the element mask is the prefix of compact
 // keys each row sees. No key outside the keep set is loaded or multiplied.
+// Packed decode (grouped-query attention, split-KV): the G x Sq query rows of
+// a key/value head (contiguous in Q and O) form the 128-row tiles, so one CTA
+// streams each key/value tile once for the whole group and the tensor cores
+// take the score and output products; a CTA covers one split of the keys and
+// writes a normalised partial output and LSE that the split combine merges.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv), Q [384, 384+Dqk/2).
 #include "kernels.h"
 #include "mask.cuh"
@@ -55,6 +60,9 @@ struct FwdParams {
   const int32_t *mcnt, *midx, *fcnt, *fidx;  // forward lists
   __nv_bfloat16* o;
   float* lse;
+  // packed decode: rows per group, row tiles per group, splits, keys per split
+  int pk_R, pk_nrt, pk_nsplit, pk_per;
+  float *o_part, *lse_part;  // [nsplit][B*H*Sq][Dv], [nsplit][B*H*Sq] (nsplit > 1)
 };
 
 template <int DQK, int DV>
@@ -98,7 +106,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
   reg_fence32(r + 96);
 }
 
-template <int DQK, int DV, bool CAP, bool GAT>
+template <int DQK, int DV, bool CAP, bool GAT, bool PK = false>
 __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -132,10 +140,34 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   const int lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int L = blockIdx.x;
-  const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
-  const int bh = L % BH;
-  const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
-  const int q0 = qt * 128;
+  int bh, bkv, q0;
+  // packed decode: this CTA's keys [kbeg, kend), its rows' query positions
+  // [pa, pb], its split and the row id of its group's first row
+  int kbeg = 0, kend = p.Sk, pa = 0, pb = 0, split = 0, row_base = 0;
+  if constexpr (PK) {
+    split = L % p.pk_nsplit;
+    const int rest = L / p.pk_nsplit;
+    const int rt = rest % p.pk_nrt;
+    bkv = rest / p.pk_nrt;
+    bh = (bkv / p.Hkv) * p.H + (bkv % p.Hkv) * p.G;  // first query head of the group
+    row_base = bh * p.Sq;
+    q0 = rt * 128;  // first group row of this CTA
+    kbeg = split * p.pk_per;
+    kend = min(kbeg + p.pk_per, p.Sk);
+    const int r1 = min(q0 + 127, p.pk_R - 1);
+    if (q0 / p.Sq == r1 / p.Sq) {
+      pa = q0 % p.Sq;
+      pb = r1 % p.Sq;
+    } else {
+      pa = 0;
+      pb = p.Sq - 1;
+    }
+  } else {
+    const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
+    bh = L % BH;
+    bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
+    q0 = qt * 128;
+  }
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
   const int Skv = p.Skv;
   const int delta = p.Sk - p.Sq;
@@ -146,7 +178,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   TileWalk walk;
   int nslots;
   int c_first = 0, c_last = 0;
-  if (gat) {
+  if (PK) {
+    nslots = kend > kbeg ? (kend + 127) / 128 - kbeg / 128 : 0;
+  } else if (gat) {
     nslots = (Skv + 127) / 128;
   } else if (p.has_lists) {
     const int r = q0 / p.sparse_m;
@@ -156,6 +190,18 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     nslots = (p.Sk + 127) / 128;
   }
   auto slot = [&](int s, int* kv0, bool* masked) -> bool {
+    if constexpr (PK) {
+      // rows at query positions [pa, pb] (monotone intervals: the first and
+      // last position bound every row's interval)
+      const int st = kbeg + s * 128, k1 = min(st + 128, p.Sk);
+      int lo_a, hi_a, lo_b, hi_b;
+      row_interval(p.mask, pa, p.Sq, p.Sk, lo_a, hi_a);
+      row_interval(p.mask, pb, p.Sq, p.Sk, lo_b, hi_b);
+      if (hi_b < st || lo_a > k1 - 1) return false;
+      *kv0 = st;
+      *masked = !(k1 - st == 128 && lo_b <= st && hi_a >= k1 - 1);
+      return true;
+    }
     if (gat) return gathered_slot_rows(s, c_first, c_last, kv0, masked);
     return p.has_lists ? walk_slot(walk, s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked)
                        : dense_slot(s, p.mask, true, q0, p.Sq, p.Sk, kv0, masked);
@@ -204,7 +250,12 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         mbar_expect_tx(q_full, C::QTILE);
-        for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+        for (int j = 0; j < C::NQSLAB; ++j) {
+          if constexpr (PK)  // packed rows: one row range over all heads
+            tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), row_base + q0, 0);
+          else
+            tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
+        }
         int n = 0, nk = 0, nv = 0;
         bool ok = true;
         auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -333,7 +384,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     const int grp = sw >> 2;       // which half of the key columns
     const int quarter = warp & 3;  // TMEM lane quarter
     const int row = quarter * 32 + lane;
-    const int i = q0 + row;
+    // query position of this row (the row itself, or its position within its
+    // head when rows are packed), whether it exists, and its output row id
+    const int i = PK ? (q0 + row) % p.Sq : q0 + row;
+    const bool valid = PK ? q0 + row < p.pk_R : i < p.Sq;
+    const size_t orow_id = PK ? (size_t)row_base + q0 + row : (size_t)bh * p.Sq + i;
     const int cb = grp * 64;       // first S column of this thread
     constexpr int DVH = DV / 2;    // O columns of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -521,11 +576,21 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       }
       if (ok) {
         const bool live = n > 0 && l_tot > 0.f;
-        __nv_bfloat16* orow = p.o + ((size_t)bh * p.Sq + i) * DV + grp * DVH;
-        if (!live && i < p.Sq) {
+        __nv_bfloat16* orow = p.o + orow_id * DV + grp * DVH;
+        // split partials (packed decode with several splits): fp32 O / l and LSE
+        const bool part = PK && p.pk_nsplit > 1;
+        const size_t prow = (size_t)split * BH * p.Sq + orow_id;
+        float* oprow = part ? p.o_part + prow * DV + grp * DVH : nullptr;
+        if (!live && valid) {
+          if (part) {
 #pragma unroll
-          for (int c = 0; c < DVH; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          if (grp == 0 && p.lse) p.lse[(size_t)bh * p.Sq + i] = -INFINITY;
+            for (int c = 0; c < DVH; c += 4) *reinterpret_cast<float4*>(oprow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (grp == 0) p.lse_part[prow] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int c = 0; c < DVH; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+            if (grp == 0 && p.lse) p.lse[orow_id] = -INFINITY;
+          }
         }
         if (n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
           tc_fence_after();
@@ -541,7 +606,13 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
               tmem_ld16(tl + C::T_O + grp * DVH + c0, orr);
               tmem_wait_ld16(orr);
             }
-            if (i < p.Sq && live) {
+            if (valid && live && part) {
+#pragma unroll
+              for (int c = 0; c < CH; c += 4)
+                *reinterpret_cast<float4*>(oprow + c0 + c) =
+                    make_float4(__uint_as_float(orr[c]) * inv, __uint_as_float(orr[c + 1]) * inv,
+                                __uint_as_float(orr[c + 2]) * inv, __uint_as_float(orr[c + 3]) * inv);
+            } else if (valid && live) {
               uint32_t pkd[CH / 2];
 #pragma unroll
               for (int c = 0; c < CH / 2; ++c)
@@ -552,8 +623,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
                     make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
             }
           }
-          if (grp == 0 && i < p.Sq && live && p.lse)
-            p.lse[(size_t)bh * p.Sq + i] = (m_run + __log2f(l_tot)) * kLn2 + p.mask.slope * (float)i;
+          if (grp == 0 && valid && live) {
+            const float L_nat = (m_run + __log2f(l_tot)) * kLn2 + p.mask.slope * (float)i;
+            if (part) p.lse_part[prow] = L_nat;
+            else if (p.lse) p.lse[orow_id] = L_nat;
+          }
         }
       }
     }
@@ -645,6 +719,57 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   if (s.Dqk == 64 && s.Dv == 64) return launch_fwd_cap<64, 64>(prm, grid, cap, st);
   if (s.Dqk == 128 && s.Dv == 128) return launch_fwd_cap<128, 128>(prm, grid, cap, st);
   if (s.Dqk == 192 && s.Dv == 128) return launch_fwd_cap<192, 128>(prm, grid, cap, st);
+  return GBATTN_ERR_UNSUPPORTED;
+}
+
+template <int D>
+static int launch_packed(const FwdParams& prm, int grid, cudaStream_t st) {
+  using C = FwdCfg<D, D>;
+  auto kern = fwd_bf16_kernel<D, D, false, false, true>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return GBATTN_ERR_CUDA;
+    attr_set = true;
+  }
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int fwd_packed_decode_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                             int num_splits, void* o, float* lse, float* o_part, float* lse_part, cudaStream_t st) {
+  FwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int sw = s.Dqk >= 64 ? 128 : 64;
+  const int BHkv = s.B * s.Hkv;
+  // Q as one range of B*H*Sq rows: a group's rows are consecutive
+  if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.B * s.H * s.Sq, 1, sw)) return GBATTN_ERR_CUDA;
+  if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
+  if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
+  prm.B = s.B;
+  prm.H = s.H;
+  prm.Sq = s.Sq;
+  prm.Sk = s.Sk;
+  prm.Hkv = s.Hkv;
+  prm.G = s.H / s.Hkv;
+  prm.Skv = s.Sk;
+  prm.scale_log2 = scale * kLog2e;
+  prm.mask.kind = causal ? GBATTN_MASK_CAUSAL : GBATTN_MASK_NONE;
+  prm.mask.window_left = -1;
+  prm.mask.nkw = (s.Sk + 31) / 32;
+  prm.o = reinterpret_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.pk_R = prm.G * s.Sq;
+  prm.pk_nrt = (prm.pk_R + 127) / 128;
+  prm.pk_nsplit = num_splits;
+  int per = (s.Sk + num_splits - 1) / num_splits;
+  prm.pk_per = (per + 127) / 128 * 128;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  const long long grid = (long long)BHkv * prm.pk_nrt * num_splits;
+  if (grid >= (1ll << 31)) return GBATTN_ERR_ARG;
+  if (s.Dqk == 64 && s.Dv == 64) return launch_packed<64>(prm, (int)grid, st);
+  if (s.Dqk == 128 && s.Dv == 128) return launch_packed<128>(prm, (int)grid, st);
   return GBATTN_ERR_UNSUPPORTED;
 }
 

@@ -36,7 +36,8 @@
  *   - scale <= 0 selects 1/sqrt(Dqk), the pages' default softmax scale.
  *   - Supported head dims: bf16 (Dqk,Dv) in {(32,32),(64,64),(128,128),
  *     (192,128)} on the tensor-core path; fp32 any 1 <= Dqk,Dv <= 128 on the
- *     exact CUDA-core path. Any Sq, Sk >= 1; ragged tile edges are masked.
+ *     exact CUDA-core path. Any Sq, Sk >= 1 (bf16 attn_fwd / attn_bwd: below
+ *     2^22, i.e. fewer than 32768 tiles of 128); ragged tile edges are masked.
  */
 #ifndef GBATTN_H
 #define GBATTN_H

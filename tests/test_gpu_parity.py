@@ -271,7 +271,8 @@ def test_gqa_forward_backward(case):
                                              (4, 1, 2, 128, "causal"),    # 8 rows
                                              (16, 2, 3, 128, "causal"),   # 24 rows: two CTAs of 16 rows
                                              (8, 1, 1, 64, "none"),       # MQA-style, D=64
-                                             (6, 3, 1, 128, "none")])     # 2 rows: one CTA per row
+                                             (6, 3, 1, 128, "none"),      # 2 rows per group
+                                             (64, 1, 3, 128, "causal")])  # 192 rows: two 128-row tiles
 def test_gqa_splitkv_decode(n, H, Hkv, Sq, D, kind):
     c = Case(2, H, Sq, 1500, D, D, kind, Hkv=Hkv, lists=False, sparse=None)
     o, lse = ga.attn_fwd_splitkv(c.dev["q"], c.dev["k"], c.dev["v"], 0.0, c.spec, n)

@@ -613,10 +613,12 @@ int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, 
     prm.o_part = static_cast<float*>(ws);
     prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(rows * s.Dv * sizeof(float), 256));
   }
-  if (prm.G > 1 && !paged) {
-    // grouped query heads, dense cache: the group's rows packed into 128-row
-    // tiles of the tensor-core forward kernel, one CTA per key/value tile range
-    const int rc = fwd_packed_decode_launch(s, q, k, v, scale, causal, num_splits, o, lse, prm.o_part, prm.lse_part, st);
+  if (prm.G > 1 && (!paged || !paged->page_table || paged->page_size % 128 == 0)) {
+    // grouped query heads: the group's rows packed into 128-row tiles of the
+    // tensor-core forward kernel, one CTA per key/value tile range (a paged
+    // pool qualifies when a 128-key tile never crosses a page)
+    const int rc = fwd_packed_decode_launch(s, q, k, v, scale, causal, num_splits, o, lse, prm.o_part, prm.lse_part,
+                                            paged, st);
     if (rc != GBATTN_OK || num_splits == 1) return rc;
     const long long rows = (long long)prm.BH * prm.Sq;
     if (s.Dqk == 128) combine_kernel<128><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(prm);

@@ -61,8 +61,12 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   // packed decode: rows per group, row tiles per group, splits, keys per split
-  int pk_R, pk_nrt, pk_nsplit, pk_per;
+  int pk_R, pk_nrt, pk_nsplit;
   float *o_part, *lse_part;  // [nsplit][B*H*Sq][Dv], [nsplit][B*H*Sq] (nsplit > 1)
+  const int32_t* pk_seqlens;  // [B] keys per sequence, or nullptr (all Sk)
+  const int32_t* pk_pages;    // [B][pk_max_pages] page table, or nullptr (dense cache):
+                              // tm_k / tm_v then map the pool [num_pages * Hkv, page_size, D]
+  int pk_page_size, pk_max_pages, pk_num_pages;
 };
 
 template <int DQK, int DV>
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   // packed decode: this CTA's keys [kbeg, kend), its rows' query positions
   // [pa, pb], its split and the row id of its group's first row
   int kbeg = 0, kend = p.Sk, pa = 0, pb = 0, split = 0, row_base = 0;
+  int skb = p.Sk;  // keys of this sequence (packed decode with per-sequence counts)
   if constexpr (PK) {
     split = L % p.pk_nsplit;
     const int rest = L / p.pk_nsplit;
@@ -152,8 +157,18 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     bh = (bkv / p.Hkv) * p.H + (bkv % p.Hkv) * p.G;  // first query head of the group
     row_base = bh * p.Sq;
     q0 = rt * 128;  // first group row of this CTA
-    kbeg = split * p.pk_per;
-    kend = min(kbeg + p.pk_per, p.Sk);
+    if (p.pk_seqlens) {
+      skb = __ldg(p.pk_seqlens + bkv / p.Hkv);
+      const int cap = p.pk_pages ? p.pk_max_pages * p.pk_page_size : p.Sk;
+      if (skb < 0 || skb > cap) {
+        if (threadIdx.x == 0) raise_dev_error(GBATTN_ERR_BLOCKS);
+        skb = max(0, min(skb, cap));
+      }
+    }
+    // split s covers keys [s L, (s + 1) L), L = ceil(keys / n) rounded up to 128
+    const int per = ((skb + p.pk_nsplit - 1) / p.pk_nsplit + 127) / 128 * 128;
+    kbeg = split * per;
+    kend = min(kbeg + per, skb);
     const int r1 = min(q0 + 127, p.pk_R - 1);
     if (q0 / p.Sq == r1 / p.Sq) {
       pa = q0 % p.Sq;
@@ -169,7 +184,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     q0 = qt * 128;
   }
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
-  const int Skv = p.Skv;
+  const int Skv = PK ? skb : p.Skv;
+  const int SkM = PK ? skb : p.Sk;  // key count the masks align to
   const int delta = p.Sk - p.Sq;
   const uint32_t* keep_h = p.mask.keep ? p.mask.keep + (size_t)bh * p.mask.nkw : nullptr;
   const int32_t* pos_h = gat ? p.kidx + (size_t)bh * p.Sk : nullptr;
@@ -193,10 +209,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     if constexpr (PK) {
       // rows at query positions [pa, pb] (monotone intervals: the first and
       // last position bound every row's interval)
-      const int st = kbeg + s * 128, k1 = min(st + 128, p.Sk);
+      const int st = kbeg + s * 128, k1 = min(st + 128, SkM);
       int lo_a, hi_a, lo_b, hi_b;
-      row_interval(p.mask, pa, p.Sq, p.Sk, lo_a, hi_a);
-      row_interval(p.mask, pb, p.Sq, p.Sk, lo_b, hi_b);
+      row_interval(p.mask, pa, p.Sq, SkM, lo_a, hi_a);
+      row_interval(p.mask, pb, p.Sq, SkM, lo_b, hi_b);
       if (hi_b < st || lo_a > k1 - 1) return false;
       *kv0 = st;
       *masked = !(k1 - st == 128 && lo_b <= st && hi_a >= k1 - 1);
@@ -262,17 +278,31 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         int kv0;
         bool masked;
         while (ok && it.next(&kv0, &masked)) {
+          // (row, head) coordinates of the key/value tile: a dense head, or the
+          // page holding the tile in a paged pool (pages hold multiples of 128 keys)
+          int ky = kv0, kz = bkv;
+          if constexpr (PK) {
+            if (p.pk_pages) {
+              int page = __ldg(p.pk_pages + (size_t)(bkv / p.Hkv) * p.pk_max_pages + kv0 / p.pk_page_size);
+              if (page < 0 || page >= p.pk_num_pages) {
+                raise_dev_error(GBATTN_ERR_BLOCKS);  // read page 0 instead; the output is invalid
+                page = 0;
+              }
+              ky = kv0 % p.pk_page_size;
+              kz = page * p.Hkv + bkv % p.Hkv;
+            }
+          }
           const int ks = n % C::KST;
           if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(k_full + ks, C::QTILE);
           for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), kv0, bkv);
+            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), ky, kz);
           ++nk;
           const int vs = n % C::VST;
           if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(v_full + vs, C::VTILE);
           for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), kv0, bkv);
+            tma_load_3d(sV + vs * C::VTILE + j * C::VSLAB, &p.tm_v, v_full + vs, j * (C::SWV / 2), ky, kz);
           ++nv;
           ++n;
         }
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     int lo = 0, hi;
     if constexpr (GAT) hi = gathered_row_hi(keep_h, p.mask.nkw, q0 + quarter * 32 + delta);
-    else row_interval(p.mask, i, p.Sq, p.Sk, lo, hi);
+    else row_interval(p.mask, i, p.Sq, SkM, lo, hi);
     const float* kb = p.mask.key_bias ? p.mask.key_bias + (size_t)bh * p.Sk : nullptr;
     const uint32_t* keep = GAT ? nullptr : keep_h;  // gathered keys are all kept
     if (p.mask.table) keep = i < p.Sq ? table_row(p.mask, bh, p.Sq, i) : nullptr;  // this row's element bits
@@ -737,15 +767,28 @@ static int launch_packed(const FwdParams& prm, int grid, cudaStream_t st) {
 }
 
 int fwd_packed_decode_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
-                             int num_splits, void* o, float* lse, float* o_part, float* lse_part, cudaStream_t st) {
+                             int num_splits, void* o, float* lse, float* o_part, float* lse_part,
+                             const PagedKV* paged, cudaStream_t st) {
   FwdParams prm;
   memset(&prm, 0, sizeof(prm));
   const int sw = s.Dqk >= 64 ? 128 : 64;
   const int BHkv = s.B * s.Hkv;
   // Q as one range of B*H*Sq rows: a group's rows are consecutive
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.B * s.H * s.Sq, 1, sw)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
-  if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
+  if (paged && paged->page_table) {
+    // the pool as [num_pages * Hkv heads of page_size rows]
+    const int heads = paged->num_pages * s.Hkv;
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, paged->page_size, heads, sw)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, paged->page_size, heads, sw)) return GBATTN_ERR_CUDA;
+    prm.pk_pages = paged->page_table;
+    prm.pk_page_size = paged->page_size;
+    prm.pk_max_pages = paged->max_pages;
+    prm.pk_num_pages = paged->num_pages;
+  } else {
+    if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
+    if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, sw)) return GBATTN_ERR_CUDA;
+  }
+  if (paged) prm.pk_seqlens = paged->seqlens;
   prm.B = s.B;
   prm.H = s.H;
   prm.Sq = s.Sq;
@@ -762,8 +805,6 @@ int fwd_packed_decode_launch(const Shape& s, const void* q, const void* k, const
   prm.pk_R = prm.G * s.Sq;
   prm.pk_nrt = (prm.pk_R + 127) / 128;
   prm.pk_nsplit = num_splits;
-  int per = (s.Sk + num_splits - 1) / num_splits;
-  prm.pk_per = (per + 127) / 128 * 128;
   prm.o_part = o_part;
   prm.lse_part = lse_part;
   const long long grid = (long long)BHkv * prm.pk_nrt * num_splits;

@@ -56,11 +56,6 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
                     const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
                     float* dv, float* dkey_bias, void* ws, cudaStream_t st);
-// Split-KV decode of grouped query heads on the tensor cores (the forward
-// kernel in packed mode): writes O / LSE directly (num_splits == 1) or the
-// split partials o_part / lse_part for the combine. Dense cache, D = 64 / 128.
-int fwd_packed_decode_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
-                             int num_splits, void* o, float* lse, float* o_part, float* lse_part, cudaStream_t st);
 // Paged key/value cache of the decode path: pages of page_size keys of one
 // key/value head ([num_pages, Hkv, page_size, D]); seqlens may be given
 // without a page table (a dense cache with per-sequence key counts).
@@ -69,6 +64,13 @@ struct PagedKV {
   const int32_t* page_table;  // [B][max_pages] or nullptr
   int page_size, max_pages, num_pages;
 };
+// Split-KV decode of grouped query heads on the tensor cores (the forward
+// kernel in packed mode): writes O / LSE directly (num_splits == 1) or the
+// split partials o_part / lse_part for the combine. D = 64 / 128; a dense
+// cache, or a paged one whose pages hold a multiple of 128 keys.
+int fwd_packed_decode_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
+                             int num_splits, void* o, float* lse, float* o_part, float* lse_part,
+                             const PagedKV* paged, cudaStream_t st);
 int splitkv_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, int causal,
                    int num_splits, void* o, float* lse, void* ws, cudaStream_t st, const PagedKV* paged);
 // Split-KV forward with its split partials in the library's static scratch

@@ -246,7 +246,10 @@ int attn_fwd_splitkv(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, 
  *     max_pages_per_seq * page_size). CAUSAL aligns query i with key
  *     i + seqlens_k[b] - Sq.
  *   - Splits cut each sequence's own keys (L = ceil(seqlens_k[b]/num_splits)
- *     rounded up to 128). A page index outside [0, num_pages) or a key count
+ *     rounded up to 128). With GQA and page_size a multiple of 128, the
+ *     packed tensor-core path of attn_fwd_splitkv runs on the pages (one TMA
+ *     tile load per 128 keys, the page looked up per tile).
+ *   - A page index outside [0, num_pages) or a key count
  *     outside its range is not read: the kernel raises GBATTN_ERR_BLOCKS
  *     (gbattn_last_device_error) and the affected outputs are invalid.
  * Other arguments, workspace and status codes as attn_fwd_splitkv.

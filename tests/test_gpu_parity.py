@@ -311,7 +311,7 @@ def _paged_cache(k, v, page_size, seqlens, extra_pages, seed):
 
 @pytest.mark.parametrize("page_size,n,kind,Hkv,H", [(64, 1, "none", 2, 4), (128, 4, "causal", 1, 4),
                                                      (256, 16, "none", 4, 4), (192, 2, "causal", 2, 4),
-                                                     (128, 2, "causal", 1, 16)])
+                                                     (128, 2, "causal", 1, 16), (256, 1, "none", 2, 8)])
 def test_paged_splitkv_decode(page_size, n, kind, Hkv, H):
     B, Sq, S, D = 4, 2, 1100, 128
     c = Case(B, H, Sq, S, D, D, kind, Hkv=Hkv, lists=False, sparse=None)
@@ -334,13 +334,14 @@ def test_paged_splitkv_decode(page_size, n, kind, Hkv, H):
             check_lse(f64(lse[b, h]), l_ref)
 
 
-def test_paged_decode_bad_page_index_raises_device_error():
+@pytest.mark.parametrize("H,Hkv,page", [(2, 2, 64), (4, 1, 128)])  # per-row kernel; packed tensor-core path
+def test_paged_decode_bad_page_index_raises_device_error(H, Hkv, page):
     # a page index outside the pool is not read: the kernel flags it
-    B, H, D = 1, 2, 64
+    B, D = 1, 64
     q = torch.randn(B, H, 1, D).to(torch.bfloat16).cuda()
-    kc = torch.zeros(2, H, 64, D, dtype=torch.bfloat16).cuda()
+    kc = torch.zeros(2, Hkv, page, D, dtype=torch.bfloat16).cuda()
     table = torch.tensor([[0, 5]], dtype=torch.int32).cuda()
-    seqlens = torch.tensor([100], dtype=torch.int32).cuda()
+    seqlens = torch.tensor([page + 36], dtype=torch.int32).cuda()
     ga.attn_fwd_splitkv_paged(q, kc, kc, table, seqlens, 0.0, None, 1)
     torch.cuda.synchronize()
     assert ga.load_library().gbattn_last_device_error(None) == ga.binding.ERR_BLOCKS

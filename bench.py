@@ -130,6 +130,25 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def reduce_max(values, world, device):
+    """Max over ranks of each per-rank timing (ms): with replicas the job
+    takes as long as its slowest rank. world == 1 returns the values as is."""
+    if world == 1:
+        return dict(values)
+    import torch
+    import torch.distributed as dist
+    keys = sorted(values)
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {k: float(v) for k, v in zip(keys, t.tolist())}
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (units per second)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -223,10 +242,14 @@ def run_ours(args, rank, world, local_rank):
         for i, n in enumerate(names):
             ev[n].append(marks[i].elapsed_time(marks[i + 1]))
     per = {n: statistics.mean(v) for n, v in ev.items()}
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    red = reduce_max(dict(per, total=total_ms), world, dev)
+    total_ms = red.pop("total")
+    per = red
+
+    # ---------------- extensions outside the step (grouped-query paged decode)
+    ext = None
+    if not args.no_extensions and args.only == "all":
+        ext = run_extensions(ga, torch, dev, st, rank)  # ~17 GB more beside the 34 GB decode cache
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
@@ -241,8 +264,8 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     ms_step = total_ms / args.steps
     prefill_ms = per["mask"] + per["fwd"] + per["bwd"]
-    value = world * (fwd_f + bwd_f) / (prefill_ms * 1e-3) / 1e12
-    dec = {f"n={n}": round(decode_bytes() / (per[f"dec{n}"] * 1e-3) / 1e9, 1) for n in D["splits"]}
+    value = job_rate(fwd_f + bwd_f, world, prefill_ms) / 1e12
+    dec = {f"n={n}": round(job_rate(decode_bytes(), world, per[f"dec{n}"]) / 1e9, 1) for n in D["splits"]}
     traffic = load_traffic()
     tpeak = peaks["bf16_tflops_sustained"]
     kern = {
@@ -289,9 +312,58 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
     }
+    if ext is not None:
+        out["extensions"] = ext
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(quick=args.quick_cpu)
     return out
+
+
+def run_extensions(ga, torch, dev, st, rank):
+    """Grouped-query decode over a paged cache (not part of the step; timed on
+    its own): B=32, H=32 query heads on Hkv=8 key/value heads, 65536 keys per
+    sequence in a shuffled pool of 256-key pages, D=128, 4 splits. GB/s counts
+    the unique K/V bytes (each key/value row read once per group)."""
+    from block_sparse_attention_tma_gb300.synth import make_device_inputs
+    B, H, Hkv, Sk, D, page, n = 32, 32, 8, 65536, 128, 256, 4
+    x = make_device_inputs(B, H, 1, Sk, D, D, "bf16", seed=7 + rank, device=dev, dout=False, Hkv=Hkv)
+    npg = Sk // page
+    perm = torch.randperm(B * npg, generator=torch.Generator().manual_seed(11)).to(dev)
+    pools = []
+    for name in ("k", "v"):
+        src = x[name].view(B, Hkv, npg, page, D).permute(0, 2, 1, 3, 4).reshape(B * npg, Hkv, page, D)
+        pool = torch.empty_like(src)
+        pool[perm] = src
+        pools.append(pool)
+        x[name] = None
+    table = perm.view(B, npg).to(torch.int32).contiguous()
+    seqlens = torch.full((B,), Sk, dtype=torch.int32, device=dev)
+    o = torch.empty(B, H, 1, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, 1, dtype=torch.float32, device=dev)
+    ws = torch.empty(ga.attn_fwd_splitkv_workspace_bytes(B, H, 1, D, n), dtype=torch.uint8, device=dev)
+    run = lambda: ga.attn_fwd_splitkv_paged(x["q"], pools[0], pools[1], table, seqlens, 0.0, None, n,  # noqa: E731
+                                            o=o, lse=lse, workspace=ws, stream=st)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record(st)
+    for _ in range(reps):
+        run()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    uniq = B * Hkv * Sk * D * 2 * 2
+    rc = ga.load_library().gbattn_last_device_error(None)
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} in the extension run")
+    del pools, x
+    torch.cuda.empty_cache()
+    return {"gqa_paged_decode": {"config": f"B={B} H={H} Hkv={Hkv} Sq=1 Sk={Sk} D={D} bf16, {page}-key pages "
+                                           f"(shuffled pool), splits={n}",
+                                 "ms": round(ms, 4), "unique_kv_gbs": round(uniq / (ms * 1e-3) / 1e9, 1),
+                                 "kernel": "fwd_bf16_kernel<128,128> packed decode + combine"}}
 
 
 def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
@@ -440,6 +512,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extensions", action="store_true", help="skip the grouped-query paged decode line")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
     ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",

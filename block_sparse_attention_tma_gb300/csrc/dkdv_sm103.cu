@@ -24,6 +24,11 @@ struct DkdvCfg {
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
   static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
   static constexpr int QST = 2;
+  // elementwise warps: NG per TMEM lane quarter, each thread one key row and
+  // CW = 128 / NG of the tile's query columns
+  static constexpr int NG = 2, CW = 128 / NG;
+  static constexpr int THREADS = 64 + 128 * NG;
+  static constexpr int NEW = 128 * NG;  // elementwise threads
   static constexpr int GST = DQK >= 192 ? 1 : 2;
   static constexpr int T_R = 0, T_X = 128, T_DV = 192, T_DK = 192 + DV;
   static_assert(192 + DV + DQK <= 512, "TMEM budget");
@@ -34,7 +39,7 @@ struct DkdvCfg {
          B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, B_FIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
-      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 + 4 * (kMaxGroup + 4) + TCAP * 2 +
+      1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 * (NG - 1) + 4 * (kMaxGroup + 4) + TCAP * 2 +
       NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;  // one CTA per SM
   static constexpr uint32_t ID_ST = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
@@ -43,7 +48,7 @@ struct DkdvCfg {
 };
 
 template <int DQK, int DV, bool CAP, int KM, bool DB>
-__global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
   constexpr bool GAT = KM == 1;  // gathered keys
   constexpr bool TAB = KM == 2;  // element table mask
   using C = DkdvCfg<DQK, DV>;
@@ -54,8 +59,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   uint8_t* sQ = sV + C::VTILE;                  // [QST]
   uint8_t* sG = sQ + C::QST * C::QTILE;         // [GST]
   float* sLD = reinterpret_cast<float*>(sG + C::GST * C::VTILE);  // [QST][lse2 128 | delta 128]
-  float* sDB = sLD + C::QST * 256;                                  // [128] key-bias partial sums
-  int* soff = reinterpret_cast<int*>(sDB + 128);                    // [G + 1] slot offsets of the query heads
+  float* sDB = sLD + C::QST * 256;                                  // [NG-1][128] key-bias partial sums
+  int* soff = reinterpret_cast<int*>(sDB + 128 * (C::NG - 1));      // [G + 1] slot offsets of the query heads
   uint16_t* tlist = reinterpret_cast<uint16_t*>(soff + kMaxGroup + 4);  // [TCAP]
   uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
@@ -154,8 +159,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
   }
   if (threadIdx.x == 32) {
     for (int b = 0; b < C::NBAR; ++b)
-      mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? 256
-                         : b == C::B_FIN                                             ? 128
+      mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? C::NEW
+                         : b == C::B_FIN                                             ? C::NEW - 128
                                                                                      : 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -358,9 +363,10 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
     }
   } else {
     // ------------------------------------------------------------ P / dS warps
-    // two warps per TMEM lane quarter; each thread owns one key row and half
-    // (64) of the 128 query columns of the tile
-    const int sw = warp - 2, grp = sw >> 2, cb = grp * 64;
+    // NG warps per TMEM lane quarter; each thread owns one key row and CW of
+    // the 128 query columns of the tile
+    constexpr int CW = C::CW;
+    const int sw = warp - 2, grp = sw >> 2, cb = grp * CW;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row
     const int j = k0 + row;  // key (compact index when gathered)
@@ -414,22 +420,22 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       const float* sl = sLD + qs * 256;
       const float* sd = sl + 128;
       // copy S^T out of R, then let the MMA warp reuse R for dP^T
-      uint32_t r[64];
+      uint32_t r[CW];
       tmem_ld32(tl + C::T_R + cb, r);
-      tmem_ld32(tl + C::T_R + cb + 32, r + 32);
+      if constexpr (CW == 64) tmem_ld32(tl + C::T_R + cb + 32, r + 32);
       tmem_wait_ld32(r);
-      reg_fence32(r + 32);
+      if constexpr (CW == 64) reg_fence32(r + 32);
       tc_fence_before();
       mbar_arrive(bar + C::B_RA);
       // P^T = exp2(S^T * scale * log2e + key term - lse2[q])
-      uint32_t pk[32], dc[CAP ? 32 : 1];
+      uint32_t pk[CW / 2], dc[CAP ? CW / 2 : 1];
       const int clo = masked ? (kept ? ilo - q0 : 128) - cb : 0;
-      const int chi = masked ? ihi - q0 - cb : 63;
+      const int chi = masked ? ihi - q0 - cb : CW - 1;
       {
         const float4* sl4 = reinterpret_cast<const float4*>(sl + cb);
         float* pf = reinterpret_cast<float*>(r);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
+        for (int c4 = 0; c4 < CW / 4; ++c4) {
           const float4 l4 = sl4[c4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           float dd[4];
@@ -455,25 +461,25 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         }
         if (masked) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pf[c] = (c >= clo && c <= chi) ? pf[c] : 0.f;
+          for (int c = 0; c < CW; ++c) pf[c] = (c >= clo && c <= chi) ? pf[c] : 0.f;
           if constexpr (TAB) {
-            // element table: lane l fetches the word of query rows cb + l and
-            // cb + 32 + l that holds this warp's 32 keys (k0 is a multiple of
+            // element table: lane l fetches the word of query rows cb + l (and
+            // cb + 32 + l) that holds this warp's 32 keys (k0 is a multiple of
             // 128, so the word is warp-uniform and bit l is this thread's key)
             const int jw = j >> 5;
-            const int r0 = q0 + cb + lane, r1 = r0 + 32;
             const int bq = bq0 + g_cur;
-            const uint32_t w0 = (r0 < p.Sq && jw < p.mask.nkw) ? __ldg(table_row(p.mask, bq, p.Sq, r0) + jw) : 0u;
-            const uint32_t w1 = (r1 < p.Sq && jw < p.mask.nkw) ? __ldg(table_row(p.mask, bq, p.Sq, r1) + jw) : 0u;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (!((__shfl_sync(0xffffffffu, w0, c) >> lane) & 1u)) pf[c] = 0.f;
-              if (!((__shfl_sync(0xffffffffu, w1, c) >> lane) & 1u)) pf[c + 32] = 0.f;
+            for (int h = 0; h < CW / 32; ++h) {
+              const int rq = q0 + cb + 32 * h + lane;
+              const uint32_t w = (rq < p.Sq && jw < p.mask.nkw) ? __ldg(table_row(p.mask, bq, p.Sq, rq) + jw) : 0u;
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (!((__shfl_sync(0xffffffffu, w, c) >> lane) & 1u)) pf[32 * h + c] = 0.f;
             }
           }
         }
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
+        for (int c = 0; c < CW / 2; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
       }
       // X still holds dS^T of the previous tile until its dK MMA completes
       if (n >= 1) {
@@ -484,7 +490,8 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         }
         tc_fence_after();
       }
-      tmem_st32(tl + C::T_X + grp * 32, pk);
+      if constexpr (CW == 64) tmem_st32(tl + C::T_X + grp * 32, pk);
+      else tmem_st16(tl + C::T_X + grp * 16, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_P);
@@ -496,16 +503,16 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       }
       tc_fence_after();
       tmem_ld32(tl + C::T_R + cb, r);
-      tmem_ld32(tl + C::T_R + cb + 32, r + 32);
+      if constexpr (CW == 64) tmem_ld32(tl + C::T_R + cb + 32, r + 32);
       tmem_wait_ld32(r);
-      reg_fence32(r + 32);
+      if constexpr (CW == 64) reg_fence32(r + 32);
       tc_fence_before();
       mbar_arrive(bar + C::B_RB);
-      uint32_t ds[32];
+      uint32_t ds[CW / 2];
       {
         const float4* sd4 = reinterpret_cast<const float4*>(sd + cb);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
+        for (int c4 = 0; c4 < CW / 4; ++c4) {
           const float4 d4 = sd4[c4];
           const uint32_t p01 = pk[2 * c4], p23 = pk[2 * c4 + 1];
           float d0 = bf_lo(p01) * (__uint_as_float(r[4 * c4 + 0]) - d4.x);
@@ -530,14 +537,15 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
         break;
       }
       tc_fence_after();
-      tmem_st32(tl + C::T_X + grp * 32, ds);
+      if constexpr (CW == 64) tmem_st32(tl + C::T_X + grp * 32, ds);
+      else tmem_st16(tl + C::T_X + grp * 16, ds);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar + C::B_DS);
       ++n;
     }
     // ---- epilogue: dV, dK rows of this thread's key (32-column chunks split
-    // between the two warps of a lane quarter)
+    // between the NG warps of a lane quarter)
     if (ok) {
       const bool wrote = n > 0;
       if (wrote) {
@@ -547,19 +555,22 @@ __global__ void __launch_bounds__(320, 1) dkdv_kernel(const __grid_constant__ Bw
       const bool jin = j < Skv;
       const int jo = orig();
       if constexpr (DB) {
-        // key-bias gradient of this key: both halves' sums
-        if (ok && grp == 1) {
-          sDB[row] = dbs;
+        // key-bias gradient of this key: the NG column groups' sums
+        if (ok && grp >= 1) {
+          sDB[(grp - 1) * 128 + row] = dbs;
           mbar_arrive(bar + C::B_FIN);
         } else if (ok && mbar_wait(bar + C::B_FIN, 0, abort_flag) && jin) {
-          p.dbias[(size_t)bq0 * p.Sk + jo] = dbs + sDB[row];
+          float t = dbs;
+#pragma unroll
+          for (int g2 = 0; g2 < C::NG - 1; ++g2) t += sDB[g2 * 128 + row];
+          p.dbias[(size_t)bq0 * p.Sk + jo] = t;
         }
       }
       if (ok) {
         __nv_bfloat16* dvrow = p.dv + ((size_t)bkv * p.Sk + jo) * DV;
         __nv_bfloat16* dkrow = p.dk + ((size_t)bkv * p.Sk + jo) * DQK;
 #pragma unroll 1
-        for (int c0 = grp * 32; c0 < DV + DQK; c0 += 64) {
+        for (int c0 = grp * 32; c0 < DV + DQK; c0 += 32 * C::NG) {
           const bool isv = c0 < DV;
           uint32_t a[32];
           if (wrote) {
@@ -605,7 +616,7 @@ template <int DQK, int DV, bool CAP, int KM, bool DB>
 static int launch_one(const BwdParams& prm, int grid, cudaStream_t st) {
   static bool attr = false;
   if (set_smem_once(dkdv_kernel<DQK, DV, CAP, KM, DB>, DkdvCfg<DQK, DV>::SMEM, &attr)) return GBATTN_ERR_CUDA;
-  dkdv_kernel<DQK, DV, CAP, KM, DB><<<grid, 320, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
+  dkdv_kernel<DQK, DV, CAP, KM, DB><<<grid, DkdvCfg<DQK, DV>::THREADS, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

@@ -142,3 +142,42 @@ def test_splitkv_decode_32x32x65536(n):
         check_lse(f64(lse[b, h]), l_ref)
     del x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("Hkv,paged,n", [(8, True, 4), (1, False, 4), (4, False, 1)])
+def test_gqa_decode_32x32x65536(Hkv, paged, n):
+    # grouped-query decode at the decode workload's size: packed tensor-core
+    # path, dense or over a shuffled 256-key page pool with per-sequence lengths
+    B, H, Sk, D, page = 32, 32, 65536, 128, 256
+    x = make_device_inputs(B, H, 1, Sk, D, D, "bf16", seed=42, dout=False, Hkv=Hkv)
+    G = H // Hkv
+    if paged:
+        npg = Sk // page
+        kc = x["k"].view(B, Hkv, npg, page, D).permute(0, 2, 1, 3, 4).reshape(B * npg, Hkv, page, D)
+        vc = x["v"].view(B, Hkv, npg, page, D).permute(0, 2, 1, 3, 4).reshape(B * npg, Hkv, page, D)
+        perm = torch.randperm(B * npg, generator=torch.Generator().manual_seed(3)).cuda()
+        kpool = torch.empty_like(kc)
+        vpool = torch.empty_like(vc)
+        kpool[perm] = kc
+        vpool[perm] = vc
+        del kc, vc
+        table = perm.view(B, npg).to(torch.int32).contiguous()
+        rng = np.random.default_rng(5)
+        lens = rng.integers(1, Sk + 1, size=B)
+        lens[0], lens[1] = Sk, 1
+        seqlens = torch.from_numpy(lens.astype(np.int32)).cuda()
+        o, lse = ga.attn_fwd_splitkv_paged(x["q"], kpool, vpool, table, seqlens, 0.0, None, n)
+    else:
+        lens = np.full(B, Sk)
+        o, lse = ga.attn_fwd_splitkv(x["q"], x["k"], x["v"], 0.0, None, n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    for (b, h) in ((0, 0), (1, 5), (7, 31), (20, 17), (31, 8)):
+        L = int(lens[b])
+        hk = h // G
+        p = orc.Problem(f64(x["q"][b, h]), f64(x["k"][b, hk, :L]), f64(x["v"][b, hk, :L]))
+        o_ref, l_ref = p.forward()
+        check_out(f64(o[b, h]), o_ref)
+        check_lse(f64(lse[b, h]), l_ref)
+    del x
+    torch.cuda.empty_cache()

@@ -319,13 +319,13 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
-def run_extensions(ga, torch, dev, st, rank):
+def run_extensions(ga, torch, dev, st, rank, Sk=65536):
     """Grouped-query decode over a paged cache (not part of the step; timed on
     its own): B=32, H=32 query heads on Hkv=8 key/value heads, 65536 keys per
     sequence in a shuffled pool of 256-key pages, D=128, 4 splits. GB/s counts
     the unique K/V bytes (each key/value row read once per group)."""
     from block_sparse_attention_tma_gb300.synth import make_device_inputs
-    B, H, Hkv, Sk, D, page, n = 32, 32, 8, 65536, 128, 256, 4
+    B, H, Hkv, D, page, n = 32, 32, 8, 128, 256, 4
     x = make_device_inputs(B, H, 1, Sk, D, D, "bf16", seed=7 + rank, device=dev, dout=False, Hkv=Hkv)
     npg = Sk // page
     perm = torch.randperm(B * npg, generator=torch.Generator().manual_seed(11)).to(dev)
@@ -515,8 +515,9 @@ def main():
     ap.add_argument("--no-extensions", action="store_true", help="skip the grouped-query paged decode line")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
     ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "gqa"], default="all",
                     help="time one part only (profiling runs); prints a short line, not the bench line")
+    ap.add_argument("--gqa-sk", type=int, default=65536, help="keys of the grouped-query decode (--only gqa)")
     ap.add_argument("--decode-sk", type=int, default=DECODE["Sk"], help="decode keys (profiling runs only)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -535,9 +536,18 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.only == "all" and args.decode_sk != DECODE["Sk"]:
         ap.error("--decode-sk is for profiling runs with --only")
-    out = run_ours(args, rank, world, local_rank)
-    if rank == 0 and out is not None:
-        print(json.dumps(out), flush=True)
+    if args.only == "gqa":
+        import torch
+        import block_sparse_attention_tma_gb300 as ga
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        ext = run_extensions(ga, torch, dev, torch.cuda.current_stream(dev), rank, Sk=args.gqa_sk)
+        if rank == 0:
+            print(json.dumps({"only": "gqa", **ext}), flush=True)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

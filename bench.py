@@ -366,21 +366,38 @@ def run_extensions(ga, torch, dev, st, rank, Sk=65536):
                                  "kernel": "fwd_bf16_kernel<128,128> packed decode + combine"}}
 
 
-def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
-    """Same step through the C ABI with host buffers: pinned host inputs are
-    copied in and the step's results copied out inside the timed region."""
+def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=4):
+    """Same step through the C ABI with host buffers: every step copies its
+    inputs in from pinned host memory and its results out, inside the timed
+    region. The step is cut into `nch` independent chunks (heads for the
+    prefill, sequences for the decode) on `nch` streams, the way a caller of
+    the stream-ordered API overlaps one chunk's copies with another's kernels;
+    the work per step is the same as the device-only step."""
     P, D = PREFILL, DECODE
     B, H, S, Dqk, Dv = P["B"], P["H"], P["S"], P["Dqk"], P["Dv"]
+    hc = H // nch
+    streams = [torch.cuda.Stream(dev) for _ in range(nch)]
+    # prefill chunk c = heads [c*hc, (c+1)*hc): contiguous host / device slices (B == 1)
     h_in = {n: t.pin_memory() for n, t in x.items()}
-    d_in = {n: torch.empty_like(t, device=dev) for n, t in x.items()}
     outs = {"o": (B, H, S, Dv), "dq": (B, H, S, Dqk), "dk": (B, H, S, Dqk), "dv": (B, H, S, Dv)}
-    h_out = {n: torch.empty(s, dtype=torch.bfloat16).pin_memory() for n, s in outs.items()}
+    h_out = {n: torch.empty(sh, dtype=torch.bfloat16).pin_memory() for n, sh in outs.items()}
     h_lse = torch.empty(B, H, S, dtype=torch.float32).pin_memory()
-    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
-    o = torch.empty(B, H, S, Dv, dtype=torch.bfloat16, device=dev)
-    dq, dk, dv = (torch.empty(s, dtype=torch.bfloat16, device=dev) for s in (outs["dq"], outs["dk"], outs["dv"]))
-    ws = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, H, S, S, Dqk, Dv), dtype=torch.uint8, device=dev)
-    # decode: host copies of the KV cache (34 GB pinned) are what a host caller holds
+    chunks = []
+    for c in range(nch):
+        hs = slice(c * hc, (c + 1) * hc)
+        ch = {"hs": hs, "in": {n: torch.empty_like(t[:, hs], device=dev) for n, t in x.items()}}
+        ch["spec"] = spec
+        ch["lists"] = ga.alloc_block_lists(B, hc, S, S, P["sparse_m"], P["sparse_n"], device=dev)
+        ch["o"] = torch.empty(B, hc, S, Dv, dtype=torch.bfloat16, device=dev)
+        ch["lse"] = torch.empty(B, hc, S, dtype=torch.float32, device=dev)
+        ch["dq"] = torch.empty(B, hc, S, Dqk, dtype=torch.bfloat16, device=dev)
+        ch["dk"] = torch.empty(B, hc, S, Dqk, dtype=torch.bfloat16, device=dev)
+        ch["dv"] = torch.empty(B, hc, S, Dv, dtype=torch.bfloat16, device=dev)
+        ch["ws"] = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, hc, S, S, Dqk, Dv), dtype=torch.uint8,
+                               device=dev)
+        chunks.append(ch)
+    # decode chunk c = sequences [c*bc, (c+1)*bc); the host holds the KV cache (34 GB pinned)
+    bc = D["B"] // nch
     dh = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in dx.items()}
     for n, t in dx.items():
         dh[n].copy_(t)
@@ -389,25 +406,34 @@ def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
     d_lse = torch.empty(D["B"], D["H"], D["Sq"], dtype=torch.float32, device=dev)
     h_do = torch.empty(d_o.shape, dtype=torch.bfloat16).pin_memory()
     nmax = max(D["splits"])
-    dws = torch.empty(ga.attn_fwd_splitkv_workspace_bytes(D["B"], D["H"], D["Sq"], D["D"], nmax), dtype=torch.uint8,
-                      device=dev)
+    dws = [torch.empty(ga.attn_fwd_splitkv_workspace_bytes(bc, D["H"], D["Sq"], D["D"], nmax), dtype=torch.uint8,
+                       device=dev) for _ in range(nch)]
 
     def prefill():
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        ga.build_block_mask(B, H, S, S, spec, lists)
-        ga.attn_fwd(d_in["q"], d_in["k"], d_in["v"], 0.0, spec, lists, o=o, lse=lse)
-        ga.attn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["do"], lse, 0.0, spec, lists, dq=dq, dk=dk, dv=dv,
-                    workspace=ws)
-        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-            h_out[n].copy_(t, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        for ch, s in zip(chunks, streams):
+            hs = ch["hs"]
+            with torch.cuda.stream(s):
+                for n in h_in:
+                    ch["in"][n].copy_(h_in[n][:, hs], non_blocking=True)
+                sp = ga.MaskSpec(kind=spec.kind, rel_bias_slope=spec.rel_bias_slope)
+                ga.build_block_mask(B, hc, S, S, sp, ch["lists"])
+                ga.attn_fwd(ch["in"]["q"], ch["in"]["k"], ch["in"]["v"], 0.0, sp, ch["lists"], o=ch["o"],
+                            lse=ch["lse"])
+                ga.attn_bwd(ch["in"]["q"], ch["in"]["k"], ch["in"]["v"], ch["o"], ch["in"]["do"], ch["lse"], 0.0,
+                            sp, ch["lists"], dq=ch["dq"], dk=ch["dk"], dv=ch["dv"], workspace=ch["ws"])
+                for n in ("o", "dq", "dk", "dv"):
+                    h_out[n][:, hs].copy_(ch[n], non_blocking=True)
+                h_lse[:, hs].copy_(ch["lse"], non_blocking=True)
 
     def decode():
-        for n in dh:
-            dd[n].copy_(dh[n], non_blocking=True)
-        ga.attn_fwd_splitkv(dd["q"], dd["k"], dd["v"], 0.0, None, nmax, o=d_o, lse=d_lse, workspace=dws)
-        h_do.copy_(d_o, non_blocking=True)
+        for c, s in enumerate(streams):
+            bs = slice(c * bc, (c + 1) * bc)
+            with torch.cuda.stream(s):
+                for n in dh:
+                    dd[n][bs].copy_(dh[n][bs], non_blocking=True)
+                ga.attn_fwd_splitkv(dd["q"][bs], dd["k"][bs], dd["v"][bs], 0.0, None, nmax, o=d_o[bs], lse=d_lse[bs],
+                                    workspace=dws[c])
+                h_do[bs].copy_(d_o[bs], non_blocking=True)
 
     steps = max(2, min(args.steps, 5))
     res = {}
@@ -419,12 +445,16 @@ def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st):
             fn()
         torch.cuda.synchronize()
         res[name] = (time.perf_counter() - t0) / steps
+    rc = ga.load_library().gbattn_last_device_error(None)
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} in the end-to-end run")
     fwd_f, bwd_f, _ = prefill_flops()
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values()) + h_lse.numel() * 4
     dh2d = sum(t.numel() * t.element_size() for t in dh.values())
     return {"value": round((fwd_f + bwd_f) / res["prefill"] / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(res["prefill"] * 1e3, 3),
+            "pipelining": f"{nch} head chunks (prefill) / {nch} sequence chunks (decode) on {nch} streams",
             "decode": {"value": round(decode_bytes() / res["decode"] / 1e9, 1), "unit": "GB/s",
                        "splits": nmax, "h2d_bytes_per_step": dh2d,
                        "d2h_bytes_per_step": h_do.numel() * 2, "ms_per_step": round(res["decode"] * 1e3, 3)},

@@ -21,9 +21,11 @@ struct BwdParams {
   const float* delta;  // [BH][sq_pad]
   __nv_bfloat16 *dq, *dk, *dv;
   float* dbias;        // [BH][Sk] key-bias gradient, or nullptr
-  int gather;          // gathered keys: tm_k / tm_v are 2-D row-gather maps
+  int gather;          // gathered keys: tm_k / tm_v are 2-D row-gather maps (dK/dV
+                       // kernel); the dQ kernel copies rows of gk / gv by index
   int Skv;             // key extent the kernels stream (Sk, or the kept-key count)
   const int32_t* kidx; // [BH][Sk] kept key indices (gathered keys)
+  const __nv_bfloat16 *gk, *gv;  // K [B*H*Sk, Dqk], V [B*H*Sk, Dv] (gathered keys)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -89,15 +89,19 @@ __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_b
 // CTA = (b, h, 128-row query tile), walking the forward lists (thread = query
 // row). Per kv tile n: S_n = Q K_n^T -> [0,128), dP_n = dO V_n^T -> [128,256);
 // dS_n = P (dP - delta) -> [448,512) (bf16); dQ += dS_n K_n -> [256,256+Dqk).
-// dQ of tile n is issued after S / dP of tile n+1.
-template <int DQK, int DV>
+// dQ of tile n is issued after S / dP of tile n+1, so the K stage of tile n
+// is free only once dQ_n is done; the V stage once dP_n is done.
+template <int DQK, int DV, bool GAT>
 struct DqCfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
   static constexpr int SWV = DV >= 64 ? 128 : 64;
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
   static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
-  static constexpr int KST = 2;
-  static constexpr int VST = DQK >= 192 ? 1 : 2;
+  // Stages (measured at 8K causal, 16 heads): a third K stage hides the K
+  // load behind dQ; at Dqk = 128 it costs the second V stage, which the
+  // slower cp.async copies of gathered keys cannot spare.
+  static constexpr int KST = DQK == 64 || (DQK == 128 && !GAT) ? 3 : 2;
+  static constexpr int VST = DQK >= 192 || (DQK == 128 && !GAT) ? 1 : 2;
   static constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 448;
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
   // B_RS / B_RP: the elementwise warps have copied S / dP out of TMEM;
@@ -114,7 +118,7 @@ struct DqCfg {
 
 template <int DQK, int DV, bool CAP, bool GAT>
 __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdParams p) {
-  using C = DqCfg<DQK, DV>;
+  using C = DqCfg<DQK, DV, GAT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
@@ -169,7 +173,11 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
     build_tile_list(slot, nslots, tlist, C::TCAP, tcount);
   }
   if (threadIdx.x == 32) {
-    for (int b = 0; b < C::NBAR; ++b) mbar_init(bar + b, (b == C::B_DS || b == C::B_RS || b == C::B_RP) ? 256 : 1);
+    // gathered K / V tiles: one arrival per producer lane once its copies landed
+    for (int b = 0; b < C::NBAR; ++b) {
+      const bool kv_full = (b >= C::B_KF && b < C::B_KF + C::KST) || (b >= C::B_VF && b < C::B_VF + C::VST);
+      mbar_init(bar + b, (b == C::B_DS || b == C::B_RS || b == C::B_RP) ? 256 : (GAT && kv_full) ? 32 : 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -223,13 +231,16 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         }
       }
     } else {
-      // gathered keys: lane 0 waits and issues Q / dO; every lane gathers 4
-      // rows of each K and V tile
-      int n = 0, nk = 0, nv = 0;
+      // gathered keys: lane 0 waits and issues Q / dO; the warp copies the
+      // kept rows of each K and V tile with cp.async (lane l looks up the
+      // rows l, l + 32, l + 64 and l + 96 of the tile)
+      int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
       int kv0;
       bool masked;
+      const __nv_bfloat16* kh = p.gk + (size_t)bkv * p.Sk * DQK;
+      const __nv_bfloat16* vh = p.gv + (size_t)bkv * p.Sk * DV;
       while (ok && it.next(&kv0, &masked)) {
         if (n == 0 && lane == 0) {
           mbar_expect_tx(bar + C::B_QG, C::QTILE + C::VTILE);
@@ -238,39 +249,27 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
           for (int j = 0; j < C::NVSLAB; ++j)
             tma_load_3d(sG + j * C::VSLAB, &p.tm_do, bar + C::B_QG, j * (C::SWV / 2), q0, bh);
         }
-        int gr[4];
+        int ro[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) gr[e] = bkv * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
-        const int ks = n % C::KST;
-        bool w = true;
-        if (lane == 0 && n >= C::KST) w = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag);
-        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-        if (lane == 0) mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < C::NQSLAB; ++j)
-          tma_gather4(sK + ks * C::QTILE + j * C::QSLAB + 4 * lane * C::SWQ, &p.tm_k, bar + C::B_KF + ks,
-                      j * (C::SWQ / 2), gr[0], gr[1], gr[2], gr[3]);
-        ++nk;
+        for (int e = 0; e < 4; ++e) ro[e] = __ldg(pos_h + min(kv0 + 32 * e + lane, Skv - 1));
+        // V first: its stage is released by dP of tile n - VST, before the K
+        // stage (released by dQ of tile n - KST, issued one tile later). The
+        // empty barriers complete once the tensor cores have read the stage.
         const int vs = n % C::VST;
+        bool w = true;
         if (lane == 0 && n >= C::VST) w = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag);
         if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-        if (lane == 0) mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < C::NVSLAB; ++j)
-          tma_gather4(sV + vs * C::VTILE + j * C::VSLAB + 4 * lane * C::SWV, &p.tm_v, bar + C::B_VF + vs,
-                      j * (C::SWV / 2), gr[0], gr[1], gr[2], gr[3]);
-        ++nv;
+        gather_tile_async<DV, C::SWV>(sV + vs * C::VTILE, vh, ro, lane);
+        cp_async_arrive(bar + C::B_VF + vs);
+        const int ks = n % C::KST;
+        if (lane == 0 && n >= C::KST) w = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag);
+        if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+        gather_tile_async<DQK, C::SWQ>(sK + ks * C::QTILE, kh, ro, lane);
+        cp_async_arrive(bar + C::B_KF + ks);
         ++n;
       }
-      if (lane == 0 && *abort_flag) {
-        if (nk > 0) mbar_drain(bar + C::B_QG, 0);
-        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t)
-          mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
-        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t)
-          mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
-      }
+      cp_async_wait_all();  // every copy of this thread lands before the CTA exits
+      if (lane == 0 && *abort_flag && n > 0) mbar_drain(bar + C::B_QG, 0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -301,6 +300,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         if (n == 0 && !(ok = mbar_wait(bar + C::B_QG, 0, abort_flag))) break;
         const int ks = n % C::KST, vs = n % C::VST;
         if (!(ok = mbar_wait(bar + C::B_KF + ks, (n / C::KST) & 1, abort_flag))) break;
+        if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_RS, (n - 1) & 1, abort_flag))) break;  // S_{n-1} read
         tc_fence_after();
         {
@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         }
         umma_commit(bar + C::B_S);
         if (!(ok = mbar_wait(bar + C::B_VF + vs, (n / C::VST) & 1, abort_flag))) break;
+        if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_RP, (n - 1) & 1, abort_flag))) break;  // dP_{n-1} read
         tc_fence_after();
         {
@@ -521,8 +522,8 @@ static int set_smem_once(K kern, int bytes, bool* flag) {
 template <int DQK, int DV, bool CAP, bool GAT>
 static int launch_dq(const BwdParams& prm, const Shape& s, cudaStream_t st) {
   static bool attr = false;
-  if (set_smem_once(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV>::SMEM, &attr)) return GBATTN_ERR_CUDA;
-  dq_kernel<DQK, DV, CAP, GAT><<<((s.Sq + 127) / 128) * s.B * s.H, 320, DqCfg<DQK, DV>::SMEM, st>>>(prm);
+  if (set_smem_once(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV, GAT>::SMEM, &attr)) return GBATTN_ERR_CUDA;
+  dq_kernel<DQK, DV, CAP, GAT><<<((s.Sq + 127) / 128) * s.B * s.H, 320, DqCfg<DQK, DV, GAT>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
@@ -555,6 +556,8 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.gather = m.gather;
   prm.Skv = m.gather ? m.kept : s.Sk;
   prm.kidx = m.gather ? m.keep_idx : nullptr;
+  prm.gk = static_cast<const __nv_bfloat16*>(k);
+  prm.gv = static_cast<const __nv_bfloat16*>(v);
   prm.dbias = dkey_bias;
   prm.B = s.B;
   prm.H = s.H;

@@ -130,6 +130,50 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
+// Row gather with 16-byte asynchronous copies (cp.async, generic proxy).
+// The copying threads' completion is tracked on an mbarrier; the thread that
+// waits on it issues fence_async_smem() before the tensor cores read the tile.
+//
+// Copies one 128-row K-major bf16 tile of D columns into the layout a tiled
+// TMA load with an SW-byte swizzle writes: D * 2 / SW slabs of 128 rows x SW
+// bytes, the 16-byte chunk c of row r of a slab stored at chunk
+// c ^ ((r * SW / 128) % (SW / 16)). Tile row r is row ro[r / 32] of lane
+// r % 32 of the row-major [rows, D] matrix src. Each warp instruction copies
+// 512 / SW whole slab rows (coalesced global reads).
+template <int D, int SW>
+__device__ __forceinline__ void gather_tile_async(uint8_t* tile, const __nv_bfloat16* src, const int (&ro)[4],
+                                                  int lane) {
+  constexpr int CPR = SW / 16;   // 16-byte chunks per slab row
+  constexpr int RPI = 32 / CPR;  // slab rows per warp instruction
+  constexpr int NSLAB = D * 2 / SW;
+  constexpr int SLAB = 128 * SW;
+  const int c = lane % CPR, h = lane / CPR;
+  // row RPI * i + h: its swizzled chunk depends on i only through i % 2
+  uint32_t dl[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int r = RPI * q + h;
+    dl[q] = smem_u32(tile) + h * SW + ((c ^ ((r * SW / 128) & (CPR - 1))) << 4);
+  }
+  const char* sl = reinterpret_cast<const char*>(src) + c * 16;
+#pragma unroll
+  for (int i = 0; i < 4 * CPR; ++i) {
+    // rows 32e .. 32e + 31 are copied by instructions e * CPR .. e * CPR + CPR - 1
+    const int row = __shfl_sync(0xffffffffu, ro[i / CPR], (RPI * i + h) & 31);
+    const char* g = sl + (size_t)row * (D * 2);
+    const uint32_t d = dl[i & 1] + RPI * i * SW;
+#pragma unroll
+    for (int sb = 0; sb < NSLAB; ++sb)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + sb * SLAB), "l"(g + sb * SW) : "memory");
+  }
+}
+// Arrives on bar once every cp.async this thread has issued so far has landed
+// (counts as one of the arrivals the barrier was initialised with).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 1-D bulk copy global -> shared. dst, src 16-byte aligned; bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

@@ -52,9 +52,10 @@ struct FwdParams {
   float cap_post;      // softcap * log2(e)
   MaskParams mask;
   int has_lists;
-  int gather;          // gathered keys: tm_k / tm_v are 2-D row-gather maps
+  int gather;          // gathered keys: rows of gk / gv copied by index
   int Skv;             // streamed key extent (Sk, or the kept-key count)
   const int32_t* kidx; // [B*H, Sk] kept key indices (gathered keys)
+  const __nv_bfloat16 *gk, *gv;  // K [B*H*Sk, Dqk], V [B*H*Sk, Dv] (gathered keys)
   int sub;             // sparse_n / 128
   int nqb, nkb, sparse_m;
   const int32_t *mcnt, *midx, *fcnt, *fidx;  // forward lists
@@ -236,8 +237,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   if (threadIdx.x == 32) {
     mbar_init(q_full, 1);
     mbar_init(q_tmem, 128);
-    for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
+    // gathered tiles: one arrival per producer lane once its copies landed
+    for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, GAT ? 32 : 1); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, GAT ? 32 : 1); mbar_init(v_empty + i, 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 256); }
     for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 64);
     mbar_init(o_done, 1);
@@ -314,52 +316,41 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         }
       }
     } else if (any_tile) {
-      // gathered keys: lane 0 waits and issues Q; every lane gathers 4 rows
-      // of each K and V tile
+      // gathered keys: lane 0 waits and issues Q; the warp copies the kept
+      // rows of each K and V tile with cp.async (lane l looks up the rows
+      // l, l + 32, l + 64 and l + 96 of the tile)
       if (lane == 0) {
         tma_prefetch_desc(&p.tm_q);
-        tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_v);
         mbar_expect_tx(q_full, C::QTILE);
         for (int j = 0; j < C::NQSLAB; ++j) tma_load_3d(sQ + j * C::QSLAB, &p.tm_q, q_full, j * (C::SWQ / 2), q0, bh);
       }
-      int n = 0, nk = 0, nv = 0;
+      int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
       int kv0;
       bool masked;
+      const __nv_bfloat16* kh = p.gk + (size_t)bkv * p.Sk * DQK;
+      const __nv_bfloat16* vh = p.gv + (size_t)bkv * p.Sk * DV;
       while (ok && it.next(&kv0, &masked)) {
-        int gr[4];
+        int ro[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) gr[e] = bkv * p.Sk + __ldg(pos_h + min(kv0 + 4 * lane + e, Skv - 1));
+        for (int e = 0; e < 4; ++e) ro[e] = __ldg(pos_h + min(kv0 + 32 * e + lane, Skv - 1));
         const int ks = n % C::KST;
         bool w = true;
         if (lane == 0 && n >= C::KST) w = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag);
         if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-        if (lane == 0) mbar_expect_tx(k_full + ks, C::QTILE);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < C::NQSLAB; ++j)
-          tma_gather4(sK + ks * C::QTILE + j * C::QSLAB + 4 * lane * C::SWQ, &p.tm_k, k_full + ks, j * (C::SWQ / 2),
-                      gr[0], gr[1], gr[2], gr[3]);
-        ++nk;
+        // (the empty barrier completes once the tensor cores have read the stage)
+        gather_tile_async<DQK, C::SWQ>(sK + ks * C::QTILE, kh, ro, lane);
+        cp_async_arrive(k_full + ks);
         const int vs = n % C::VST;
         if (lane == 0 && n >= C::VST) w = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag);
         if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-        if (lane == 0) mbar_expect_tx(v_full + vs, C::VTILE);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < C::NVSLAB; ++j)
-          tma_gather4(sV + vs * C::VTILE + j * C::VSLAB + 4 * lane * C::SWV, &p.tm_v, v_full + vs, j * (C::SWV / 2),
-                      gr[0], gr[1], gr[2], gr[3]);
-        ++nv;
+        gather_tile_async<DV, C::SWV>(sV + vs * C::VTILE, vh, ro, lane);
+        cp_async_arrive(v_full + vs);
         ++n;
       }
-      if (lane == 0 && *abort_flag) {
-        mbar_drain(q_full, 0);
-        for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
-        for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
-      }
+      cp_async_wait_all();  // every copy of this thread lands before the CTA exits
+      if (lane == 0 && *abort_flag) mbar_drain(q_full, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -371,6 +362,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
         const int vs = j % C::VST;
         if (!mbar_wait(v_full + vs, (j / C::VST) & 1, abort_flag)) return false;
+        if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         tc_fence_after();
         // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows
         const uint32_t vlo = vd.lo + ((vs * C::VTILE) >> 4);
@@ -391,6 +383,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       while (ok && it.next(&kv0, &masked)) {
         const int ks = n % C::KST;
         if (!(ok = mbar_wait(k_full + ks, (n / C::KST) & 1, abort_flag))) break;
+        if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         tc_fence_after();
         const uint32_t d = tmem + (n & 1) * 128;
         const uint32_t klo = kd.lo + ((ks * C::QTILE) >> 4);
@@ -460,21 +453,60 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
     int kv0;
     bool masked;
+    // With a key bias its loads run ahead of the tiles: the original key
+    // indices of tile n + 2 and the bias values of tile n + 1 are loaded
+    // while tile n is processed (-1: no key).
+    auto ahead = it;
+    auto key_of = [&](int st, int e) -> int {
+      const int j = st + cb + e * 32 + lane;
+      if (j >= Skv) return -1;
+      if constexpr (GAT) return __ldg(pos_h + j);
+      return j;
+    };
+    int jo_cur[2] = {-1, -1}, jo_nx[2] = {-1, -1};
+    float bv_cur[2] = {0.f, 0.f};
+    if (kb && ok) {
+      int st;
+      bool mk;
+      if (ahead.next(&st, &mk)) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) jo_cur[e] = key_of(st, e);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) bv_cur[e] = jo_cur[e] >= 0 ? __ldg(kb + jo_cur[e]) : 0.f;
+      if (ahead.next(&st, &mk)) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) jo_nx[e] = key_of(st, e);
+      }
+    }
     while (ok && it.next(&kv0, &masked)) {
       const int sb = n & 1;
       // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
       // columns; each warp keeps its own copy, so only a warp sync is needed
       float* ctw = colterm + (sw * 2 + sb) * 64;
+      if (kb) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = kv0 + cb + e * 32 + lane;
-        float c = 0.f;
-        if (j < Skv) {
-          int jo = j;  // original key index
-          if constexpr (GAT) jo = __ldg(pos_h + j);
-          c = ((kb ? __ldg(kb + jo) : 0.f) - p.mask.slope * (float)jo) * kLog2e;
+        for (int e = 0; e < 2; ++e)
+          ctw[e * 32 + lane] = jo_cur[e] >= 0 ? (bv_cur[e] - p.mask.slope * (float)jo_cur[e]) * kLog2e : 0.f;
+        int st;
+        bool mk;
+        int jo_n2[2] = {-1, -1};
+        if (ahead.next(&st, &mk)) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) jo_n2[e] = key_of(st, e);
         }
-        ctw[e * 32 + lane] = c;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          bv_cur[e] = jo_nx[e] >= 0 ? __ldg(kb + jo_nx[e]) : 0.f;
+          jo_cur[e] = jo_nx[e];
+          jo_nx[e] = jo_n2[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int jo = key_of(kv0, e);  // original key index
+          ctw[e * 32 + lane] = jo >= 0 ? -p.mask.slope * (float)jo * kLog2e : 0.f;
+        }
       }
       __syncwarp();
       ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
@@ -698,9 +730,9 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;
   const int BHkv = s.B * s.Hkv;
-  if (m.gather) {
-    if (!make_tmap_bf16_rows(&prm.tm_k, k, s.Dqk, (long long)BHkv * s.Sk, swq)) return GBATTN_ERR_CUDA;
-    if (!make_tmap_bf16_rows(&prm.tm_v, v, s.Dv, (long long)BHkv * s.Sk, swv)) return GBATTN_ERR_CUDA;
+  if (m.gather) {  // rows copied by index, no tensor maps
+    prm.gk = static_cast<const __nv_bfloat16*>(k);
+    prm.gv = static_cast<const __nv_bfloat16*>(v);
   } else {
     if (!make_tmap_bf16_3d(&prm.tm_k, k, s.Dqk, s.Sk, BHkv, swq)) return GBATTN_ERR_CUDA;
     if (!make_tmap_bf16_3d(&prm.tm_v, v, s.Dv, s.Sk, BHkv, swv)) return GBATTN_ERR_CUDA;

@@ -250,6 +250,7 @@ def run_ours(args, rank, world, local_rank):
     ext = None
     if not args.no_extensions and args.only == "all":
         ext = run_extensions(ga, torch, dev, st, rank)  # ~17 GB more beside the 34 GB decode cache
+        ext.update(run_workload_sweep(ga, torch, dev, st, g, rank))
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
@@ -364,6 +365,101 @@ def run_extensions(ga, torch, dev, st, rank, Sk=65536):
                                            f"(shuffled pool), splits={n}",
                                  "ms": round(ms, 4), "unique_kv_gbs": round(uniq / (ms * 1e-3) / 1e9, 1),
                                  "kernel": "fwd_bf16_kernel<128,128> packed decode + combine"}}
+
+
+def mask_pairs(kind, S, window_left=-1, block_size=0, prefix_len=0):
+    """Allowed (q, k) pairs of one S x S head, from each mask's definition:
+    causal j <= i; sliding i - W <= j <= i; block-diagonal i // Bs == j // Bs;
+    prefix-LM j < P or j <= i."""
+    if kind == "causal":
+        return S * (S + 1) // 2
+    if kind == "sliding":
+        W = min(window_left, S - 1)
+        return W * (W + 1) // 2 + (S - W) * (W + 1)
+    if kind == "block_diag":
+        nb, r = divmod(S, block_size)
+        return nb * block_size * block_size + r * r
+    if kind == "prefix_lm":
+        P = min(prefix_len, S)
+        return P * P + S * (S + 1) // 2 - P * (P + 1) // 2
+    raise ValueError(kind)
+
+
+def time_fwd_bwd(ga, torch, st, g, spec, lists, reps=10):
+    """Mean ms of attn_fwd and of attn_bwd (CUDA events on the launching
+    stream, after 3 warm-up calls of each)."""
+    B, H, S, Dqk = g["q"].shape
+    Dv = g["v"].shape[-1]
+    dev = g["q"].device
+    ga.build_block_mask(B, H, S, S, spec, lists, stream=st)
+    o = torch.empty(B, H, S, Dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    ws = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, H, S, S, Dqk, Dv), dtype=torch.uint8,
+                     device=dev)
+    fwd = lambda: ga.attn_fwd(g["q"], g["k"], g["v"], 0.0, spec, lists, o=o, lse=lse, stream=st)  # noqa: E731
+    bwd = lambda: ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists,  # noqa: E731
+                              dq=dq, dk=dk, dv=dv, workspace=ws, stream=st)
+    out = []
+    for fn in (fwd, bwd):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / reps)
+    rc = ga.load_library().gbattn_last_device_error(None)
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} in the workload sweep")
+    return out
+
+
+def run_workload_sweep(ga, torch, dev, st, g, rank):
+    """The other mask kinds of the 16K MLA prefill (sliding W = Sk/3,
+    block-diagonal 1024, prefix-LM 2048, each with the relative bias), and the
+    dynamic top-k workload (B=1, H=16, S=8192, top-2048 keys per head by an
+    N(0,1) key bias, with causal) at D = 32 and 64. Not part of the step;
+    FLOPs count the allowed pairs (fwd 2N(Dqk+Dv), bwd 2N(3Dqk+2Dv))."""
+    from block_sparse_attention_tma_gb300.synth import make_inputs
+    P = PREFILL
+    B, H, S, Dqk, Dv = P["B"], P["H"], P["S"], P["Dqk"], P["Dv"]
+    lists = ga.alloc_block_lists(B, H, S, S, P["sparse_m"], P["sparse_n"], device=dev)
+    kinds = {"sliding": dict(kind=ga.SLIDING, window_left=S // 3),
+             "block_diag": dict(kind=ga.BLOCK_DIAG, block_size=1024),
+             "prefix_lm": dict(kind=ga.PREFIX_LM, prefix_len=2048)}
+    masks = {}
+    for name, kw in kinds.items():
+        spec = ga.MaskSpec(rel_bias_slope=P["slope"], **kw)
+        fms, bms = time_fwd_bwd(ga, torch, st, g, spec, lists)
+        n = B * H * mask_pairs(name, S, window_left=kw.get("window_left", -1), block_size=kw.get("block_size", 0),
+                               prefix_len=kw.get("prefix_len", 0))
+        masks[name] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
+                       "fwd_tflops": round(2 * n * (Dqk + Dv) / (fms * 1e-3) / 1e12, 1),
+                       "bwd_tflops": round(2 * n * (3 * Dqk + 2 * Dv) / (bms * 1e-3) / 1e12, 1)}
+    del lists
+    dyn = {}
+    Bd, Hd, Sd, topk = 1, 16, 8192, 2048
+    for D in (32, 64):
+        x = make_inputs(Bd, Hd, Sd, Sd, D, D, "bf16", seed=42 + rank, bias=True)
+        gd = {k: t.to(dev) for k, t in x.items()}
+        spec = ga.MaskSpec(kind=ga.DYNAMIC_TOPK, topk=topk, key_bias=gd["key_bias"])
+        dl = ga.alloc_block_lists(Bd, Hd, Sd, Sd, 128, 128, device=dev)
+        fms, bms = time_fwd_bwd(ga, torch, st, gd, spec, dl)
+        # pairs: every kept key p is seen by the rows p .. S-1
+        kept = torch.topk(x["key_bias"].double(), topk, dim=-1).indices
+        n = int((Sd - kept).sum())
+        dyn[f"d{D}"] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
+                        "fwd_tflops": round(2 * n * 2 * D / (fms * 1e-3) / 1e12, 1),
+                        "bwd_tflops": round(2 * n * 5 * D / (bms * 1e-3) / 1e12, 1)}
+        del gd, dl
+    torch.cuda.empty_cache()
+    return {"mla16k_mask_kinds": dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
+                                                     f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}"),
+            "dynamic_topk": dict(dyn, config=f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) "
+                                             "key bias, with causal; kept keys streamed compacted")}
 
 
 def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=4):
@@ -542,7 +638,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extensions", action="store_true", help="skip the grouped-query paged decode line")
+    ap.add_argument("--no-extensions", action="store_true", help="skip the informational lines (paged GQA decode, mask-kind and dynamic sweeps)")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
     ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "gqa"], default="all",

@@ -23,7 +23,9 @@
 // but removes the fp32 dQ accumulator, its atomics and its memory traffic.
 //
 // Gathered keys (dynamic top-k mask with its kept-key index list): both
-// kernels work on compact tiles of kept keys built by TMA row gathers; dK / dV
+// kernels work on compact tiles of kept keys (the dQ kernel copies each tile's
+// rows with cp.async, the dK/dV kernel its one K / V tile with TMA row
+// gathers); dK / dV
 // rows are written back to the keys' original rows and a small kernel zeroes
 // the rows of the keys outside the keep set. The key-bias gradient
 // (dkey_bias_j = sum_i dS_ij before the softcap factor) is the row sum of

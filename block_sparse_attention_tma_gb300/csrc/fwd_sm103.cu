@@ -27,10 +27,12 @@
 // shared-memory traffic per tile (K + V reads, K + V TMA writes) then fits
 // the time of the two MMAs.
 // Gathered keys (dynamic top-k mask with its kept-key index list): the key
-// tiles are compact tiles of kept keys only, built by TMA row gathers (each
-// producer lane gathers 4 of the 128 rows); the bias and rel-bias terms use
-// each key's original index and the element mask is the prefix of compact
-// keys each row sees. No key outside the keep set is loaded or multiplied.
+// tiles are compact tiles of kept keys only, which the producer warp copies
+// row by row with 16-byte cp.async into the swizzled tile layout (completion
+// tracked on the tile's mbarrier); the bias and rel-bias terms use each key's
+// original index, loaded a tile ahead, and the element mask is the prefix of
+// compact keys each row sees. No key outside the keep set is loaded or
+// multiplied.
 // Packed decode (grouped-query attention, split-KV): the G x Sq query rows of
 // a key/value head (contiguous in Q and O) form the 128-row tiles, so one CTA
 // streams each key/value tile once for the whole group and the tensor cores

@@ -168,7 +168,7 @@ GATHER_CASES = [
 @pytest.mark.parametrize("gather", [True, False])
 @pytest.mark.parametrize("case", GATHER_CASES, ids=lambda c: f"{c[2]}x{c[3]}-d{c[4]}-k{c[5]}")
 def test_dynamic_forward_backward_dkey_bias(case, gather):
-    # gather=True streams only the kept keys (TMA row gathers); gather=False
+    # gather=True streams only the kept keys (compact tiles); gather=False
     # walks the block lists and tests the keep bits: both against the oracle
     B, H, Sq, Sk, D, topk, ex = case
     Dv = 128 if D == 192 else D

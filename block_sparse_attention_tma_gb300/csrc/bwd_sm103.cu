@@ -100,9 +100,10 @@ struct DqCfg {
   static constexpr int QSLAB = 128 * SWQ, NQSLAB = DQK * 2 / SWQ, QTILE = 128 * DQK * 2;
   static constexpr int VSLAB = 128 * SWV, NVSLAB = DV * 2 / SWV, VTILE = 128 * DV * 2;
   // Stages (measured at 8K causal, 16 heads): a third K stage hides the K
-  // load behind dQ; at Dqk = 128 it costs the second V stage, which the
-  // slower cp.async copies of gathered keys cannot spare.
-  static constexpr int KST = DQK == 64 || (DQK == 128 && !GAT) ? 3 : 2;
+  // load behind dQ (Dqk <= 64: shared memory to spare); at Dqk = 128 it costs
+  // the second V stage, which the slower cp.async copies of gathered keys
+  // cannot spare.
+  static constexpr int KST = DQK <= 64 || (DQK == 128 && !GAT) ? 3 : 2;
   static constexpr int VST = DQK >= 192 || (DQK == 128 && !GAT) ? 1 : 2;
   static constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 448;
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
@@ -366,19 +367,15 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
     int kv0;
     bool masked;
+    // gathered keys: original index -> bias loads run ahead (a dependent pair
+    // per tile); otherwise the tile's time hides the one bias load
+    auto kt = [&]() {
+      if constexpr (GAT) return key_terms<GAT>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
+      else return KeyTermsDirect{kb, Skv, cb + lane, p.mask.slope};
+    }();
     while (ok && it.next(&kv0, &masked)) {
       float* ctw = colterm + (sw * 2 + (n & 1)) * 64;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int jj = kv0 + cb + e * 32 + lane;
-        float c = 0.f;
-        if (jj < Skv) {
-          int jo = jj;  // original key index
-          if constexpr (GAT) jo = __ldg(pos_h + jj);
-          c = ((kb ? __ldg(kb + jo) : 0.f) - p.mask.slope * (float)jo) * kLog2e;
-        }
-        ctw[e * 32 + lane] = c;
-      }
+      kt.emit(kv0, ctw);
       __syncwarp();
       uint32_t kw[2] = {0xffffffffu, 0xffffffffu};
       if (keep) {

@@ -455,61 +455,13 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
     int kv0;
     bool masked;
-    // With a key bias its loads run ahead of the tiles: the original key
-    // indices of tile n + 2 and the bias values of tile n + 1 are loaded
-    // while tile n is processed (-1: no key).
-    auto ahead = it;
-    auto key_of = [&](int st, int e) -> int {
-      const int j = st + cb + e * 32 + lane;
-      if (j >= Skv) return -1;
-      if constexpr (GAT) return __ldg(pos_h + j);
-      return j;
-    };
-    int jo_cur[2] = {-1, -1}, jo_nx[2] = {-1, -1};
-    float bv_cur[2] = {0.f, 0.f};
-    if (kb && ok) {
-      int st;
-      bool mk;
-      if (ahead.next(&st, &mk)) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) jo_cur[e] = key_of(st, e);
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) bv_cur[e] = jo_cur[e] >= 0 ? __ldg(kb + jo_cur[e]) : 0.f;
-      if (ahead.next(&st, &mk)) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) jo_nx[e] = key_of(st, e);
-      }
-    }
+    auto kt = key_terms<GAT>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
     while (ok && it.next(&kv0, &masked)) {
       const int sb = n & 1;
       // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
       // columns; each warp keeps its own copy, so only a warp sync is needed
       float* ctw = colterm + (sw * 2 + sb) * 64;
-      if (kb) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          ctw[e * 32 + lane] = jo_cur[e] >= 0 ? (bv_cur[e] - p.mask.slope * (float)jo_cur[e]) * kLog2e : 0.f;
-        int st;
-        bool mk;
-        int jo_n2[2] = {-1, -1};
-        if (ahead.next(&st, &mk)) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) jo_n2[e] = key_of(st, e);
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          bv_cur[e] = jo_nx[e] >= 0 ? __ldg(kb + jo_nx[e]) : 0.f;
-          jo_cur[e] = jo_nx[e];
-          jo_nx[e] = jo_n2[e];
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int jo = key_of(kv0, e);  // original key index
-          ctw[e * 32 + lane] = jo >= 0 ? -p.mask.slope * (float)jo * kLog2e : 0.f;
-        }
-      }
+      kt.emit(kv0, ctw);
       __syncwarp();
       ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {

@@ -322,4 +322,97 @@ __device__ __forceinline__ TileSeq<SlotFn> tile_seq(SlotFn slot, const uint16_t*
   return TileSeq<SlotFn>{list, count, count <= cap ? 1 : 0, nslots, 0, 0, slot};
 }
 
+// Per-key score terms (key bias_j - slope * j) * log2(e) of one warp's 64
+// key columns [cb, cb + 64) of each visited tile, j the key's original index
+// (pos[] of the compact index for gathered keys). With a key bias the loads
+// run ahead of the tiles: while tile n is processed, the original indices of
+// tile n + 2 and the bias values of tile n + 1 are loaded, so the dependent
+// index -> bias loads never stall the caller. `seq` must be a copy of the
+// caller's tile sequence taken before its first next().
+template <bool GAT, class Seq>
+struct KeyTerms {
+  Seq ahead;
+  const float* kb;   // key bias of this head, or nullptr
+  const int32_t* pos;  // gathered keys: original index of each compact key
+  int skv, col0;       // streamed key extent; col0 = cb + lane
+  float slope;
+  int jo_cur[2], jo_nx[2];
+  float bv_cur[2];
+
+  __device__ __forceinline__ int key_of(int st, int e) const {
+    const int j = st + col0 + e * 32;
+    if (j >= skv) return -1;
+    if constexpr (GAT) return __ldg(pos + j);
+    return j;
+  }
+  __device__ __forceinline__ void start() {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      jo_cur[e] = jo_nx[e] = -1;
+      bv_cur[e] = 0.f;
+    }
+    if (!kb) return;
+    int st;
+    bool mk;
+    if (ahead.next(&st, &mk)) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) jo_cur[e] = key_of(st, e);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) bv_cur[e] = jo_cur[e] >= 0 ? __ldg(kb + jo_cur[e]) : 0.f;
+    if (ahead.next(&st, &mk)) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) jo_nx[e] = key_of(st, e);
+    }
+  }
+  // Writes this lane's two terms of the tile starting at compact key kv0
+  // (the tile the caller's sequence just returned) to ct[lane], ct[32 + lane].
+  __device__ __forceinline__ void emit(int kv0, float* ct) {
+    if (kb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        ct[e * 32 + (col0 & 31)] = jo_cur[e] >= 0 ? (bv_cur[e] - slope * (float)jo_cur[e]) * kLog2e : 0.f;
+      int st;
+      bool mk;
+      int jo_n2[2] = {-1, -1};
+      if (ahead.next(&st, &mk)) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) jo_n2[e] = key_of(st, e);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        bv_cur[e] = jo_nx[e] >= 0 ? __ldg(kb + jo_nx[e]) : 0.f;
+        jo_cur[e] = jo_nx[e];
+        jo_nx[e] = jo_n2[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int jo = key_of(kv0, e);
+        ct[e * 32 + (col0 & 31)] = jo >= 0 ? -slope * (float)jo * kLog2e : 0.f;
+      }
+    }
+  }
+};
+// The same terms loaded when each tile starts (no look-ahead state).
+struct KeyTermsDirect {
+  const float* kb;
+  int skv, col0;
+  float slope;
+  __device__ __forceinline__ void emit(int kv0, float* ct) const {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = kv0 + col0 + e * 32;
+      ct[e * 32 + (col0 & 31)] = j < skv ? ((kb ? __ldg(kb + j) : 0.f) - slope * (float)j) * kLog2e : 0.f;
+    }
+  }
+};
+template <bool GAT, class Seq>
+__device__ __forceinline__ KeyTerms<GAT, Seq> key_terms(const Seq& seq, const float* kb, const int32_t* pos, int skv,
+                                                       int col0, float slope) {
+  KeyTerms<GAT, Seq> t{seq, kb, pos, skv, col0, slope, {-1, -1}, {-1, -1}, {0.f, 0.f}};
+  t.start();
+  return t;
+}
+
 }  // namespace gb

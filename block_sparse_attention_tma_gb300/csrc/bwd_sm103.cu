@@ -536,6 +536,38 @@ static int launch_dq(const BwdParams& prm, const Shape& s, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+// A second stream of this host thread on the current device, with its fork /
+// join events: the dQ grid runs on it beside the dK/dV grid (the two read the
+// same inputs and write different outputs), so each grid's CTAs fill the
+// other's last wave. Both grids take a whole SM per CTA, so they interleave
+// rather than share SMs. Created on first use and kept for the thread's
+// lifetime; nullptr (run both on the caller's stream) if creation fails.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static const SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream ss[kMaxDevices];
+  thread_local bool failed[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  SideStream& t = ss[dev];
+  if (!t.stream && !failed[dev]) {
+    if (cudaStreamCreateWithFlags(&t.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&t.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&t.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      failed[dev] = true;
+      t = SideStream{};
+    }
+  }
+  return t.stream ? &t : nullptr;
+}
+
 template <int DQK, int DV>
 static int launch_dq_cap(const BwdParams& prm, const Shape& s, bool cap, cudaStream_t st) {
   if (prm.gather)
@@ -630,16 +662,30 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   }
   const bool cap = m.softcap > 0.f;
   const int nkt = (prm.Skv + 127) / 128;  // key tiles (compact tiles when gathered)
+  // dQ on the side stream, forked after the preprocess and joined back
+  const SideStream* side = nkt > 0 ? side_stream() : nullptr;
+  if (side && (cudaEventRecord(side->fork, st) != cudaSuccess ||
+               cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)) {
+    cudaGetLastError();
+    side = nullptr;
+  }
+  const cudaStream_t sq = side ? side->stream : st;
+  int rc = GBATTN_OK;
   if (nkt > 0) {
     const int key_mode = m.gather ? 1 : (prm.mask.table ? 2 : 0);
-    const int rc = dkdv_launch(prm, s.Dqk, s.Dv, cap, key_mode, dkey_bias != nullptr, nkt * s.B * s.Hkv, st);
-    if (rc != GBATTN_OK) return rc;
+    rc = dkdv_launch(prm, s.Dqk, s.Dv, cap, key_mode, dkey_bias != nullptr, nkt * s.B * s.Hkv, st);
   }
-  if (s.Dqk == 32 && s.Dv == 32) return launch_dq_cap<32, 32>(prm, s, cap, st);
-  if (s.Dqk == 64 && s.Dv == 64) return launch_dq_cap<64, 64>(prm, s, cap, st);
-  if (s.Dqk == 128 && s.Dv == 128) return launch_dq_cap<128, 128>(prm, s, cap, st);
-  if (s.Dqk == 192 && s.Dv == 128) return launch_dq_cap<192, 128>(prm, s, cap, st);
-  return GBATTN_ERR_UNSUPPORTED;
+  if (rc == GBATTN_OK) {
+    if (s.Dqk == 32 && s.Dv == 32) rc = launch_dq_cap<32, 32>(prm, s, cap, sq);
+    else if (s.Dqk == 64 && s.Dv == 64) rc = launch_dq_cap<64, 64>(prm, s, cap, sq);
+    else if (s.Dqk == 128 && s.Dv == 128) rc = launch_dq_cap<128, 128>(prm, s, cap, sq);
+    else if (s.Dqk == 192 && s.Dv == 128) rc = launch_dq_cap<192, 128>(prm, s, cap, sq);
+    else rc = GBATTN_ERR_UNSUPPORTED;
+  }
+  if (side && (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+               cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess))
+    return GBATTN_ERR_CUDA;
+  return rc;
 }
 
 GB_DEFINE_ERROR_READER(bwd_take_error)

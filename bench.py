@@ -419,8 +419,9 @@ def time_fwd_bwd(ga, torch, st, g, spec, lists, reps=10):
 
 def run_workload_sweep(ga, torch, dev, st, g, rank):
     """The other mask kinds of the 16K MLA prefill (sliding W = Sk/3,
-    block-diagonal 1024, prefix-LM 2048, each with the relative bias), and the
-    dynamic top-k workload (B=1, H=16, S=8192, top-2048 keys per head by an
+    block-diagonal 1024, prefix-LM 2048, each with the relative bias), the
+    dense masked workload (B=2, H=8, S=2048, D=64: causal, sliding W=512), and
+    the dynamic top-k workload (B=1, H=16, S=8192, top-2048 keys per head by an
     N(0,1) key bias, with causal) at D = 32 and 64. Not part of the step;
     FLOPs count the allowed pairs (fwd 2N(Dqk+Dv), bwd 2N(3Dqk+2Dv))."""
     from block_sparse_attention_tma_gb300.synth import make_inputs
@@ -440,6 +441,20 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
                        "fwd_tflops": round(2 * n * (Dqk + Dv) / (fms * 1e-3) / 1e12, 1),
                        "bwd_tflops": round(2 * n * (3 * Dqk + 2 * Dv) / (bms * 1e-3) / 1e12, 1)}
     del lists
+    # dense masked workload: B=2, H=8, S=2048, D=64, causal and causal sliding W=512
+    Bd, Hd, Sd, Dd = 2, 8, 2048, 64
+    x = make_inputs(Bd, Hd, Sd, Sd, Dd, Dd, "bf16", seed=42 + rank)
+    gd = {k: t.to(dev) for k, t in x.items()}
+    dl = ga.alloc_block_lists(Bd, Hd, Sd, Sd, 128, 128, device=dev)
+    dense = {}
+    for name, kw, kind in (("causal", dict(kind=ga.CAUSAL), "causal"),
+                           ("sliding_w512", dict(kind=ga.SLIDING, window_left=512), "sliding")):
+        fms, bms = time_fwd_bwd(ga, torch, st, gd, ga.MaskSpec(**kw), dl)
+        n = Bd * Hd * mask_pairs(kind, Sd, window_left=kw.get("window_left", -1))
+        dense[name] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
+                       "fwd_tflops": round(2 * n * 2 * Dd / (fms * 1e-3) / 1e12, 1),
+                       "bwd_tflops": round(2 * n * 5 * Dd / (bms * 1e-3) / 1e12, 1)}
+    del gd, dl
     dyn = {}
     Bd, Hd, Sd, topk = 1, 16, 8192, 2048
     for D in (32, 64):
@@ -456,7 +471,8 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
                         "bwd_tflops": round(2 * n * 5 * D / (bms * 1e-3) / 1e12, 1)}
         del gd, dl
     torch.cuda.empty_cache()
-    return {"mla16k_mask_kinds": dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
+    return {"dense2k": dict(dense, config=f"B={Bd} H={Hd} Sq=Sk={Sd} D={Dd} bf16, kernel tiles 128x128"),
+            "mla16k_mask_kinds": dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
                                                      f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}"),
             "dynamic_topk": dict(dyn, config=f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) "
                                              "key bias, with causal; kept keys streamed compacted")}

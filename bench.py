@@ -454,6 +454,7 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
         dense[name] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
                        "fwd_tflops": round(2 * n * 2 * Dd / (fms * 1e-3) / 1e12, 1),
                        "bwd_tflops": round(2 * n * 5 * Dd / (bms * 1e-3) / 1e12, 1)}
+    dense["config"] = f"B={Bd} H={Hd} Sq=Sk={Sd} D={Dd} bf16, kernel tiles 128x128"
     del gd, dl
     dyn = {}
     Bd, Hd, Sd, topk = 1, 16, 8192, 2048
@@ -471,7 +472,7 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
                         "bwd_tflops": round(2 * n * 5 * D / (bms * 1e-3) / 1e12, 1)}
         del gd, dl
     torch.cuda.empty_cache()
-    return {"dense2k": dict(dense, config=f"B={Bd} H={Hd} Sq=Sk={Sd} D={Dd} bf16, kernel tiles 128x128"),
+    return {"dense2k": dense,
             "mla16k_mask_kinds": dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
                                                      f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}"),
             "dynamic_topk": dict(dyn, config=f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) "

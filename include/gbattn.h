@@ -204,6 +204,13 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int Sq, int Sk, int Dqk
  * apply: the bias is added after the cap). The dynamic keep set is held fixed
  * (it changes only where two biases cross). Written for every key, 0 for keys
  * no query sees; also defined when key_bias is NULL (the gradient at zero).
+ * Stream: stream-ordered on `stream` like every call. The bf16 path runs its
+ * query-parallel (dQ) grid on a second stream that the library creates once
+ * per calling host thread and device, forked from `stream` after the
+ * preprocess (event record / wait) and joined back into `stream` before the
+ * call returns, so work issued on `stream` afterwards sees every gradient and
+ * CUDA graph capture on `stream` captures both grids. If that stream cannot be
+ * created, both grids run on `stream`.
  */
 int attn_bwd(int dtype, int B, int H, int Hkv, int Sq, int Sk, int Dqk, int Dv,
              const void* q, const void* k, const void* v, const void* o,

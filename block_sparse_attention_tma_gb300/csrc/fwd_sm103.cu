@@ -38,6 +38,8 @@
 // streams each key/value tile once for the whole group and the tensor cores
 // take the score and output products; a CTA covers one split of the keys and
 // writes a normalised partial output and LSE that the split combine merges.
+// Softmax warps whose rows hold no query row of the group only keep the
+// barriers in step.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+Dv), Q [384, 384+Dqk/2).
 #include "kernels.h"
 #include "mask.cuh"
@@ -413,6 +415,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     // head when rows are packed), whether it exists, and its output row id
     const int i = PK ? (q0 + row) % p.Sq : q0 + row;
     const bool valid = PK ? q0 + row < p.pk_R : i < p.Sq;
+    const bool wact = !PK || q0 + quarter * 32 < p.pk_R;  // some row of this warp exists
     const size_t orow_id = PK ? (size_t)row_base + q0 + row : (size_t)bh * p.Sq + i;
     const int cb = grp * 64;       // first S column of this thread
     constexpr int DVH = DV / 2;    // O columns of this thread
@@ -458,6 +461,17 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     auto kt = key_terms<GAT>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
     while (ok && it.next(&kv0, &masked)) {
       const int sb = n & 1;
+      if constexpr (PK) {
+        // packed decode: a warp whose 32 rows hold no query row of the group
+        // only keeps the barriers in step (S of this tile is computed, so P
+        // of the tile two before is consumed and the arrival cannot run ahead)
+        if (!wact) {
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag)))) break;
+          mbar_arrive(p_full + sb);
+          ++n;
+          continue;
+        }
+      }
       // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
       // columns; each warp keeps its own copy, so only a warp sync is needed
       float* ctw = colterm + (sw * 2 + sb) * 64;

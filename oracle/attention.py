@@ -27,7 +27,7 @@ Sources (titles of the pages the method is taken from):
          softmax merge algebra (m_new = max(m1, m2); l and o rescaled by
          exp(m - m_new)); fp32 tolerance atol = rtol = 1e-4.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
   * Sq != Sk aligns the causal diagonal bottom-right: delta = Sk - Sq.
   * sliding window keeps keys j with 0 <= (i + delta) - j <= window_left
     (window_left + 1 keys, self included); window_left < 0 = unbounded.

@@ -109,6 +109,72 @@ def _check(rc: int, what: str):
         raise GbattnError(rc, what)
 
 
+def _check_tensors(what: str, specs, device_of: Optional[torch.Tensor] = None):
+    """Checks the tensors of one call before any pointer crosses the C ABI,
+    which takes raw pointers and derives sizes from the shapes given to it.
+
+    specs: (name, tensor or None, expected shape (None = any, an int entry of
+    None = any size there), allowed dtypes). Every given tensor must be
+    contiguous, have the expected shape and dtype, and sit on the same CUDA
+    device as `device_of` (default: the first given tensor). Raises ValueError.
+    """
+    ref = device_of
+    for name, t, shape, dtypes in specs:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{what}: {name} must be a torch.Tensor")
+        if shape is not None:
+            ok = t.dim() == len(shape) and all(e is None or e == d for e, d in zip(shape, t.shape))
+            if not ok:
+                want = "[" + ", ".join("*" if e is None else str(e) for e in shape) + "]"
+                raise ValueError(f"{what}: {name} has shape {list(t.shape)}, expected {want}")
+        if dtypes is not None and t.dtype not in dtypes:
+            raise ValueError(f"{what}: {name} has dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: {name} must be contiguous")
+        if ref is None:
+            ref = t
+    for name, t, _, _ in specs:
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"{what}: {name} must be on a CUDA device (is on {t.device})")
+        if t.device != ref.device:
+            raise ValueError(f"{what}: {name} is on {t.device}, the other tensors on {ref.device}")
+
+
+_FLOAT = (torch.bfloat16, torch.float32)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+
+
+def _qkv_dims(what, q, k, v):
+    """Reads B, H, Hkv, Sq, Sk, Dqk, Dv off the q / k / v trio and returns
+    them with the trio's check specs (for one _check_tensors call, so that
+    every shape is checked before any device)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{what}: {name} must be a 4-D tensor [B, heads, S, D]")
+    B, H, Sq, Dqk = q.shape
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    if q.dtype not in _FLOAT:
+        raise ValueError(f"{what}: q has dtype {q.dtype}, expected bfloat16 or float32")
+    specs = [("q", q, None, None), ("k", k, (B, Hkv, Sk, Dqk), (q.dtype,)), ("v", v, (B, Hkv, Sk, Dv), (q.dtype,))]
+    return (B, H, Hkv, Sq, Sk, Dqk, Dv), specs
+
+
+def _mask_tensors(what, mask, B, H, Sq, Sk):
+    if mask is None:
+        return []
+    nw = (Sk + 31) // 32
+    out = [("mask.key_bias", mask.key_bias, (B, H, Sk), _F32)]
+    if mask.table is not None:
+        shape = (Sq, nw) if mask.table.dim() == 2 else (B, H, Sq, nw)
+        out.append(("mask.table", mask.table, shape, _I32))
+    return out
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -168,6 +234,12 @@ class BlockLists:
         return b
 
 
+def _list_tensors(lists: Optional[BlockLists]):
+    if lists is None:
+        return []
+    return [(f"lists.{n}", t, None, _I32) for n, t in lists.tensors.items()]
+
+
 def alloc_block_lists(B, H, Sq, Sk, sparse_m, sparse_n, device="cuda", gather=True) -> BlockLists:
     """Allocates every list array. gather=True also allocates the dynamic
     mask's kept-key index list, with which the bf16 kernels stream only the
@@ -189,6 +261,7 @@ def alloc_block_lists(B, H, Sq, Sk, sparse_m, sparse_n, device="cuda", gather=Tr
 
 def build_block_mask(B, H, Sq, Sk, mask: MaskSpec, lists: BlockLists, stream=None) -> BlockLists:
     lib = load_library()
+    _check_tensors("build_block_mask", _mask_tensors("build_block_mask", mask, B, H, Sq, Sk) + _list_tensors(lists))
     cm, cb = mask.c(), lists.c()
     _check(lib.build_block_mask(B, H, Sq, Sk, ctypes.byref(cm), ctypes.byref(cb), _stream(stream)),
            "build_block_mask")
@@ -200,8 +273,9 @@ def attn_fwd(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, lists: Optiona
     """q [B, H, Sq, Dqk]; k, v [B, Hkv, Sk, D] (Hkv divides H: grouped-query
     attention when Hkv < H)."""
     lib = load_library()
-    B, H, Sq, Dqk = q.shape
-    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    (B, H, Hkv, Sq, Sk, Dqk, Dv), qkv = _qkv_dims("attn_fwd", q, k, v)
+    _check_tensors("attn_fwd", qkv + [("o", o, (B, H, Sq, Dv), (q.dtype,)), ("lse", lse, (B, H, Sq), _F32)]
+                   + _mask_tensors("attn_fwd", mask, B, H, Sq, Sk) + _list_tensors(lists), device_of=q)
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
@@ -225,8 +299,14 @@ def attn_bwd(q, k, v, o, dout, lse, scale=0.0, mask: Optional[MaskSpec] = None,
     """Returns (dq, dk, dv); when dkey_bias (fp32 [B, H, Sk] on the GPU) is
     given it receives the gradient of the key bias."""
     lib = load_library()
-    B, H, Sq, Dqk = q.shape
-    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    (B, H, Hkv, Sq, Sk, Dqk, Dv), qkv = _qkv_dims("attn_bwd", q, k, v)
+    _check_tensors("attn_bwd", qkv + [("o", o, (B, H, Sq, Dv), (q.dtype,)), ("dout", dout, (B, H, Sq, Dv), (q.dtype,)),
+                                ("lse", lse, (B, H, Sq), _F32), ("dq", dq, (B, H, Sq, Dqk), (q.dtype,)),
+                                ("dk", dk, (B, Hkv, Sk, Dqk), (q.dtype,)), ("dv", dv, (B, Hkv, Sk, Dv), (q.dtype,)),
+                                ("dkey_bias", dkey_bias, (B, H, Sk), _F32), ("workspace", workspace, None, None)]
+                   + _mask_tensors("attn_bwd", mask, B, H, Sq, Sk) + _list_tensors(lists), device_of=q)
+    if o is None or dout is None or lse is None:
+        raise ValueError("attn_bwd: o, dout and lse are required")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -251,8 +331,9 @@ def attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits) -> int:
 def attn_fwd_splitkv(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None, num_splits=1, o=None, lse=None,
                      workspace=None, stream=None):
     lib = load_library()
-    B, H, Sq, Dqk = q.shape
-    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    (B, H, Hkv, Sq, Sk, Dqk, Dv), qkv = _qkv_dims("attn_fwd_splitkv", q, k, v)
+    _check_tensors("attn_fwd_splitkv", qkv + [("o", o, (B, H, Sq, Dv), (q.dtype,)), ("lse", lse, (B, H, Sq), _F32),
+                                        ("workspace", workspace, None, None)], device_of=q)
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
@@ -275,9 +356,18 @@ def attn_fwd_splitkv_paged(q, k_cache, v_cache, page_table, seqlens_k, scale=0.0
     page_size, D] bf16, page_table [B, max_pages] int32 and seqlens_k [B]
     int32 on the GPU."""
     lib = load_library()
+    what = "attn_fwd_splitkv_paged"
+    for name, t, nd in (("q", q, 4), ("k_cache", k_cache, 4), ("v_cache", v_cache, 4), ("page_table", page_table, 2),
+                        ("seqlens_k", seqlens_k, 1)):
+        if not isinstance(t, torch.Tensor) or t.dim() != nd:
+            raise ValueError(f"{what}: {name} must be a {nd}-D tensor")
     B, H, Sq, Dqk = q.shape
     num_pages, Hkv, page_size, Dv = v_cache.shape
     max_pages = page_table.shape[1]
+    _check_tensors(what, [("q", q, None, _FLOAT), ("k_cache", k_cache, (num_pages, Hkv, page_size, Dqk), (q.dtype,)),
+                          ("v_cache", v_cache, None, (q.dtype,)), ("page_table", page_table, (B, max_pages), _I32),
+                          ("seqlens_k", seqlens_k, (B,), _I32), ("o", o, (B, H, Sq, Dv), (q.dtype,)),
+                          ("lse", lse, (B, H, Sq), _F32), ("workspace", workspace, None, None)], device_of=q)
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:
@@ -308,8 +398,9 @@ def attn_fwd_splitkv_noalloc(q, k, v, scale=0.0, mask: Optional[MaskSpec] = None
     work overlaps race on that array. Pass preallocated o / lse to allocate
     nothing here either."""
     lib = load_library()
-    B, H, Sq, Dqk = q.shape
-    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    (B, H, Hkv, Sq, Sk, Dqk, Dv), qkv = _qkv_dims("attn_fwd_splitkv_noalloc", q, k, v)
+    _check_tensors("attn_fwd_splitkv_noalloc", qkv + [("o", o, (B, H, Sq, Dv), (q.dtype,)), ("lse", lse, (B, H, Sq), _F32)],
+                   device_of=q)
     if o is None:
         o = torch.empty(B, H, Sq, Dv, dtype=q.dtype, device=q.device)
     if lse is None:

@@ -518,20 +518,10 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
 }
 
 // ------------------------------------------------------------------ host
-template <typename K>
-static int set_smem_once(K kern, int bytes, bool* flag) {
-  if (!*flag) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    *flag = true;
-  }
-  return GBATTN_OK;
-}
-
 template <int DQK, int DV, bool CAP, bool GAT>
 static int launch_dq(const BwdParams& prm, const Shape& s, cudaStream_t st) {
-  static bool attr = false;
-  if (set_smem_once(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV, GAT>::SMEM, &attr)) return GBATTN_ERR_CUDA;
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV, GAT>::SMEM, attr)) return GBATTN_ERR_CUDA;
   dq_kernel<DQK, DV, CAP, GAT><<<((s.Sq + 127) / 128) * s.B * s.H, 320, DqCfg<DQK, DV, GAT>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }

@@ -537,13 +537,8 @@ static int launch_group(const DecParams& prm, cudaStream_t st) {
   constexpr int CHB = kDecChunk * D * 2;
   constexpr int RC = 4 * RPG;
   constexpr int SMEM = 128 + 2 * kDecStages * CHB + 2 * kDecStages * 8 + kDecWarps * RC * (D + 2) * 4 + 16;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(splitkv_group_kernel<D, RPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
-        cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(splitkv_group_kernel<D, RPG>, SMEM, attr)) return GBATTN_ERR_CUDA;
   const int R = prm.G * prm.Sq;
   const int nrch = (R + RC - 1) / RC;
   const long long grid = (long long)(prm.BH / prm.G) * nrch * prm.nsplit;
@@ -556,12 +551,8 @@ template <int D>
 static int launch_dec(const DecParams& prm, cudaStream_t st) {
   constexpr int CHB = kDecChunk * D * 2;
   constexpr int SMEM = 128 + 2 * kDecStages * CHB + 2 * kDecStages * 8 + kDecWarps * (D + 2) * 4 + 16;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(splitkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(splitkv_kernel<D>, SMEM, attr)) return GBATTN_ERR_CUDA;
   const int R = prm.G * prm.Sq;  // query rows per key/value head
   if (prm.G > 1 && R >= 4) {
     // query heads share key/value heads: one CTA streams each chunk for up to 8 (D=128) or 16 (D=64) rows

@@ -602,20 +602,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <typename K>
-static int set_smem_once(K kern, int bytes, bool* flag) {
-  if (!*flag) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    *flag = true;
-  }
-  return GBATTN_OK;
-}
-
 template <int DQK, int DV, bool CAP, int KM, bool DB>
 static int launch_one(const BwdParams& prm, int grid, cudaStream_t st) {
-  static bool attr = false;
-  if (set_smem_once(dkdv_kernel<DQK, DV, CAP, KM, DB>, DkdvCfg<DQK, DV>::SMEM, &attr)) return GBATTN_ERR_CUDA;
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(dkdv_kernel<DQK, DV, CAP, KM, DB>, DkdvCfg<DQK, DV>::SMEM, attr)) return GBATTN_ERR_CUDA;
   dkdv_kernel<DQK, DV, CAP, KM, DB><<<grid, DkdvCfg<DQK, DV>::THREADS, DkdvCfg<DQK, DV>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }

@@ -673,12 +673,8 @@ template <int DQK, int DV, bool CAP, bool GAT>
 static int launch_fwd(const FwdParams& prm, int grid, cudaStream_t st) {
   using C = FwdCfg<DQK, DV>;
   auto kern = fwd_bf16_kernel<DQK, DV, CAP, GAT>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(kern, C::SMEM, attr)) return GBATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
@@ -756,12 +752,8 @@ template <int D>
 static int launch_packed(const FwdParams& prm, int grid, cudaStream_t st) {
   using C = FwdCfg<D, D>;
   auto kern = fwd_bf16_kernel<D, D, false, false, true>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-      return GBATTN_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (ensure_smem(kern, C::SMEM, attr)) return GBATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }

@@ -7,9 +7,33 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/gbattn.h"
 
 namespace gb {
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device. The attribute belongs to the function in one device's context, so
+// it is set once per device ordinal: `done` holds one bit per device (< 64;
+// higher ordinals set it on every launch). Two host threads may both set it
+// the first time, which is harmless.
+template <typename K>
+inline int ensure_smem(K kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GBATTN_ERR_CUDA;
+  }
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return GBATTN_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return GBATTN_ERR_CUDA;
+  }
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return GBATTN_OK;
+}
 
 // Largest number of query heads per key/value head (GQA group) the
 // tensor-core backward accepts.

@@ -280,9 +280,16 @@ int attn_fwd_splitkv_paged(int dtype, int B, int H, int Hkv, int Sq, int Dqk, in
  * They cannot provide the split workspace attn_fwd_splitkv asks for. This
  * entry point takes the same arguments minus the workspace and keeps the split
  * partials in a scratch array that the library holds in device memory: a
- * file-scope array of GBATTN_NOALLOC_SCRATCH_BYTES bytes, reserved on every GPU
- * that loads the library until the process exits. It calls no cudaMalloc,
- * cudaFree or allocating library routine.
+ * file-scope array of GBATTN_NOALLOC_SCRATCH_BYTES bytes, held on every GPU
+ * that loads the library's decode code until the process exits. It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - When the array's memory is committed: the CUDA runtime loads a device
+ *     code module on a device when it is first used there (CUDA's default
+ *     lazy module loading), and the array comes into being with its module.
+ *     So the first call on each device (or the first split-KV call of any
+ *     kind) can itself need 16 MiB of free device memory and fail with
+ *     GBATTN_ERR_CUDA if there is none. Make one warm-up call on each device
+ *     before your engine's allocator reserves the rest of the memory.
  *   - Limit: attn_fwd_splitkv_workspace_bytes(B, H, Sq, Dv, num_splits) must
  *     not exceed GBATTN_NOALLOC_SCRATCH_BYTES; larger problems are rejected
  *     with GBATTN_ERR_WORKSPACE (use attn_fwd_splitkv with your own workspace).

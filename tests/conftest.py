@@ -25,3 +25,13 @@ def read_golden(name):
                 continue
             rows.append(line.split())
     return rows
+
+
+def golden_setup():
+    """The [FSA] test set-up fixture as a dict: splits and head_dims as int
+    lists, seed as an int."""
+    out = {}
+    for row in read_golden("fsa_pr148_test_setup.txt"):
+        vals = [int(x) for x in row[1:]]
+        out[row[0]] = vals if len(vals) > 1 else vals[0]
+    return out

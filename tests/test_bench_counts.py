@@ -30,3 +30,23 @@ def test_dynamic_pair_count_matches_oracle():
     keep = orc.topk_keep(bias.double().numpy(), topk)
     m = orc.allowed(orc.DYNAMIC_TOPK, S, S, np.arange(S), np.arange(S), keep=keep)
     assert count == int(m.sum())
+
+
+def test_fsa_test_setup_fixture_drives_the_seeds_and_splits():
+    """The [FSA] Testing section's set-up (tests/golden/fsa_pr148_test_setup.txt):
+    split counts 1/2/4/8/16 and seed 42. The split-KV parity tests take their
+    split counts from the fixture; the bench's decode workload and the seeded
+    input generator's default must agree with it."""
+    import inspect
+
+    import bench
+    from block_sparse_attention_tma_gb300 import synth
+    from conftest import golden_setup
+
+    g = golden_setup()
+    assert g["splits"] == [1, 2, 4, 8, 16]
+    assert tuple(g["splits"]) == bench.DECODE["splits"]
+    assert inspect.signature(synth.make_inputs).parameters["seed"].default == g["seed"]
+    assert inspect.signature(synth.make_device_inputs).parameters["seed"].default == g["seed"]
+    # the head dims the bf16 tensor-core path supports are among the page's
+    assert {32, 64, 128, 192} <= set(g["head_dims"])

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import block_sparse_attention_tma_gb300 as ga
-from conftest import read_golden
+from conftest import golden_setup, read_golden
 from helpers import Case, check_dbias, check_grad, check_lse, check_out, f64, assert_no_device_error, make_table
 from oracle import attention as orc
 
@@ -433,7 +433,8 @@ def test_fp32_key_bias_gradient(kind, ex):
 
 
 # ------------------------------------------------------------------ a6-a7 split-KV decode
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 16])
+# split counts of the [FSA] test set-up (tests/golden/fsa_pr148_test_setup.txt)
+@pytest.mark.parametrize("n", golden_setup()["splits"])
 @pytest.mark.parametrize("D,Sq,Sk,kind", [(128, 1, 3000, "none"), (64, 3, 1100, "causal"), (128, 2, 77, "none")])
 def test_splitkv_decode(n, D, Sq, Sk, kind):
     c = Case(2, 3, Sq, Sk, D, D, kind, lists=False, sparse=None)

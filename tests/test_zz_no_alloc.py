@@ -4,10 +4,14 @@ belongs to a host engine's allocator, or a decode loop that must never call
 cudaMalloc once it runs). Its split partials live in the library's own static
 scratch array instead of a caller workspace.
 
-The GPU test calls it through the C ABI twice in a row, with different inputs
-and split counts, and checks each result against attn_fwd_splitkv given its
-own workspace, within the bf16 tolerance the parity tests use. The file is
-named to be collected last, and it works in a fresh process too.
+The GPU tests call it through the C ABI twice in a row per case, with
+different inputs and split counts, and check each result against
+attn_fwd_splitkv given its own workspace (the same kernels: bit for bit) and
+against the fp64 oracle within the bf16 tolerance the parity tests use. The
+cases cover the per-row CUDA-core decode (Hkv = H), the packed tensor-core
+decode of grouped query heads (Hkv < H, whose split partials then also live
+in the static scratch) and a causal decode with several query rows. The file
+is named to be collected last, and it works in a fresh process too.
 """
 import ctypes
 
@@ -16,22 +20,28 @@ import pytest
 import torch
 
 from block_sparse_attention_tma_gb300 import binding as bd
+from block_sparse_attention_tma_gb300.synth import make_inputs
+from oracle import attention as orc
 
 SCRATCH = 16 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 
-def _call_noalloc(q, k, v, n, o, lse):
+def _mask(causal):
+    return bd.MaskSpec(kind=bd.CAUSAL if causal else bd.NONE).c()
+
+
+def _call_noalloc(q, k, v, n, o, lse, causal):
     lib = bd.load_library()
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
-    m = bd.MaskSpec().c()
+    m = _mask(causal)
     return lib.attn_fwd_splitkv_noalloc(bd.BF16, B, H, k.shape[1], Sq, Sk, D, D, q.data_ptr(), k.data_ptr(),
                                         v.data_ptr(), 0.0,
                                         ctypes.byref(m), n, o.data_ptr(), lse.data_ptr(),
                                         torch.cuda.current_stream().cuda_stream)
 
 
-def _call_with_workspace(q, k, v, n):
+def _call_with_workspace(q, k, v, n, causal):
     lib = bd.load_library()
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
@@ -39,7 +49,7 @@ def _call_with_workspace(q, k, v, n):
     lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     need = lib.attn_fwd_splitkv_workspace_bytes(B, H, Sq, D, n)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    m = bd.MaskSpec().c()
+    m = _mask(causal)
     rc = lib.attn_fwd_splitkv(bd.BF16, B, H, k.shape[1], Sq, Sk, D, D, q.data_ptr(), k.data_ptr(), v.data_ptr(), 0.0,
                               ctypes.byref(m), n, o.data_ptr(), lse.data_ptr(), ws.data_ptr(), need,
                               torch.cuda.current_stream().cuda_stream)
@@ -57,21 +67,38 @@ def test_rejects_problems_larger_than_the_scratch():
     assert lib.attn_fwd_splitkv_workspace_bytes(64, 64, 1, 128, 64) > SCRATCH
 
 
+# (B, H, Hkv, Sq, Sk, D, splits, causal): two calls in a row per case
+CASES = {
+    "per_row": ((4, 8, 8, 1, 4000, 128, 8, False), (2, 16, 16, 3, 2500, 64, 16, False)),
+    "gqa_packed": ((2, 32, 8, 1, 3000, 128, 4, False), (3, 16, 4, 2, 1500, 64, 8, False)),
+    "causal": ((2, 4, 4, 5, 700, 128, 4, True), (1, 8, 2, 3, 900, 64, 2, True)),
+}
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_workspace_entry_point_and_oracle_on_two_calls(name):
     dev = torch.device("cuda")
-    g = torch.Generator(device=dev).manual_seed(42)
-    for B, H, Sq, Sk, D, n in ((4, 8, 1, 4000, 128, 8), (2, 16, 3, 2500, 64, 16)):
-        q = torch.randn(B, H, Sq, D, generator=g, device=dev).bfloat16()
-        k = torch.randn(B, H, Sk, D, generator=g, device=dev).bfloat16()
-        v = torch.randn(B, H, Sk, D, generator=g, device=dev).bfloat16()
+    for call, (B, H, Hkv, Sq, Sk, D, n, causal) in enumerate(CASES[name]):
+        x = make_inputs(B, H, Sq, Sk, D, D, "bf16", seed=42 + call, dout=False, Hkv=Hkv)
+        q, k, v = (x[t].to(dev) for t in ("q", "k", "v"))
         o = torch.full((B, H, Sq, D), float("nan"), dtype=torch.bfloat16, device=dev)
         lse = torch.full((B, H, Sq), float("nan"), dtype=torch.float32, device=dev)
-        assert _call_noalloc(q, k, v, n, o, lse) == 0
-        o_ref, lse_ref = _call_with_workspace(q, k, v, n)
+        assert _call_noalloc(q, k, v, n, o, lse, causal) == 0
+        o_ref, lse_ref = _call_with_workspace(q, k, v, n, causal)
         torch.cuda.synchronize()
         assert bd.load_library().gbattn_last_device_error(None) == 0
-        a, r = o.double().cpu().numpy(), o_ref.double().cpu().numpy()
-        assert not np.isnan(a).any()
-        assert np.all(np.abs(a - r) <= 2e-2 + 2e-2 * np.abs(r))
-        assert np.max(np.abs(lse.double().cpu().numpy() - lse_ref.double().cpu().numpy())) <= 2e-2
+        assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+        # same kernels, partials in another buffer: identical results
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+        # and the fp64 oracle, head by head (query head h reads key/value head h // (H / Hkv))
+        f64 = lambda t: t.float().double().numpy()  # noqa: E731
+        qh, kh, vh = f64(x["q"]), f64(x["k"]), f64(x["v"])
+        og, lg = f64(o.cpu()), lse.cpu().double().numpy()
+        G = H // Hkv
+        for b in range(B):
+            for h in range(H):
+                p = orc.Problem(qh[b, h], kh[b, h // G], vh[b, h // G], kind=orc.CAUSAL if causal else orc.NONE)
+                o_r, l_r = p.forward()
+                assert np.all(np.abs(og[b, h] - o_r) <= 2e-2 + 2e-2 * np.abs(o_r)), (name, call, b, h)
+                assert np.max(np.abs(lg[b, h] - l_r)) <= 2e-2, (name, call, b, h)

@@ -10,4 +10,5 @@ from .binding import (  # noqa: F401
     NONE, CAUSAL, SLIDING, BLOCK_DIAG, PREFIX_LM, DYNAMIC_TOPK, MINI_CAUSAL, TABLE, pack_mask_table,
     build_block_mask, alloc_block_lists, attn_fwd, attn_bwd, attn_fwd_splitkv, attn_fwd_splitkv_paged,
     attn_fwd_splitkv_noalloc, attn_bwd_workspace_bytes, attn_fwd_splitkv_workspace_bytes, load_library,
+    set_dkdv_cta_pair, last_device_error,
 )

@@ -75,6 +75,10 @@ _SIGS = [
     ("attn_fwd_splitkv_noalloc", ctypes.c_int, [ctypes.c_int] * 8 + [ctypes.c_void_p] * 3
      + [ctypes.c_float, ctypes.POINTER(_Mask), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("gbattn_last_device_error", ctypes.c_int, [ctypes.c_void_p]),
+    ("gbattn_set_dkdv_cta_pair", ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    # include/gbattn_test.h: a test hook, not part of the attention API
+    ("gbattn_test_fwd_stalled", ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5
+     + [ctypes.c_ulonglong, ctypes.c_void_p]),
 ]
 
 EXPORTS = [s[0] for s in _SIGS]
@@ -384,6 +388,14 @@ def attn_fwd_splitkv_paged(q, k_cache, v_cache, page_table, seqlens_k, scale=0.0
                                       0 if workspace is None else workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "attn_fwd_splitkv_paged")
     return o, lse
+
+
+def set_dkdv_cta_pair(mode: int) -> int:
+    """Selects attn_bwd's dK/dV kernel where the CTA-pair kernel applies: 1 =
+    CTA pair, 0 = one CTA, -1 = library default. Returns the previous mode."""
+    prev = ctypes.c_int(0)
+    _check(load_library().gbattn_set_dkdv_cta_pair(int(mode), ctypes.byref(prev)), "gbattn_set_dkdv_cta_pair")
+    return prev.value
 
 
 def last_device_error(stream=None) -> int:

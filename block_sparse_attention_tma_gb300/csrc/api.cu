@@ -7,10 +7,22 @@
 #include <mutex>
 
 #include "kernels.h"
+#include "../../include/gbattn_test.h"
 
 namespace gb {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+namespace {
+// gbattn_set_dkdv_cta_pair: -1 = library default, 0 = one-CTA kernel, 1 = CTA pair
+std::atomic<int> g_dkdv_pair{-1};
+constexpr bool kDkdvPairDefault = false;
+}  // namespace
+
+bool dkdv_cta_pair_enabled() {
+  const int v = g_dkdv_pair.load(std::memory_order_relaxed);
+  return v < 0 ? kDkdvPairDefault : v != 0;
+}
 
 size_t bwd_workspace_bytes(const Shape& s) {
   const size_t BH = (size_t)s.B * s.H;
@@ -174,11 +186,16 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes) {
+  return make_tmap_bf16_3d_box(map, base, D, S, BH, swizzle_bytes, 128);
+}
+
+bool make_tmap_bf16_3d_box(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes,
+                           int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  cuuint32_t box[3] = {(cuuint32_t)(swizzle_bytes / 2), 128, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(swizzle_bytes / 2), (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -430,10 +447,33 @@ int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Hkv, int Sq, int Sk, i
                                 need, o, lse, static_cast<cudaStream_t>(stream));
 }
 
+int gbattn_test_fwd_stalled(int B, int H, int Sq, int Sk, int D, const void* q, const void* k, const void* v,
+                            void* o, float* lse, unsigned long long wait_ns, gbattn_stream stream) {
+  if (!dims_ok(B, H, Sq, Sk) || !q || !k || !v || !o || !lse) return GBATTN_ERR_ARG;
+  if (wait_ns < 1 || wait_ns > 2000000000ull) return GBATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse)) return GBATTN_ERR_ALIGN;
+  if (D != 32 && D != 64 && D != 128) return GBATTN_ERR_UNSUPPORTED;
+  if (!bf16_seq_ok(Sq, Sk)) return GBATTN_ERR_UNSUPPORTED;
+  const int rc = device_check();
+  if (rc) return rc;
+  HostMask hm;
+  check_mask(nullptr, &hm);
+  const Shape s{B, H, Sq, Sk, D, D, H};
+  const FwdTestHook hook{wait_ns, 1};
+  return fwd_bf16_launch(s, q, k, v, resolve_scale(0.f, D), hm, o, lse, static_cast<cudaStream_t>(stream), &hook);
+}
+
+int gbattn_set_dkdv_cta_pair(int mode, int* previous) {
+  if (mode < -1 || mode > 1) return GBATTN_ERR_ARG;
+  const int prev = g_dkdv_pair.exchange(mode);
+  if (previous) *previous = prev;
+  return GBATTN_OK;
+}
+
 int gbattn_last_device_error(gbattn_stream stream) {
   if (device_check() != GBATTN_OK) return GBATTN_ERR_UNSUPPORTED;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GBATTN_ERR_CUDA;
-  int errs[6] = {fwd_take_error(),    bwd_take_error(),    dkdv_take_error(),
+  int errs[7] = {fwd_take_error(),    bwd_take_error(),    dkdv_take_error(),   dkdv2_take_error(),
                  simt_take_error(),   decode_take_error(), blockmask_take_error()};
   for (int e : errs)
     if (e == GBATTN_ERR_CUDA) return e;

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   uint16_t* tlist = reinterpret_cast<uint16_t*>(colterm + 8 * 128);  // [TCAP]
   uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtl abort_flag = wait_ctl(reinterpret_cast<volatile int*>(tmem_slot + 1), p.wait_ns);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
   int* gcount = reinterpret_cast<int*>(tmem_slot + 4);  // [2] gathered keys seen by the first / last row
 
@@ -227,11 +227,11 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
           ++n;
         }
         if (*abort_flag) {
-          if (nk > 0) mbar_drain(bar + C::B_QG, 0);
+          if (nk > 0) mbar_drain(bar + C::B_QG, 0, abort_flag);
           for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t)
-            mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1);
+            mbar_drain(bar + C::B_KF + t % C::KST, (t / C::KST) & 1, abort_flag);
           for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t)
-            mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1);
+            mbar_drain(bar + C::B_VF + t % C::VST, (t / C::VST) & 1, abort_flag);
         }
       }
     } else {
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         ++n;
       }
       cp_async_wait_all();  // every copy of this thread lands before the CTA exits
-      if (lane == 0 && *abort_flag && n > 0) mbar_drain(bar + C::B_QG, 0);
+      if (lane == 0 && *abort_flag && n > 0) mbar_drain(bar + C::B_QG, 0, abort_flag);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
       umma_commit(bar + C::B_DONE);
       if (*abort_flag) {
         umma_commit(bar + C::B_DRAIN);
-        mbar_drain(bar + C::B_DRAIN, 0);
+        mbar_drain(bar + C::B_DRAIN, 0, abort_flag);
       }
     }
   } else {
@@ -663,7 +663,21 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   int rc = GBATTN_OK;
   if (nkt > 0) {
     const int key_mode = m.gather ? 1 : (prm.mask.table ? 2 : 0);
-    rc = dkdv_launch(prm, s.Dqk, s.Dv, cap, key_mode, dkey_bias != nullptr, nkt * s.B * s.Hkv, st);
+    // the CTA-pair dK/dV kernel: closed-form masks (lists whose sparse blocks
+    // span both 128-key tiles of a pair), Dqk / Dv = 192 / 128 or 128 / 128
+    const bool pair = key_mode == 0 && dkdv2_supported(s.Dqk, s.Dv) && (!prm.has_lists || prm.sparse_n % 256 == 0) &&
+                      dkdv_cta_pair_enabled();
+    if (pair) {
+      const int swqc = (s.Dqk / 2) % 64 == 0 ? 128 : 64;
+      if (!make_tmap_bf16_3d_box(&prm.tm_qr, q, s.Dqk, s.Sq, BH, 128, 64) ||
+          !make_tmap_bf16_3d_box(&prm.tm_qc, q, s.Dqk, s.Sq, BH, swqc, 128) ||
+          !make_tmap_bf16_3d_box(&prm.tm_gr, dout, s.Dv, s.Sq, BH, 128, 64))
+        rc = GBATTN_ERR_CUDA;
+      else
+        rc = dkdv2_launch(prm, s.Dqk, s.Dv, cap, dkey_bias != nullptr, (nkt + 1) / 2, st);
+    } else {
+      rc = dkdv_launch(prm, s.Dqk, s.Dv, cap, key_mode, dkey_bias != nullptr, nkt * s.B * s.Hkv, st);
+    }
   }
   if (rc == GBATTN_OK) {
     if (s.Dqk == 32 && s.Dv == 32) rc = launch_dq_cap<32, 32>(prm, s, cap, sq);

@@ -33,8 +33,20 @@ __device__ __forceinline__ void raise_dev_error(int code) { atomicCAS(&g_dev_err
   }
 
 // A wait that has not finished after this many nanoseconds gives up. Every
-// wait in these kernels normally ends within microseconds.
+// wait in these kernels normally ends within microseconds. A launch may set
+// a shorter limit (its parameter block's wait_ns; 0 = this default).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// The abort flag a CTA's roles share (in shared memory) and the time limit
+// of their waits. *w reads or writes the flag.
+struct WaitCtl {
+  volatile int* flag;
+  uint64_t limit_ns;
+  __device__ __forceinline__ volatile int& operator*() const { return *flag; }
+};
+__device__ __forceinline__ WaitCtl wait_ctl(volatile int* flag, uint64_t limit_ns) {
+  return WaitCtl{flag, limit_ns ? limit_ns : kWaitLimitNs};
+}
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
@@ -76,9 +88,9 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up (returns
-// false, raising GBATTN_ERR_TIMEOUT once) after kWaitLimitNs, or as soon as
-// *abort is set by another role of the same CTA.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// false, raising GBATTN_ERR_TIMEOUT once) after abort.limit_ns, or as soon as
+// the abort flag is set by another role of the same CTA.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& abort) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try(a, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -86,7 +98,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try(a, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > abort.limit_ns) {
         raise_dev_error(GBATTN_ERR_TIMEOUT);
         *abort = 1;
         return false;
@@ -95,12 +107,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Bounded wait used only on the way out of an aborted kernel.
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+// Bounded wait used only on the way out of an aborted kernel (the same time
+// limit as the kernel's other waits).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = global_ns();
   while (!mbar_try(a, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return;
+    if (global_ns() - t0 > w.limit_ns) return;
   }
 }
 
@@ -355,6 +368,105 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// CTA pairs (a cluster of two CTAs on two SMs): the tcgen05 operations of a
+// pair use .cta_group::2. One thread of the even CTA issues an MMA with
+// M = 256 whose A rows and D rows are split 128 / 128 between the two CTAs
+// (each CTA's own shared memory / tensor memory at the same offsets) and
+// whose B operand is split N / 2 / N / 2 (CTA r provides columns
+// [r N/2, (r+1) N/2) of B at the same shared-memory offset). Every tcgen05
+// instruction of such a kernel uses .cta_group::2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Non-blocking probe with acquire at cluster scope (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for barriers the peer CTA arrives on (cluster-scope acquire).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& abort) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_cluster(a, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_cluster(a, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > abort.limit_ns) {
+        raise_dev_error(GBATTN_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+// Whole-cluster execution barrier (every thread of both CTAs).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Tensor-memory allocation of a CTA pair: one warp of each CTA executes it;
+// both CTAs get the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Pair MMA, D(tmem) (+)= A(smem) * B(smem), descriptors as 32-bit halves.
+__device__ __forceinline__ void mma2_ss(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi,
+                                        uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Pair MMA, D(tmem) (+)= A(tmem) * B(smem).
+__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in both CTAs of the pair when
+// every pair MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
 
 // ---------------------------------------------------------------------------
 // Small math helpers (hardware instructions, no library code)

@@ -40,6 +40,7 @@ struct DecParams {
   const int32_t* page_table;  // [B][max_pages], or nullptr (dense cache)
   int page_size, max_pages, num_pages;
   float scale_log2;
+  unsigned long long wait_ns;  // time limit of every wait (0 = kWaitLimitNs)
 };
 
 // Address of the key/value row `key` of sequence b, key/value head hkv.
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
   uint64_t* full = reinterpret_cast<uint64_t*>(sV + kDecStages * CHB);
   uint64_t* empty = full + kDecStages;
   float* red = reinterpret_cast<float*>(empty + kDecStages);  // [kDecWarps][D + 2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kDecWarps * (D + 2));
+  const WaitCtl abort_flag = wait_ctl(reinterpret_cast<volatile int*>(red + kDecWarps * (D + 2)), p.wait_ns);
 
   const int split = blockIdx.x % p.nsplit;
   const int rowid = blockIdx.x / p.nsplit;  // bh * Sq + i
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_kernel(const DecParams
       }
       if (*abort_flag)
         for (int c = (issued > kDecStages ? issued - kDecStages : 0); c < issued; ++c)
-          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1);
+          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ compute
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_group_kernel(const Dec
   uint64_t* full = reinterpret_cast<uint64_t*>(sV + kDecStages * CHB);
   uint64_t* empty = full + kDecStages;
   float* red = reinterpret_cast<float*>(empty + kDecStages);  // [kDecWarps][RC][D + 2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kDecWarps * RC * (D + 2));
+  const WaitCtl abort_flag = wait_ctl(reinterpret_cast<volatile int*>(red + kDecWarps * RC * (D + 2)), p.wait_ns);
 
   const int split = blockIdx.x % p.nsplit;
   const int rest = blockIdx.x / p.nsplit;
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) splitkv_group_kernel(const Dec
       }
       if (*abort_flag)
         for (int c = (issued > kDecStages ? issued - kDecStages : 0); c < issued; ++c)
-          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1);
+          mbar_drain(full + c % kDecStages, (c / kDecStages) & 1, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ compute

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
   uint16_t* tlist = reinterpret_cast<uint16_t*>(soff + kMaxGroup + 4);  // [TCAP]
   uint64_t* bar = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtl abort_flag = wait_ctl(reinterpret_cast<volatile int*>(tmem_slot + 1), p.wait_ns);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
   int* gpos = reinterpret_cast<int*>(tmem_slot + 4);  // [2] first / last key of a gathered tile
 
@@ -213,11 +213,11 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
           ++n;
         }
         if (*abort_flag) {
-          if (nq > 0) mbar_drain(bar + C::B_KV, 0);
+          if (nq > 0) mbar_drain(bar + C::B_KV, 0, abort_flag);
           for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t)
-            mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
+            mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1, abort_flag);
           for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t)
-            mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
+            mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1, abort_flag);
         }
       }
     } else {
@@ -269,11 +269,11 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
         ++n;
       }
       if (lane == 0 && *abort_flag) {
-        if (n > 0) mbar_drain(bar + C::B_KV, 0);
+        if (n > 0) mbar_drain(bar + C::B_KV, 0, abort_flag);
         for (int t = (nq > C::QST ? nq - C::QST : 0); t < nq; ++t)
-          mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1);
+          mbar_drain(bar + C::B_QF + t % C::QST, (t / C::QST) & 1, abort_flag);
         for (int t = (ng > C::GST ? ng - C::GST : 0); t < ng; ++t)
-          mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1);
+          mbar_drain(bar + C::B_GF + t % C::GST, (t / C::GST) & 1, abort_flag);
       }
     }
   } else if (warp == 1) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
       umma_commit(bar + C::B_DONE);
       if (*abort_flag) {
         umma_commit(bar + C::B_DRAIN);
-        mbar_drain(bar + C::B_DRAIN, 0);
+        mbar_drain(bar + C::B_DRAIN, 0, abort_flag);
       }
     }
   } else {

@@ -72,6 +72,8 @@ struct FwdParams {
   const int32_t* pk_pages;    // [B][pk_max_pages] page table, or nullptr (dense cache):
                               // tm_k / tm_v then map the pool [num_pages * Hkv, page_size, D]
   int pk_page_size, pk_max_pages, pk_num_pages;
+  unsigned long long wait_ns;  // time limit of every wait (0 = kWaitLimitNs)
+  int test_withhold_k;         // test hook: the K tile of the first visited tile is never loaded
 };
 
 template <int DQK, int DV>
@@ -89,8 +91,8 @@ struct FwdCfg {
   static constexpr int T_O = 256, T_Q = 384;
   static_assert(T_Q + DQK / 2 <= 512 && T_O + DV <= T_Q, "TMEM budget");
   // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
-  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2][4 lane quarters], fin
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 8 + 1;
+  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2][4 lane quarters], fin, o_fin
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 8 + 1 + 1;
   static constexpr int THREADS = 320;
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
@@ -140,8 +142,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
   uint64_t* drain = o_done + 1;
   uint64_t* xbar = drain + 1;  // [2][4]: the two warps of a lane quarter exchange row maxima
   uint64_t* fin = xbar + 8;
+  // one phase: every PV product of the CTA has completed (the epilogue's wait;
+  // a parity wait on o_done there could pass two phases early)
+  uint64_t* o_fin = fin + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const WaitCtl abort_flag = wait_ctl(reinterpret_cast<volatile int*>(tmem_slot + 1), p.wait_ns);
   int* tcount = reinterpret_cast<int*>(tmem_slot + 2);
   int* gcount = reinterpret_cast<int*>(tmem_slot + 4);  // [2] gathered keys seen by the first / last row
 
@@ -249,6 +254,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(fin, 256);
+    mbar_init(o_fin, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -300,10 +306,12 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
           }
           const int ks = n % C::KST;
           if (n >= C::KST && !(ok = mbar_wait(k_empty + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
-          mbar_expect_tx(k_full + ks, C::QTILE);
-          for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), ky, kz);
-          ++nk;
+          if (!(p.test_withhold_k && n == 0)) {
+            mbar_expect_tx(k_full + ks, C::QTILE);
+            for (int j = 0; j < C::NQSLAB; ++j)
+              tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, k_full + ks, j * (C::SWQ / 2), ky, kz);
+          }
+          ++nk;  // a withheld tile counts too: its drain below gives up after the time limit
           const int vs = n % C::VST;
           if (n >= C::VST && !(ok = mbar_wait(v_empty + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(v_full + vs, C::VTILE);
@@ -314,9 +322,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         }
         if (*abort_flag) {
           // let every copy this thread started land before the CTA exits
-          mbar_drain(q_full, 0);
-          for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1);
-          for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1);
+          mbar_drain(q_full, 0, abort_flag);
+          for (int t = (nk > C::KST ? nk - C::KST : 0); t < nk; ++t) mbar_drain(k_full + t % C::KST, (t / C::KST) & 1, abort_flag);
+          for (int t = (nv > C::VST ? nv - C::VST : 0); t < nv; ++t) mbar_drain(v_full + t % C::VST, (t / C::VST) & 1, abort_flag);
         }
       }
     } else if (any_tile) {
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         ++n;
       }
       cp_async_wait_all();  // every copy of this thread lands before the CTA exits
-      if (lane == 0 && *abort_flag) mbar_drain(q_full, 0);
+      if (lane == 0 && *abort_flag) mbar_drain(q_full, 0, abort_flag);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -399,10 +407,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         if (n >= 1 && !(ok = issue_pv(n - 1))) break;
         ++n;
       }
-      if (ok && n >= 1) issue_pv(n - 1);
+      if (ok && n >= 1 && issue_pv(n - 1)) umma_commit(o_fin);
       if (*abort_flag) {
         umma_commit(drain);
-        mbar_drain(drain, 0);
+        mbar_drain(drain, 0, abort_flag);
       }
     }
   } else {
@@ -563,7 +571,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       l_run = (resc ? l_run * alpha : l_run) + lsum;
       m_run = m_use;
       if (__any_sync(0xffffffffu, resc)) {
-        // O must not be in flight: PV of the previous tile has completed
+        // O must not be in flight: PV of the previous tile has completed.
+        // (S of this tile was issued after PV of tile n - 2, so at most one
+        // o_done phase is outstanding and the parity wait is exact.)
         ok = mbar_wait(o_done, (n - 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -622,7 +632,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
             if (grp == 0 && p.lse) p.lse[orow_id] = -INFINITY;
           }
         }
-        if (n > 0 && __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
+        if (n > 0 && __all_sync(0xffffffffu, mbar_wait(o_fin, 0, abort_flag))) {
           tc_fence_after();
           const float inv = live ? 1.f / l_tot : 0.f;
           constexpr int CH = DVH >= 32 ? 32 : 16;
@@ -687,9 +697,13 @@ static int launch_fwd_cap(const FwdParams& prm, int grid, bool cap, cudaStream_t
 }
 
 int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale, const HostMask& m,
-                    void* o, float* lse, cudaStream_t st) {
+                    void* o, float* lse, cudaStream_t st, const FwdTestHook* hook) {
   FwdParams prm;
   memset(&prm, 0, sizeof(prm));
+  if (hook) {
+    prm.wait_ns = hook->wait_ns;
+    prm.test_withhold_k = hook->withhold_first_k_tile;
+  }
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;

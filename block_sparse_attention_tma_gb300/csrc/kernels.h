@@ -65,13 +65,24 @@ struct HostMask {
 // Encodes a 3-D bf16 tensor map over [BH, S, D] (D innermost) with a box of
 // (swizzle_bytes/2) x 128 x 1 and the given swizzle (64 or 128 bytes).
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes);
+// The same with a box of (swizzle_bytes/2) x box_rows x 1.
+bool make_tmap_bf16_3d_box(CUtensorMap* map, const void* base, int D, int S, int BH, int swizzle_bytes,
+                           int box_rows);
 // Encodes a 2-D bf16 tensor map over [rows, D] with a box one row high and
 // (swizzle_bytes/2) wide, for TMA row gathers (tile::gather4).
 bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, int D, long long rows, int swizzle_bytes);
 
+// Test hook of the bf16 forward (the abort path of its bounded waits): a
+// shorter wait limit, and the K tile of the first visited tile withheld so
+// that the MMA thread's wait for it runs out.
+struct FwdTestHook {
+  unsigned long long wait_ns;
+  int withhold_first_k_tile;
+};
+
 // Kernel launchers: return GBATTN_OK or GBATTN_ERR_CUDA.
 int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, float scale,
-                    const HostMask& m, void* o, float* lse, cudaStream_t st);
+                    const HostMask& m, void* o, float* lse, cudaStream_t st, const FwdTestHook* hook = nullptr);
 int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, float scale,
                     const HostMask& m, float* o, float* lse, cudaStream_t st);
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o,
@@ -108,9 +119,14 @@ int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbat
 int fwd_take_error();
 int bwd_take_error();
 int dkdv_take_error();
+int dkdv2_take_error();
 int simt_take_error();
 int decode_take_error();
 int blockmask_take_error();
+
+// Which dK/dV kernel attn_bwd runs where the CTA-pair kernel applies
+// (gbattn_set_dkdv_cta_pair; process-wide).
+bool dkdv_cta_pair_enabled();
 
 // Workspace layout of attn_bwd: [delta fp32 BH x ceil128(Sq)][lse2 fp32 BH x ceil128(Sq)]
 size_t bwd_workspace_bytes(const Shape& s);

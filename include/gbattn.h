@@ -309,6 +309,26 @@ int attn_fwd_splitkv_noalloc(int dtype, int B, int H, int Hkv, int Sq, int Sk, i
                              const gbattn_mask* mask, int num_splits, void* o, float* lse,
                              gbattn_stream stream);
 
+/*
+ * gbattn_set_dkdv_cta_pair - which dK/dV kernel attn_bwd runs where the
+ * CTA-pair kernel applies ("Enable 2CTA for SM100 block-sparse backward",
+ * Summary: the 2-CTA backward over kv sub-tiles of a sparse block).
+ *   The CTA-pair kernel runs a cluster of two CTAs per 256 keys whose
+ *   tcgen05 MMAs span both SMs (M = 256 keys, each CTA holding half of the
+ *   query-side operand). It applies to bf16 calls without gathered keys or an
+ *   element table, with Dqk / Dv = 192 / 128 or 128 / 128, and with block
+ *   lists whose sparse_n is a multiple of 256 (or no lists); other calls
+ *   always run the one-CTA kernel. Both give the same gradients up to fp32
+ *   summation order and both are deterministic.
+ *   mode: 1 = the CTA-pair kernel where it applies, 0 = the one-CTA kernel,
+ *   -1 = the library's default (the one measured faster on GB300).
+ *   previous: if not NULL, receives the mode in effect before the call.
+ *   Process-wide; takes effect for calls issued after it returns.
+ * Returns GBATTN_OK, or GBATTN_ERR_ARG for a mode outside -1..1 (nothing
+ * changes).
+ */
+int gbattn_set_dkdv_cta_pair(int mode, int* previous);
+
 /* Synchronises `stream`, then returns and clears the device-side error word
  * of the current device: GBATTN_OK, GBATTN_ERR_TIMEOUT (a bounded wait inside
  * a kernel ran out; the kernel returned early and its outputs are invalid) or

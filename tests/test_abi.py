@@ -2,6 +2,7 @@
 include/gbattn.h declares, and rejects bad arguments on the host (before any
 CUDA call) with the documented status codes."""
 import ctypes
+import glob
 import os
 import re
 
@@ -12,10 +13,13 @@ import block_sparse_attention_tma_gb300 as ga
 from block_sparse_attention_tma_gb300 import binding as bd
 
 HEADER = os.path.join(ROOT, "include", "gbattn.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    """Every function declared in include/*.h (the API header and the test
+    hooks' header)."""
+    src = "\n".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "sizeof")))
@@ -34,6 +38,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         assert hasattr(lib, n), n
     assert set(bd.EXPORTS) >= set(declared_functions())
+    assert "gbattn_test_fwd_stalled" in declared_functions()
     assert lib.gbattn_version() == 102
 
 
@@ -149,3 +154,26 @@ def test_build_block_mask_argument_checks():
     assert lib.build_block_mask(1, 1, 128, 128, ctypes.byref(m), None, None) == bd.ERR_ARG
     b2 = bd._Blocks(64, 128, *[FAKE] * 9)
     assert lib.build_block_mask(1, 1, 128, 128, ctypes.byref(m), ctypes.byref(b2), None) == bd.ERR_BLOCKS
+
+
+def test_stalled_forward_hook_rejects_bad_arguments_on_the_host():
+    lib = ga.load_library()
+    f = FAKE
+    assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 64, f, f, f, f, f, 0, None) == bd.ERR_ARG  # wait 0
+    assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 64, f, f, f, f, f, 3 * 10**9, None) == bd.ERR_ARG
+    assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 64, f + 2, f, f, f, f, 10**6, None) == bd.ERR_ALIGN
+    assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 96, f, f, f, f, f, 10**6, None) == bd.ERR_UNSUPPORTED
+    assert lib.gbattn_test_fwd_stalled(0, 1, 128, 128, 64, f, f, f, f, f, 10**6, None) == bd.ERR_ARG
+
+
+def test_dkdv_cta_pair_selector_host_side():
+    lib = ga.load_library()
+    prev = ctypes.c_int(99)
+    assert lib.gbattn_set_dkdv_cta_pair(1, ctypes.byref(prev)) == bd.OK
+    first = prev.value
+    assert first in (-1, 0, 1)
+    assert lib.gbattn_set_dkdv_cta_pair(0, ctypes.byref(prev)) == bd.OK and prev.value == 1
+    assert lib.gbattn_set_dkdv_cta_pair(2, ctypes.byref(prev)) == bd.ERR_ARG and prev.value == 1  # unchanged
+    assert lib.gbattn_set_dkdv_cta_pair(-2, None) == bd.ERR_ARG
+    assert lib.gbattn_set_dkdv_cta_pair(first, ctypes.byref(prev)) == bd.OK and prev.value == 0
+    assert ga.set_dkdv_cta_pair(first) == first

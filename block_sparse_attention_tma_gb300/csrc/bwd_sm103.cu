@@ -418,20 +418,26 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 v4 = ct[c4];
-          const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+          const int c = 4 * c4;
+          if constexpr (CAP) {
+            const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            const float x = __uint_as_float(rs[c]);
-            float t;
-            if constexpr (CAP) {
-              const float th = tanh_fast(x * p.cap_pre);
-              t = fmaf(p.cap_post, th, cv[e]);
-              dd[c] = 1.f - th * th;
-            } else {
-              t = fmaf(x, p.scale_log2, cv[e]);
+            for (int e = 0; e < 4; ++e) {
+              const float th = tanh_fast(__uint_as_float(rs[c + e]) * p.cap_pre);
+              dd[c + e] = 1.f - th * th;
+              pf[c + e] = ex2(fmaf(p.cap_post, th, cv[e]) - l2);
             }
-            pf[c] = ex2(t - l2);
+          } else {  // two columns per instruction
+            float t0, t1, t2, t3;
+            fma2(t0, t1, __uint_as_float(rs[c]), __uint_as_float(rs[c + 1]), p.scale_log2, p.scale_log2, v4.x, v4.y);
+            fma2(t2, t3, __uint_as_float(rs[c + 2]), __uint_as_float(rs[c + 3]), p.scale_log2, p.scale_log2, v4.z,
+                 v4.w);
+            sub2(t0, t1, t0, t1, l2, l2);
+            sub2(t2, t3, t2, t3, l2, l2);
+            pf[c] = ex2(t0);
+            pf[c + 1] = ex2(t1);
+            pf[c + 2] = ex2(t2);
+            pf[c + 3] = ex2(t3);
           }
         }
         if (masked) {

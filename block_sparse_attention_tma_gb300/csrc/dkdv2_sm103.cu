@@ -414,26 +414,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Dkdv2Cfg<DQK, DV>::T
 #pragma unroll
         for (int c4 = 0; c4 < CW / 4; ++c4) {
           const float4 l4 = sl4[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float dd[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            const float x = __uint_as_float(r[c]);
-            float t;
-            if constexpr (CAP) {
-              const float th = tanh_fast(x * p.cap_pre);
-              t = fmaf(p.cap_post, th, kt);
-              dd[e] = 1.f - th * th;
-            } else {
-              t = fmaf(x, p.scale_log2, kt);
-              dd[e] = 1.f;
-            }
-            pf[c] = ex2(t - lv[e]);
-          }
+          const int c = 4 * c4;
           if constexpr (CAP) {
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float dd[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float th = tanh_fast(__uint_as_float(r[c + e]) * p.cap_pre);
+              dd[e] = 1.f - th * th;
+              pf[c + e] = ex2(fmaf(p.cap_post, th, kt) - lv[e]);
+            }
             dc[2 * c4] = pack_bf16(dd[0], dd[1]);
             dc[2 * c4 + 1] = pack_bf16(dd[2], dd[3]);
+          } else {  // two columns per instruction
+            float t0, t1, t2, t3;
+            fma2(t0, t1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), p.scale_log2, p.scale_log2, kt, kt);
+            fma2(t2, t3, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), p.scale_log2, p.scale_log2, kt, kt);
+            sub2(t0, t1, t0, t1, l4.x, l4.y);
+            sub2(t2, t3, t2, t3, l4.z, l4.w);
+            pf[c] = ex2(t0);
+            pf[c + 1] = ex2(t1);
+            pf[c + 2] = ex2(t2);
+            pf[c + 3] = ex2(t3);
           }
         }
         if (masked) {

@@ -501,12 +501,14 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 v4 = ct[c4];
-          const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+          const int c = 4 * c4;
+          if constexpr (CAP) {
+            const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            if constexpr (CAP) t[c] = fmaf(p.cap_post, tanh_fast(t[c] * p.cap_pre), cv[e]);
-            else t[c] = fmaf(t[c], p.scale_log2, cv[e]);
+            for (int e = 0; e < 4; ++e) t[c + e] = fmaf(p.cap_post, tanh_fast(t[c + e] * p.cap_pre), cv[e]);
+          } else {  // two columns per instruction
+            fma2(t[c], t[c + 1], t[c], t[c + 1], p.scale_log2, p.scale_log2, v4.x, v4.y);
+            fma2(t[c + 2], t[c + 3], t[c + 2], t[c + 3], p.scale_log2, p.scale_log2, v4.z, v4.w);
           }
         }
       }
@@ -530,13 +532,17 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
           for (int c = 0; c < 64; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
         }
       }
-      // row max: 8 independent chains over this half, then the other half's
+      // row max: 8 independent chains over this half (three-input max), then
+      // the other half's
       float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = t[e];
-#pragma unroll
-      for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], t[c]);
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int e = 0; e < 8; ++e) {
+        mx[e] = max3(t[e], t[e + 8], t[e + 16]);
+        mx[e] = max3(mx[e], t[e + 24], t[e + 32]);
+        mx[e] = max3(mx[e], t[e + 40], t[e + 48]);
+        mx[e] = fmaxf(mx[e], t[e + 56]);
+      }
+      float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       float* xm = xmax + sb * 256;
       xm[grp * 128 + row] = mt;
       mbar_arrive(xbar + sb * 4 + quarter);
@@ -556,15 +562,18 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         m_use = mt;
       }
       const float msafe = (m_use == -INFINITY) ? 0.f : m_use;
-      float ls[8];
+      float ls[8];  // four chains of column pairs
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float a0 = ex2(t[2 * c] - msafe);
-        const float a1 = ex2(t[2 * c + 1] - msafe);
-        ls[c & 7] += a0 + a1;
+        float d0, d1;
+        sub2(d0, d1, t[2 * c], t[2 * c + 1], msafe, msafe);
+        const float a0 = ex2(d0);
+        const float a1 = ex2(d1);
+        const int q = 2 * (c & 3);
+        add2(ls[q], ls[q + 1], ls[q], ls[q + 1], a0, a1);
         pk[c] = pack_bf16(a0, a1);
       }
       const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));

@@ -420,14 +420,11 @@ def time_fwd_bwd(ga, torch, st, g, spec, lists, reps=10):
     return out
 
 
-def run_workload_sweep(ga, torch, dev, st, g, rank):
+def sweep_masks(ga, torch, dev, st, g):
     """The other mask kinds of the 16K MLA prefill (sliding W = Sk/3,
-    block-diagonal 1024, prefix-LM 2048, each with the relative bias), the
-    dense masked workload (B=2, H=8, S=2048, D=64: causal, sliding W=512), and
-    the dynamic top-k workload (B=1, H=16, S=8192, top-2048 keys per head by an
-    N(0,1) key bias, with causal) at D = 32 and 64. Not part of the step;
-    FLOPs count the allowed pairs (fwd 2N(Dqk+Dv), bwd 2N(3Dqk+2Dv))."""
-    from block_sparse_attention_tma_gb300.synth import make_inputs
+    block-diagonal 1024, prefix-LM 2048, each with the relative bias), and the
+    causal backward once more with the CTA-pair dK/dV kernel
+    (gbattn_set_dkdv_cta_pair) for comparison with the default one-CTA kernel."""
     P = PREFILL
     B, H, S, Dqk, Dv = P["B"], P["H"], P["S"], P["Dqk"], P["Dv"]
     lists = ga.alloc_block_lists(B, H, S, S, P["sparse_m"], P["sparse_n"], device=dev)
@@ -443,8 +440,25 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
         masks[name] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
                        "fwd_tflops": round(2 * n * (Dqk + Dv) / (fms * 1e-3) / 1e12, 1),
                        "bwd_tflops": round(2 * n * (3 * Dqk + 2 * Dv) / (bms * 1e-3) / 1e12, 1)}
-    del lists
-    # dense masked workload: B=2, H=8, S=2048, D=64, causal and causal sliding W=512
+    spec = ga.MaskSpec(kind=ga.CAUSAL, rel_bias_slope=P["slope"])
+    n = B * H * causal_pairs(S)
+    prev = ga.set_dkdv_cta_pair(1)
+    try:
+        _, bms = time_fwd_bwd(ga, torch, st, g, spec, lists)
+    finally:
+        ga.set_dkdv_cta_pair(prev)
+    masks["causal_cta_pair_bwd"] = {"bwd_ms": round(bms, 4),
+                                    "bwd_tflops": round(2 * n * (3 * Dqk + 2 * Dv) / (bms * 1e-3) / 1e12, 1),
+                                    "note": "dK/dV on CTA pairs (cta_group::2); the default one-CTA kernel is "
+                                            "the bench line's attn_bwd"}
+    return dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
+                              f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}")
+
+
+def sweep_dense(ga, torch, dev, st, rank, reps=10):
+    """The dense masked workload: B=2, H=8, S=2048, D=64, causal and causal
+    sliding W=512, 128x128 lists. FLOPs count the allowed pairs."""
+    from block_sparse_attention_tma_gb300.synth import make_inputs
     Bd, Hd, Sd, Dd = 2, 8, 2048, 64
     x = make_inputs(Bd, Hd, Sd, Sd, Dd, Dd, "bf16", seed=42 + rank)
     gd = {k: t.to(dev) for k, t in x.items()}
@@ -452,21 +466,27 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
     dense = {}
     for name, kw, kind in (("causal", dict(kind=ga.CAUSAL), "causal"),
                            ("sliding_w512", dict(kind=ga.SLIDING, window_left=512), "sliding")):
-        fms, bms = time_fwd_bwd(ga, torch, st, gd, ga.MaskSpec(**kw), dl)
+        fms, bms = time_fwd_bwd(ga, torch, st, gd, ga.MaskSpec(**kw), dl, reps=reps)
         n = Bd * Hd * mask_pairs(kind, Sd, window_left=kw.get("window_left", -1))
         dense[name] = {"fwd_ms": round(fms, 4), "bwd_ms": round(bms, 4),
                        "fwd_tflops": round(2 * n * 2 * Dd / (fms * 1e-3) / 1e12, 1),
                        "bwd_tflops": round(2 * n * 5 * Dd / (bms * 1e-3) / 1e12, 1)}
     dense["config"] = f"B={Bd} H={Hd} Sq=Sk={Sd} D={Dd} bf16, kernel tiles 128x128"
-    del gd, dl
+    return dense
+
+
+def sweep_dynamic(ga, torch, dev, st, rank, dims=(32, 64), reps=10):
+    """The dynamic top-k workload: B=1, H=16, S=8192, top-2048 keys per head by
+    an N(0,1) key bias, with causal; kept keys streamed compacted."""
+    from block_sparse_attention_tma_gb300.synth import make_inputs
     dyn = {}
     Bd, Hd, Sd, topk = 1, 16, 8192, 2048
-    for D in (32, 64):
+    for D in dims:
         x = make_inputs(Bd, Hd, Sd, Sd, D, D, "bf16", seed=42 + rank, bias=True)
         gd = {k: t.to(dev) for k, t in x.items()}
         spec = ga.MaskSpec(kind=ga.DYNAMIC_TOPK, topk=topk, key_bias=gd["key_bias"])
         dl = ga.alloc_block_lists(Bd, Hd, Sd, Sd, 128, 128, device=dev)
-        fms, bms = time_fwd_bwd(ga, torch, st, gd, spec, dl)
+        fms, bms = time_fwd_bwd(ga, torch, st, gd, spec, dl, reps=reps)
         # pairs: every kept key p is seen by the rows p .. S-1
         kept = torch.topk(x["key_bias"].double(), topk, dim=-1).indices
         n = int((Sd - kept).sum())
@@ -474,12 +494,21 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
                         "fwd_tflops": round(2 * n * 2 * D / (fms * 1e-3) / 1e12, 1),
                         "bwd_tflops": round(2 * n * 5 * D / (bms * 1e-3) / 1e12, 1)}
         del gd, dl
+    dyn["config"] = (f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) key bias, with causal; "
+                     "kept keys streamed compacted")
+    return dyn
+
+
+def run_workload_sweep(ga, torch, dev, st, g, rank):
+    """The informational lines beside the step: the 16K MLA prefill's other
+    mask kinds (and the CTA-pair dK/dV kernel), the dense masked workload and
+    the dynamic top-k workload. Not part of the step; FLOPs count the allowed
+    pairs (fwd 2N(Dqk+Dv), bwd 2N(3Dqk+2Dv))."""
+    masks = sweep_masks(ga, torch, dev, st, g)
+    dense = sweep_dense(ga, torch, dev, st, rank)
+    dyn = sweep_dynamic(ga, torch, dev, st, rank)
     torch.cuda.empty_cache()
-    return {"dense2k": dense,
-            "mla16k_mask_kinds": dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
-                                                     f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}"),
-            "dynamic_topk": dict(dyn, config=f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) "
-                                             "key bias, with causal; kept keys streamed compacted")}
+    return {"dense2k": dense, "mla16k_mask_kinds": masks, "dynamic_topk": dyn}
 
 
 def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=4):
@@ -661,8 +690,9 @@ def main():
     ap.add_argument("--no-extensions", action="store_true", help="skip the informational lines (paged GQA decode, mask-kind and dynamic sweeps)")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")
     ap.add_argument("--ref-seq", type=int, default=4096, help="sequence length of the reference-arm sample")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "gqa"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "gqa", "dense2k", "dynamic"], default="all",
                     help="time one part only (profiling runs); prints a short line, not the bench line")
+    ap.add_argument("--dyn-d", type=int, default=0, help="head dim of the dynamic workload (--only dynamic; 0 = 32 and 64)")
     ap.add_argument("--gqa-sk", type=int, default=65536, help="keys of the grouped-query decode (--only gqa)")
     ap.add_argument("--decode-sk", type=int, default=DECODE["Sk"], help="decode keys (profiling runs only)")
     args = ap.parse_args()
@@ -682,14 +712,21 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.only == "all" and args.decode_sk != DECODE["Sk"]:
         ap.error("--decode-sk is for profiling runs with --only")
-    if args.only == "gqa":
+    if args.only in ("gqa", "dense2k", "dynamic"):
         import torch
         import block_sparse_attention_tma_gb300 as ga
         dev = torch.device("cuda", local_rank)
         torch.cuda.set_device(dev)
-        ext = run_extensions(ga, torch, dev, torch.cuda.current_stream(dev), rank, Sk=args.gqa_sk)
+        st = torch.cuda.current_stream(dev)
+        if args.only == "gqa":
+            ext = run_extensions(ga, torch, dev, st, rank, Sk=args.gqa_sk)
+        elif args.only == "dense2k":
+            ext = {"dense2k": sweep_dense(ga, torch, dev, st, rank, reps=args.steps)}
+        else:
+            ext = {"dynamic_topk": sweep_dynamic(ga, torch, dev, st, rank, dims=(args.dyn_d,) if args.dyn_d else (32, 64),
+                                                 reps=args.steps)}
         if rank == 0:
-            print(json.dumps({"only": "gqa", **ext}), flush=True)
+            print(json.dumps({"only": args.only, **ext}), flush=True)
     else:
         out = run_ours(args, rank, world, local_rank)
         if rank == 0 and out is not None:

@@ -30,6 +30,8 @@ struct BwdParams {
   const int32_t* kidx; // [BH][Sk] kept key indices (gathered keys)
   const __nv_bfloat16 *gk, *gv;  // K [B*H*Sk, Dqk], V [B*H*Sk, Dv] (gathered keys)
   unsigned long long wait_ns;     // time limit of every wait (0 = kWaitLimitNs)
+  int hgroup;                     // dQ grid order: query heads per group (head_group), 0 = none
+  int hgroup_kv;                  // dK/dV grid order: key/value heads per group
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -140,9 +140,10 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqt = (p.Sq + 127) / 128;
-  const int bh = blockIdx.x % BH;
+  int bh, qt;
+  grid_tile(blockIdx.x, BH, nqt, p.hgroup, &bh, &qt);
   const int bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
-  const int q0 = (nqt - 1 - (int)(blockIdx.x / BH)) * 128;
+  const int q0 = (nqt - 1 - qt) * 128;  // heaviest (last) query tiles first
   constexpr bool gat = GAT;  // gathered keys (compile-time: the list walk keeps its own code)
   const int Skv = p.Skv;
   const int delta = p.Sk - p.Sq;
@@ -640,6 +641,10 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   float* lse2 = reinterpret_cast<float*>(w + vec_bytes);
   prm.delta = delta;
   prm.lse2 = lse2;
+  // heads grouped so that a wave's streamed tiles stay in L2 (the dQ grid
+  // streams K / V, the dK/dV grid Q / dO of every query head of its group)
+  prm.hgroup = head_group(BH, (long long)prm.Skv * (s.Dqk + s.Dv) * 2 / prm.G);
+  prm.hgroup_kv = head_group(BHkv, (long long)s.Sq * (s.Dqk + s.Dv) * 2 * prm.G);
   prm.dq = static_cast<__nv_bfloat16*>(dq);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);

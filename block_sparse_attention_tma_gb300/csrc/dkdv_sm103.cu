@@ -70,8 +70,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BHkv = p.B * p.Hkv;
-  const int bkv = blockIdx.x % BHkv;  // key/value head of this CTA
-  const int k0 = (blockIdx.x / BHkv) * 128;
+  int bkv, kt;  // key/value head of this CTA and its key tile
+  grid_tile(blockIdx.x, BHkv, (p.Skv + 127) / 128, p.hgroup_kv, &bkv, &kt);
+  const int k0 = kt * 128;
   // query heads bq0 .. bq0 + G - 1 share this key/value head (GQA); their
   // tiles are walked one head after the other and accumulate into the same
   // dK / dV. A walked tile's start is g * SqP + q0 (g = query head in the group).

@@ -61,6 +61,7 @@ struct FwdParams {
   const int32_t* kidx; // [B*H, Sk] kept key indices (gathered keys)
   const __nv_bfloat16 *gk, *gv;  // K [B*H*Sk, Dqk], V [B*H*Sk, Dv] (gathered keys)
   int sub;             // sparse_n / 128
+  int hgroup;          // CTA order: heads per group (head_group), 0 = none
   int nqb, nkb, sparse_m;
   const int32_t *mcnt, *midx, *fcnt, *fidx;  // forward lists
   __nv_bfloat16* o;
@@ -188,8 +189,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       pb = p.Sq - 1;
     }
   } else {
-    const int qt = p.nqt - 1 - L / BH;  // heaviest (last) query tiles first
-    bh = L % BH;
+    int t;
+    grid_tile(L, BH, p.nqt, p.hgroup, &bh, &t);
+    const int qt = p.nqt - 1 - t;  // heaviest (last) query tiles first
     bkv = (bh / p.H) * p.Hkv + (bh % p.H) / p.G;  // key/value head of this query head
     q0 = qt * 128;
   }
@@ -763,6 +765,8 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   }
   prm.o = reinterpret_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
+  // heads grouped so that a wave's K / V tiles stay in L2
+  prm.hgroup = head_group(BH, (long long)(m.gather ? m.kept : s.Sk) * (s.Dqk + s.Dv) * 2 / (s.H / s.Hkv));
   const int grid = prm.nqt * BH;
   if (s.Dqk == 32 && s.Dv == 32) return launch_fwd_cap<32, 32>(prm, grid, cap, st);
   if (s.Dqk == 64 && s.Dv == 64) return launch_fwd_cap<64, 64>(prm, grid, cap, st);

@@ -35,6 +35,36 @@ inline int ensure_smem(K kern, int bytes, std::atomic<unsigned long long>& done)
   return GBATTN_OK;
 }
 
+// CTA order of the prefill kernels: heads are taken in groups of this many,
+// each group's tiles in the kernel's own (heaviest-first) order, so that the
+// tiles in flight stream the operands of a few heads only and those stay in
+// L2. 0 (no grouping) when every head's streamed bytes fit in half the L2
+// anyway; otherwise as many heads as fit in 48 MB (at least 1).
+inline int head_group(long long heads, long long bytes_per_head) {
+  constexpr long long kHalfL2 = 64ll << 20, kGroupBytes = 48ll << 20;
+  if (heads <= 1 || bytes_per_head <= 0 || heads * bytes_per_head <= kHalfL2) return 0;
+  const long long g = kGroupBytes / bytes_per_head;
+  return (int)(g < 1 ? 1 : (g >= heads ? 0 : g));
+}
+
+// Tile of block b in a grid of `heads` x `ntiles` CTAs: head h and tile
+// index t (0 = the first tile in the kernel's order), with heads grouped by
+// `grp` (0: tile-major over all heads, head = b % heads).
+__host__ __device__ inline void grid_tile(int b, int heads, int ntiles, int grp, int* h, int* t) {
+  if (grp <= 0) {
+    *h = b % heads;
+    *t = b / heads;
+    return;
+  }
+  const int ngr = (heads + grp - 1) / grp;
+  int g = b / (grp * ntiles);
+  if (g > ngr - 1) g = ngr - 1;
+  const int r = b - g * grp * ntiles;
+  const int gs = heads - g * grp < grp ? heads - g * grp : grp;
+  *h = g * grp + r % gs;
+  *t = r / gs;
+}
+
 // Largest number of query heads per key/value head (GQA group) the
 // tensor-core backward accepts.
 constexpr int kMaxGroup = 128;

@@ -94,13 +94,18 @@ struct FwdCfg {
   // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
   // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2][4 lane quarters], fin, o_fin
   static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 8 + 1 + 1;
-  static constexpr int THREADS = 320;
+  // softmax warps: NG per TMEM lane quarter, each thread one query row and
+  // CWF = 128 / NG of the tile's key columns. NG = 4 (18 warps) caps a thread
+  // at 96 registers and measured slower (16K causal MLA 1.091 -> 1.243 ms),
+  // so every shape keeps two.
+  static constexpr int NG = 2, CWF = 128 / NG;
+  static constexpr int THREADS = 64 + 128 * NG;
   // + 4 KB tail slack; at least 120 KB so that one CTA holds an SM (its 512
   // TMEM columns are the whole TMEM)
-  // colterm [8 warps][2][64] + row-max exchange [2][2][128] + row sums [2][128]
+  // colterm [4 NG warps][2][CWF] + row-max exchange [2][NG][128] + row sums [NG][128]
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
-  static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 4 * 128 * 4 + 2 * 128 * 4 +
-                                   TCAP * 2 + NBAR * 8 + 32 + 2048;
+  static constexpr int SMEM_USED = 1024 + QTILE + KST * QTILE + VST * VTILE + 8 * 128 * 4 + 2 * NG * 128 * 4 +
+                                   NG * 128 * 4 + TCAP * 2 + NBAR * 8 + 32 + 2048;
   static constexpr int SMEM = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, DV, false, true);
@@ -119,16 +124,16 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t* r) {
 }
 
 template <int DQK, int DV, bool CAP, bool GAT, bool PK = false>
-__global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(FwdCfg<DQK, DV>::THREADS, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sK = sQ + C::QTILE;
   uint8_t* sV = sK + C::KST * C::QTILE;
-  float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [8 warps][2][64]
-  float* xmax = colterm + 8 * 128;                                     // [2][2 halves][128 rows]
-  float* xsum = xmax + 4 * 128;                                        // [2 halves][128 rows]
+float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG warps][2][CWF]
+  float* xmax = colterm + 8 * 128;                                     // [2][NG column groups][128 rows]
+  float* xsum = xmax + 2 * C::NG * 128;                                // [NG column groups][128 rows]
   uint16_t* tlist = reinterpret_cast<uint16_t*>(xsum + 2 * 128);  // [TCAP]
   uint64_t* bars = reinterpret_cast<uint64_t*>(tlist + C::TCAP);
   uint64_t* q_full = bars;
@@ -251,11 +256,11 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     // gathered tiles: one arrival per producer lane once its copies landed
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, GAT ? 32 : 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, GAT ? 32 : 1); mbar_init(v_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 256); }
-    for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 64);
+    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128 * C::NG); }
+    for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 32 * C::NG);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
-    mbar_init(fin, 256);
+    mbar_init(fin, 128 * C::NG);
     mbar_init(o_fin, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -417,8 +422,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int sw = warp - 2;       // 0..7
-    const int grp = sw >> 2;       // which half of the key columns
+    constexpr int NG = C::NG, CWF = C::CWF;
+    const int sw = warp - 2;       // 0 .. 4 NG - 1
+    const int grp = sw >> 2;       // which group of CWF key columns
     const int quarter = warp & 3;  // TMEM lane quarter
     const int row = quarter * 32 + lane;
     // query position of this row (the row itself, or its position within its
@@ -427,8 +433,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     const bool valid = PK ? q0 + row < p.pk_R : i < p.Sq;
     const bool wact = !PK || q0 + quarter * 32 < p.pk_R;  // some row of this warp exists
     const size_t orow_id = PK ? (size_t)row_base + q0 + row : (size_t)bh * p.Sq + i;
-    const int cb = grp * 64;       // first S column of this thread
-    constexpr int DVH = DV / 2;    // O columns of this thread
+    const int cb = grp * CWF;      // first S column of this thread
+    constexpr int DVH = DV / NG;   // O columns of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     int lo = 0, hi;
     if constexpr (GAT) hi = gathered_row_hi(keep_h, p.mask.nkw, q0 + quarter * 32 + delta);
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
     auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
     int kv0;
     bool masked;
-    auto kt = key_terms<GAT>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
+    auto kt = key_terms<GAT, CWF / 32>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
     while (ok && it.next(&kv0, &masked)) {
       const int sb = n & 1;
       if constexpr (PK) {
@@ -482,9 +488,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
           continue;
         }
       }
-      // per-key score term (key bias - slope * j) * log2(e) of this warp's 64
+      // per-key score term (key bias - slope * j) * log2(e) of this warp's CWF
       // columns; each warp keeps its own copy, so only a warp sync is needed
-      float* ctw = colterm + (sw * 2 + sb) * 64;
+      float* ctw = colterm + (sw * 2 + sb) * CWF;
       kt.emit(kv0, ctw);
       __syncwarp();
       ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
@@ -493,15 +499,15 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         break;
       }
       tc_fence_after();
-      float t[64];
+      float t[CWF];
       tmem_ld32(tl + sb * 128 + cb, reinterpret_cast<uint32_t*>(t));
-      tmem_ld32(tl + sb * 128 + cb + 32, reinterpret_cast<uint32_t*>(t) + 32);
+      if constexpr (CWF == 64) tmem_ld32(tl + sb * 128 + cb + 32, reinterpret_cast<uint32_t*>(t) + 32);
       tmem_wait_ld32(reinterpret_cast<uint32_t*>(t));
-      reg_fence32(reinterpret_cast<uint32_t*>(t) + 32);
+      if constexpr (CWF == 64) reg_fence32(reinterpret_cast<uint32_t*>(t) + 32);
       {
         const float4* ct = reinterpret_cast<const float4*>(ctw);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
+        for (int c4 = 0; c4 < CWF / 4; ++c4) {
           const float4 v4 = ct[c4];
           const int c = 4 * c4;
           if constexpr (CAP) {
@@ -518,34 +524,39 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         const int clo = lo - kv0 - cb;
         const int chi = min(hi, Skv - 1) - kv0 - cb;
         if (keep) {
-          uint32_t kw[2];
+          uint32_t kw[CWF / 32];
 #pragma unroll
-          for (int w = 0; w < 2; ++w) {
+          for (int w = 0; w < CWF / 32; ++w) {
             const int wi = ((kv0 + cb) >> 5) + w;
             kw[w] = wi < p.mask.nkw ? __ldg(keep + wi) : 0u;
           }
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < CWF; ++c) {
             const bool okc = (c >= clo) && (c <= chi) && ((kw[c >> 5] >> (c & 31)) & 1u);
             t[c] = okc ? t[c] : -INFINITY;
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
+          for (int c = 0; c < CWF; ++c) t[c] = (c >= clo && c <= chi) ? t[c] : -INFINITY;
         }
       }
-      // row max: 8 independent chains over this half (three-input max), then
-      // the other half's
+      // row max: 8 independent chains over this thread's columns (three-input
+      // max), then the other column groups'
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        mx[e] = max3(t[e], t[e + 8], t[e + 16]);
-        mx[e] = max3(mx[e], t[e + 24], t[e + 32]);
-        mx[e] = max3(mx[e], t[e + 40], t[e + 48]);
-        mx[e] = fmaxf(mx[e], t[e + 56]);
+        if constexpr (CWF == 64) {
+          mx[e] = max3(t[e], t[e + 8], t[e + 16]);
+          mx[e] = max3(mx[e], t[e + 24], t[e + 32]);
+          mx[e] = max3(mx[e], t[e + 40], t[e + 48]);
+          mx[e] = fmaxf(mx[e], t[e + 56]);
+        } else {
+          mx[e] = max3(t[e], t[e + 8], t[e + 16]);
+          mx[e] = fmaxf(mx[e], t[e + 24]);
+        }
       }
       float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      float* xm = xmax + sb * 256;
+      float* xm = xmax + sb * NG * 128;
       xm[grp * 128 + row] = mt;
       mbar_arrive(xbar + sb * 4 + quarter);
       ok = mbar_wait(xbar + sb * 4 + quarter, (n >> 1) & 1, abort_flag);
@@ -553,7 +564,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         ok = false;
         break;
       }
-      mt = fmaxf(mt, xm[(grp ^ 1) * 128 + row]);
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+        if (g != grp) mt = fmaxf(mt, xm[g * 128 + row]);
       float m_use = m_run, alpha = 1.f;
       bool resc = false;
       if (mt > m_run + 8.0f) {
@@ -567,9 +580,9 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
       float ls[8];  // four chains of column pairs
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[CWF / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < CWF / 2; ++c) {
         float d0, d1;
         sub2(d0, d1, t[2 * c], t[2 * c + 1], msafe, msafe);
         const float a0 = ex2(d0);
@@ -610,7 +623,8 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
           tmem_st16(tl + C::T_O + grp * DVH, orr);
         }
       }
-      tmem_st32(tl + sb * 128 + grp * 32, pk);
+      if constexpr (CWF == 64) tmem_st32(tl + sb * 128 + grp * 32, pk);
+      else tmem_st16(tl + sb * 128 + grp * 16, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + sb);
@@ -623,7 +637,10 @@ __global__ void __launch_bounds__(320, 1) fwd_bf16_kernel(const __grid_constant_
         xsum[grp * 128 + row] = l_run;
         mbar_arrive(fin);
         ok = __all_sync(0xffffffffu, mbar_wait(fin, 0, abort_flag));
-        if (ok) l_tot = xsum[row] + xsum[128 + row];
+        if (ok) {
+#pragma unroll
+          for (int g = 0; g < NG; ++g) l_tot += xsum[g * 128 + row];
+        }
       }
       if (ok) {
         const bool live = n > 0 && l_tot > 0.f;

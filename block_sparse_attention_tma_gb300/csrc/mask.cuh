@@ -329,15 +329,15 @@ __device__ __forceinline__ TileSeq<SlotFn> tile_seq(SlotFn slot, const uint16_t*
 // tile n + 2 and the bias values of tile n + 1 are loaded, so the dependent
 // index -> bias loads never stall the caller. `seq` must be a copy of the
 // caller's tile sequence taken before its first next().
-template <bool GAT, class Seq>
+template <bool GAT, class Seq, int NV = 2>
 struct KeyTerms {
   Seq ahead;
   const float* kb;   // key bias of this head, or nullptr
   const int32_t* pos;  // gathered keys: original index of each compact key
   int skv, col0;       // streamed key extent; col0 = cb + lane
   float slope;
-  int jo_cur[2], jo_nx[2];
-  float bv_cur[2];
+  int jo_cur[NV], jo_nx[NV];
+  float bv_cur[NV];
 
   __device__ __forceinline__ int key_of(int st, int e) const {
     const int j = st + col0 + e * 32;
@@ -347,7 +347,7 @@ struct KeyTerms {
   }
   __device__ __forceinline__ void start() {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int e = 0; e < NV; ++e) {
       jo_cur[e] = jo_nx[e] = -1;
       bv_cur[e] = 0.f;
     }
@@ -356,13 +356,13 @@ struct KeyTerms {
     bool mk;
     if (ahead.next(&st, &mk)) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) jo_cur[e] = key_of(st, e);
+      for (int e = 0; e < NV; ++e) jo_cur[e] = key_of(st, e);
     }
 #pragma unroll
-    for (int e = 0; e < 2; ++e) bv_cur[e] = jo_cur[e] >= 0 ? __ldg(kb + jo_cur[e]) : 0.f;
+    for (int e = 0; e < NV; ++e) bv_cur[e] = jo_cur[e] >= 0 ? __ldg(kb + jo_cur[e]) : 0.f;
     if (ahead.next(&st, &mk)) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) jo_nx[e] = key_of(st, e);
+      for (int e = 0; e < NV; ++e) jo_nx[e] = key_of(st, e);
     }
   }
   // Writes this lane's two terms of the tile starting at compact key kv0
@@ -370,24 +370,26 @@ struct KeyTerms {
   __device__ __forceinline__ void emit(int kv0, float* ct) {
     if (kb) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
+      for (int e = 0; e < NV; ++e)
         ct[e * 32 + (col0 & 31)] = jo_cur[e] >= 0 ? (bv_cur[e] - slope * (float)jo_cur[e]) * kLog2e : 0.f;
       int st;
       bool mk;
-      int jo_n2[2] = {-1, -1};
+      int jo_n2[NV];
+#pragma unroll
+      for (int e = 0; e < NV; ++e) jo_n2[e] = -1;
       if (ahead.next(&st, &mk)) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) jo_n2[e] = key_of(st, e);
+        for (int e = 0; e < NV; ++e) jo_n2[e] = key_of(st, e);
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
+      for (int e = 0; e < NV; ++e) {
         bv_cur[e] = jo_nx[e] >= 0 ? __ldg(kb + jo_nx[e]) : 0.f;
         jo_cur[e] = jo_nx[e];
         jo_nx[e] = jo_n2[e];
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
+      for (int e = 0; e < NV; ++e) {
         const int jo = key_of(kv0, e);
         ct[e * 32 + (col0 & 31)] = jo >= 0 ? -slope * (float)jo * kLog2e : 0.f;
       }
@@ -407,10 +409,10 @@ struct KeyTermsDirect {
     }
   }
 };
-template <bool GAT, class Seq>
-__device__ __forceinline__ KeyTerms<GAT, Seq> key_terms(const Seq& seq, const float* kb, const int32_t* pos, int skv,
-                                                       int col0, float slope) {
-  KeyTerms<GAT, Seq> t{seq, kb, pos, skv, col0, slope, {-1, -1}, {-1, -1}, {0.f, 0.f}};
+template <bool GAT, int NV = 2, class Seq>
+__device__ __forceinline__ KeyTerms<GAT, Seq, NV> key_terms(const Seq& seq, const float* kb, const int32_t* pos,
+                                                           int skv, int col0, float slope) {
+  KeyTerms<GAT, Seq, NV> t{seq, kb, pos, skv, col0, slope, {}, {}, {}};
   t.start();
   return t;
 }

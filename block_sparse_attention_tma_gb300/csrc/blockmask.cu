@@ -189,53 +189,66 @@ __device__ int block_class(const ListArgs& a, int bh, int r, int c) {
   return 1;
 }
 
-// One warp per (b, h, q-block): forward lists.
-__global__ void fwd_lists_kernel(ListArgs a) {
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (gw >= (long long)a.BH * a.nqb) return;
-  const int bh = (int)(gw / a.nqb), r = (int)(gw % a.nqb);
-  const int lane = threadIdx.x & 31;
-  const size_t row = (size_t)bh * a.nqb + r;
-  int nm = 0, nf = 0;
-  for (int c = 0; c < a.nkb; ++c) {
-    const int cls = block_class(a, bh, r, c);
-    if (lane == 0) {
-      if (cls == 1) a.q_mask_idx[row * a.nkb + nm] = c;
-      if (cls == 2) a.q_full_idx[row * a.nkb + nf] = c;
-    }
-    nm += cls == 1;
-    nf += cls == 2;
-  }
-  for (int t = nm + lane; t < a.nkb; t += 32) a.q_mask_idx[row * a.nkb + t] = 0;
-  for (int t = nf + lane; t < a.nkb; t += 32) a.q_full_idx[row * a.nkb + t] = 0;
-  if (lane == 0) {
-    a.q_mask_cnt[row] = nm;
-    a.q_full_cnt[row] = nf;
-  }
-}
+constexpr int kListWarps = 8, kListChunk = 256;
 
-// One warp per (b, h, k-block): backward lists.
-__global__ void bwd_lists_kernel(ListArgs a) {
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (gw >= (long long)a.BH * a.nkb) return;
-  const int bh = (int)(gw / a.nkb), c = (int)(gw % a.nkb);
-  const int lane = threadIdx.x & 31;
-  const size_t col = (size_t)bh * a.nkb + c;
-  int nm = 0, nf = 0;
-  for (int r = 0; r < a.nqb; ++r) {
-    const int cls = block_class(a, bh, r, c);
-    if (lane == 0) {
-      if (cls == 1) a.k_mask_idx[col * a.nqb + nm] = r;
-      if (cls == 2) a.k_full_idx[col * a.nqb + nf] = r;
+// One CTA per (b, h, fixed block): the list of the streamed blocks of that
+// block row (forward: fixed = q-block, streamed = k-blocks) or column
+// (backward: fixed = k-block, streamed = q-blocks). The streamed blocks are
+// taken in chunks of 256; each of the 8 warps classifies every 8th block of
+// the chunk (one warp-collective pair count per block), then the 256 threads
+// compact the chunk's mask and full entries in ascending order with a
+// block-wide scan. Tail entries are 0.
+template <bool FWD>
+__global__ void __launch_bounds__(kListWarps * 32) lists_kernel(ListArgs a) {
+  __shared__ unsigned char cls[kListChunk];
+  __shared__ int wsum[2][kListWarps];
+  __shared__ int s_base[2];
+  const int nfix = FWD ? a.nqb : a.nkb, nstr = FWD ? a.nkb : a.nqb;
+  const int bh = blockIdx.x / nfix, f = blockIdx.x % nfix;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)bh * nfix + f;
+  int32_t* midx = (FWD ? a.q_mask_idx : a.k_mask_idx) + row * nstr;
+  int32_t* fidx = (FWD ? a.q_full_idx : a.k_full_idx) + row * nstr;
+  if (threadIdx.x == 0) s_base[0] = s_base[1] = 0;
+  for (int c0 = 0; c0 < nstr; c0 += kListChunk) {
+    const int n = min(kListChunk, nstr - c0);
+    for (int j = warp; j < n; j += kListWarps) {
+      const int sb = c0 + j;
+      const int cl = FWD ? block_class(a, bh, f, sb) : block_class(a, bh, sb, f);
+      if (lane == 0) cls[j] = (unsigned char)cl;
     }
-    nm += cls == 1;
-    nf += cls == 2;
+    __syncthreads();
+    const int t = threadIdx.x;
+    const int cl = t < n ? cls[t] : 0;
+    const unsigned bm = __ballot_sync(0xffffffffu, cl == 1), bf = __ballot_sync(0xffffffffu, cl == 2);
+    if (lane == 0) {
+      wsum[0][warp] = __popc(bm);
+      wsum[1][warp] = __popc(bf);
+    }
+    __syncthreads();
+    int om = s_base[0], of = s_base[1];
+    for (int w = 0; w < warp; ++w) {
+      om += wsum[0][w];
+      of += wsum[1][w];
+    }
+    const unsigned below = (1u << lane) - 1u;
+    if (cl == 1) midx[om + __popc(bm & below)] = c0 + t;
+    if (cl == 2) fidx[of + __popc(bf & below)] = c0 + t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 0; w < kListWarps; ++w) {
+        s_base[0] += wsum[0][w];
+        s_base[1] += wsum[1][w];
+      }
+    }
+    __syncthreads();
   }
-  for (int t = nm + lane; t < a.nqb; t += 32) a.k_mask_idx[col * a.nqb + t] = 0;
-  for (int t = nf + lane; t < a.nqb; t += 32) a.k_full_idx[col * a.nqb + t] = 0;
-  if (lane == 0) {
-    a.k_mask_cnt[col] = nm;
-    a.k_full_cnt[col] = nf;
+  const int nm = s_base[0], nf = s_base[1];
+  for (int t = nm + threadIdx.x; t < nstr; t += blockDim.x) midx[t] = 0;
+  for (int t = nf + threadIdx.x; t < nstr; t += blockDim.x) fidx[t] = 0;
+  if (threadIdx.x == 0) {
+    (FWD ? a.q_mask_cnt : a.k_mask_cnt)[row] = nm;
+    (FWD ? a.q_full_cnt : a.k_full_cnt)[row] = nf;
   }
 }
 
@@ -273,10 +286,11 @@ int blockmask_launch(int B, int H, int Sq, int Sk, const HostMask& m, const gbat
       if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
     }
   }
-  const long long wf = (long long)a.BH * a.nqb, wb = (long long)a.BH * a.nkb;
-  fwd_lists_kernel<<<(unsigned)((wf * 32 + 127) / 128), 128, 0, st>>>(a);
+  const long long cf = (long long)a.BH * a.nqb, cb = (long long)a.BH * a.nkb;
+  if (cf >= (1ll << 31) || cb >= (1ll << 31)) return GBATTN_ERR_ARG;
+  lists_kernel<true><<<(unsigned)cf, kListWarps * 32, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
-  bwd_lists_kernel<<<(unsigned)((wb * 32 + 127) / 128), 128, 0, st>>>(a);
+  lists_kernel<false><<<(unsigned)cb, kListWarps * 32, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
   return GBATTN_OK;
 }

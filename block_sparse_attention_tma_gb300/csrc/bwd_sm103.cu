@@ -59,31 +59,40 @@ __global__ void unkept_zero_kernel(const uint32_t* __restrict__ keep, int nkw, i
 
 
 // ------------------------------------------------------------------ preprocess
+// DV / 8 lanes per row, each loading 16 bytes (8 elements) of O and of dO; a
+// warp covers 256 / DV rows, so every load instruction moves 512 contiguous
+// bytes of each tensor.
+template <int DV>
 __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ g,
-                               const float* __restrict__ lse, int BH, int Sq, int sq_pad, int Dv, float slope_log2,
+                               const float* __restrict__ lse, int BH, int Sq, int sq_pad, float slope_log2,
                                float* __restrict__ delta, float* __restrict__ lse2) {
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int LPR = DV / 8, RPW = 32 / LPR;
   const int lane = threadIdx.x & 31;
-  if (gw >= (long long)BH * sq_pad) return;
-  const int bh = (int)(gw / sq_pad), i = (int)(gw % sq_pad);
+  const long long gr = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * RPW + lane / LPR;  // padded row
+  // every lane stays for the shuffles below; lanes past the last row skip the memory accesses
+  const bool in = gr < (long long)BH * sq_pad;
+  const int sub = lane % LPR;
+  const int bh = in ? (int)(gr / sq_pad) : 0, i = in ? (int)(gr % sq_pad) : 0;
   float d = 0.f, l2 = INFINITY;
-  if (i < Sq) {
+  if (in && i < Sq) {
     const size_t row = (size_t)bh * Sq + i;
-    const __nv_bfloat16* orow = o + row * Dv;
-    const __nv_bfloat16* grow = g + row * Dv;
-    for (int c = 2 * lane; c < Dv; c += 64) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(orow + c));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(grow + c));
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + row * DV + sub * 8);
+    const uint4 gv = *reinterpret_cast<const uint4*>(g + row * DV + sub * 8);
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
       d = fmaf(a.x, b.x, fmaf(a.y, b.y, d));
     }
     const float L = lse[row];
     l2 = (L == -INFINITY) ? INFINITY : L * kLog2e - slope_log2 * (float)i;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-  if (lane == 0) {
-    delta[gw] = d;
-    lse2[gw] = l2;
+  for (int off = LPR / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+  if (in && sub == 0) {
+    delta[gr] = d;
+    lse2[gr] = l2;
   }
 }
 
@@ -649,11 +658,18 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
 
-  const long long rows = (long long)BH * prm.sq_pad;
-  bwd_pre_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, BH, s.Sq, prm.sq_pad, s.Dv,
-      m.slope * kLog2e, delta, lse2);
-  if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  {
+    const long long rows = (long long)BH * prm.sq_pad;
+    const int rpw = 256 / s.Dv;  // rows per warp
+    const unsigned blocks = (unsigned)(((rows + rpw - 1) / rpw * 32 + 255) / 256);
+    const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(o);
+    const __nv_bfloat16* gb_ = static_cast<const __nv_bfloat16*>(dout);
+    const float sl2 = m.slope * kLog2e;
+    if (s.Dv == 128) bwd_pre_kernel<128><<<blocks, 256, 0, st>>>(ob, gb_, lse, BH, s.Sq, prm.sq_pad, sl2, delta, lse2);
+    else if (s.Dv == 64) bwd_pre_kernel<64><<<blocks, 256, 0, st>>>(ob, gb_, lse, BH, s.Sq, prm.sq_pad, sl2, delta, lse2);
+    else bwd_pre_kernel<32><<<blocks, 256, 0, st>>>(ob, gb_, lse, BH, s.Sq, prm.sq_pad, sl2, delta, lse2);
+    if (cudaGetLastError() != cudaSuccess) return GBATTN_ERR_CUDA;
+  }
   if (m.gather) {
     // rows of the keys outside the keep set: zero gradients
     const long long warps = (long long)BH * prm.mask.nkw;

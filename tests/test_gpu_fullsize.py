@@ -184,3 +184,35 @@ def test_gqa_decode_32x32x65536(Hkv, paged, n):
         check_lse(f64(lse[b, h]), l_ref)
     del x
     torch.cuda.empty_cache()
+
+
+def test_gqa_16k_head_grouped_order():
+    """Grouped-query attention at a size where the prefill kernels take the
+    heads in groups (the dK/dV grid's per-key/value-head Q + dO bytes exceed
+    half the L2): 1 x 8 query heads on 2 key/value heads x 16384, 128/128,
+    causal, 256 x 512 lists. Sampled rows of O / LSE / dQ for query heads of
+    both groups, and sampled key columns of dK / dV for both key/value heads,
+    each the sum over its four query heads."""
+    B, H, Hkv, S, D = 1, 8, 2, 16384, 128
+    c = Case(B, H, S, S, D, D, "causal", sparse=(256, 512), Hkv=Hkv)
+    o, lse = c.fwd()
+    dq, dk, dv = c.bwd(o, lse)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    G = H // Hkv
+    rows, cols = sample_idx(S, k=48, seed=5), sample_idx(S, k=48, seed=6)
+    for h in (0, 5):
+        p = c.problem(0, h)
+        o_ref, l_ref = p.forward(rows)
+        check_out(f64(o[0, h])[rows], o_ref)
+        check_lse(f64(lse[0, h])[rows], l_ref)
+        dq_r, _, _, _ = p.backward(c.h["do"][0, h], rows=rows, cols=cols[:1])
+        check_grad(f64(dq[0, h])[rows], dq_r, "dQ")
+    for hk in range(Hkv):
+        dk_sum = dv_sum = 0
+        for g in range(G):
+            h = hk * G + g
+            _, dk_r, dv_r, _ = c.problem(0, h).backward(c.h["do"][0, h], rows=rows[:1], cols=cols)
+            dk_sum, dv_sum = dk_sum + dk_r, dv_sum + dv_r
+        check_grad(f64(dk[0, hk])[cols], dk_sum, "dK")
+        check_grad(f64(dv[0, hk])[cols], dv_sum, "dV")

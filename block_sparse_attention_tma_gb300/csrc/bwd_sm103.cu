@@ -652,8 +652,8 @@ int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.lse2 = lse2;
   // heads grouped so that a wave's streamed tiles stay in L2 (the dQ grid
   // streams K / V, the dK/dV grid Q / dO of every query head of its group)
-  prm.hgroup = head_group(BH, (long long)prm.Skv * (s.Dqk + s.Dv) * 2 / prm.G);
-  prm.hgroup_kv = head_group(BHkv, (long long)s.Sq * (s.Dqk + s.Dv) * 2 * prm.G);
+  prm.hgroup = head_group(BH, (long long)prm.Skv * (s.Dqk + s.Dv) * 2 / prm.G, device_l2_bytes());
+  prm.hgroup_kv = head_group(BHkv, (long long)s.Sq * (s.Dqk + s.Dv) * 2 * prm.G, device_l2_bytes());
   prm.dq = static_cast<__nv_bfloat16*>(dq);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);

@@ -783,7 +783,7 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
   prm.o = reinterpret_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   // heads grouped so that a wave's K / V tiles stay in L2
-  prm.hgroup = head_group(BH, (long long)(m.gather ? m.kept : s.Sk) * (s.Dqk + s.Dv) * 2 / (s.H / s.Hkv));
+  prm.hgroup = head_group(BH, (long long)(m.gather ? m.kept : s.Sk) * (s.Dqk + s.Dv) * 2 / (s.H / s.Hkv), device_l2_bytes());
   const int grid = prm.nqt * BH;
   if (s.Dqk == 32 && s.Dv == 32) return launch_fwd_cap<32, 32>(prm, grid, cap, st);
   if (s.Dqk == 64 && s.Dv == 64) return launch_fwd_cap<64, 64>(prm, grid, cap, st);

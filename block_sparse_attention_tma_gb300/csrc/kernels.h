@@ -35,15 +35,35 @@ inline int ensure_smem(K kern, int bytes, std::atomic<unsigned long long>& done)
   return GBATTN_OK;
 }
 
+// L2 size of the current device in bytes (cached per device ordinal; 128 MB
+// if the query fails).
+inline long long device_l2_bytes() {
+  static std::atomic<long long> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 128ll << 20;
+  }
+  if (dev >= 0 && dev < 64) {
+    const long long c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int l2 = 0;
+  long long v = 128ll << 20;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) == cudaSuccess && l2 > 0) v = l2;
+  else cudaGetLastError();
+  if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
 // CTA order of the prefill kernels: heads are taken in groups of this many,
 // each group's tiles in the kernel's own (heaviest-first) order, so that the
 // tiles in flight stream the operands of a few heads only and those stay in
 // L2. 0 (no grouping) when every head's streamed bytes fit in half the L2
-// anyway; otherwise as many heads as fit in 48 MB (at least 1).
-inline int head_group(long long heads, long long bytes_per_head) {
-  constexpr long long kHalfL2 = 64ll << 20, kGroupBytes = 48ll << 20;
-  if (heads <= 1 || bytes_per_head <= 0 || heads * bytes_per_head <= kHalfL2) return 0;
-  const long long g = kGroupBytes / bytes_per_head;
+// anyway; otherwise as many heads as fit in 3/8 of it (at least 1).
+inline int head_group(long long heads, long long bytes_per_head, long long l2_bytes) {
+  if (heads <= 1 || bytes_per_head <= 0 || heads * bytes_per_head <= l2_bytes / 2) return 0;
+  const long long g = (l2_bytes * 3 / 8) / bytes_per_head;
   return (int)(g < 1 ? 1 : (g >= heads ? 0 : g));
 }
 

@@ -42,6 +42,17 @@ def test_block_mask_bit_exact(kind, Sq, Sk, sm, sn):
     assert_no_device_error()
 
 
+# more than 256 sparse blocks along a list: the list builder compacts each
+# row / column in chunks of 256 blocks, so the entries cross a chunk boundary
+@pytest.mark.parametrize("kind", ["causal", "sliding", "prefix_lm", "none"])
+@pytest.mark.parametrize("Sq,Sk", [(300, 33000), (33000, 300)])
+def test_block_mask_bit_exact_past_256_blocks(kind, Sq, Sk):
+    c = Case(1, 1, Sq, Sk, 64, 64, kind, sparse=(128, 128), prefix_len=20000, window=17000)
+    torch.cuda.synchronize()
+    lists_equal(c, 1, 1, Sq, Sk, 128, 128)
+    assert_no_device_error()
+
+
 @pytest.mark.parametrize("topk", [0, 1, 33, 699, 700, 5000])
 def test_keep_index_bit_exact(topk):
     c = Case(2, 2, 64, 700, 64, 64, "dynamic", topk=topk, sparse=(128, 128))

@@ -18,7 +18,8 @@
 //               into TMEM once. Per tile each thread loads its 64 S values,
 //               masks (partial tiles only), folds scale * log2(e) and the
 //               per-key bias term into one FMA, exchanges its partial row max
-//               with the other half through shared memory, exp2, writes its
+//               with the other half through shared memory (the two warps of a
+//               lane quarter meet at a named barrier per tile), exp2, writes its
 //               half of P (bf16) back over the S buffer, and rescales its half
 //               of O only when the row max grows by more than 2^8 ("lazy"
 //               rescale); final O / l and LSE. Two warps per SM sub-partition
@@ -45,6 +46,20 @@
 #include "mask.cuh"
 
 namespace gb {
+
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads that
+// also returns the OR of their predicates. Every participant must reach it:
+// callers pass their failure flag through it and leave their loop together.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;
@@ -92,8 +107,8 @@ struct FwdCfg {
   static constexpr int T_O = 256, T_Q = 384;
   static_assert(T_Q + DQK / 2 <= 512 && T_O + DV <= T_Q, "TMEM budget");
   // barriers: q_full, q_tmem, k_full[KST], k_empty[KST], v_full[VST],
-  // v_empty[VST], s_full[2], p_full[2], o_done, drain, xmax[2][4 lane quarters], fin, o_fin
-  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 8 + 1 + 1;
+  // v_empty[VST], s_full[2], p_full[2], o_done, drain, fin, o_fin
+  static constexpr int NBAR = 2 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + 1 + 1;
   // softmax warps: NG per TMEM lane quarter, each thread one query row and
   // CWF = 128 / NG of the tile's key columns. NG = 4 (18 warps) caps a thread
   // at 96 registers and measured slower (16K causal MLA 1.091 -> 1.243 ms),
@@ -146,8 +161,7 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 1;
-  uint64_t* xbar = drain + 1;  // [2][4]: the two warps of a lane quarter exchange row maxima
-  uint64_t* fin = xbar + 8;
+  uint64_t* fin = drain + 1;
   // one phase: every PV product of the CTA has completed (the epilogue's wait;
   // a parity wait on o_done there could pass two phases early)
   uint64_t* o_fin = fin + 1;
@@ -257,7 +271,6 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
     for (int i = 0; i < C::KST; ++i) { mbar_init(k_full + i, GAT ? 32 : 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < C::VST; ++i) { mbar_init(v_full + i, GAT ? 32 : 1); mbar_init(v_empty + i, 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128 * C::NG); }
-    for (int i = 0; i < 8; ++i) mbar_init(xbar + i, 32 * C::NG);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(fin, 128 * C::NG);
@@ -475,14 +488,19 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
     int kv0;
     bool masked;
     auto kt = key_terms<GAT, CWF / 32>(it, kb, pos_h, Skv, cb + lane, p.mask.slope);
-    while (ok && it.next(&kv0, &masked)) {
+    // Every softmax warp walks every tile and meets its lane quarter's other
+    // warps at one named barrier per tile (the row-max exchange), which also
+    // ORs their failure flags: a warp whose wait gave up goes on to the next
+    // exchange without waiting and they all leave the loop there, so no warp
+    // is left at a barrier that a departed warp would have to reach.
+    while (it.next(&kv0, &masked)) {
       const int sb = n & 1;
       if constexpr (PK) {
         // packed decode: a warp whose 32 rows hold no query row of the group
         // only keeps the barriers in step (S of this tile is computed, so P
         // of the tile two before is consumed and the arrival cannot run ahead)
         if (!wact) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag)))) break;
+          if (!ok || !(ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag)))) break;
           mbar_arrive(p_full + sb);
           ++n;
           continue;
@@ -493,9 +511,9 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
       float* ctw = colterm + (sw * 2 + sb) * CWF;
       kt.emit(kv0, ctw);
       __syncwarp();
-      ok = mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (n >> 1) & 1, abort_flag));
+      if (!ok) {  // this tile's exchange, reporting the failure: all leave
+        bar_red_or(1 + quarter, 32 * NG, true);
         break;
       }
       tc_fence_after();
@@ -558,9 +576,7 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
       float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       float* xm = xmax + sb * NG * 128;
       xm[grp * 128 + row] = mt;
-      mbar_arrive(xbar + sb * 4 + quarter);
-      ok = mbar_wait(xbar + sb * 4 + quarter, (n >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
+      if (bar_red_or(1 + quarter, 32 * NG, false)) {
         ok = false;
         break;
       }
@@ -598,10 +614,10 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
         // O must not be in flight: PV of the previous tile has completed.
         // (S of this tile was issued after PV of tile n - 2, so at most one
         // o_done phase is outstanding and the parity wait is exact.)
-        ok = mbar_wait(o_done, (n - 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag));
+        if (!ok) {  // reported at the next exchange
+          ++n;
+          continue;
         }
         tc_fence_after();
         if constexpr (DVH >= 32) {

@@ -388,9 +388,17 @@ def mask_pairs(kind, S, window_left=-1, block_size=0, prefix_len=0):
     raise ValueError(kind)
 
 
+SWEEP_TIMING = "device time per call: CUDA graph of calls each followed by a 256 MB L2 flush, flush-only graph subtracted"
+
+
 def time_fwd_bwd(ga, torch, st, g, spec, lists, reps=10):
-    """Mean ms of attn_fwd and of attn_bwd (CUDA events on the launching
-    stream, after 3 warm-up calls of each)."""
+    """Device ms per call of attn_fwd and of attn_bwd. `reps` calls, each
+    followed by an L2 flush (a 256 MB memset), are captured in one CUDA graph,
+    replayed once to warm up and then timed with CUDA events on the capture
+    stream; a graph of the flushes alone is timed the same way and
+    subtracted. So neither host launch gaps (a 30 us kernel is shorter than
+    a Python call) nor inputs left in L2 by the previous call enter the
+    figure."""
     B, H, S, Dqk = g["q"].shape
     Dv = g["v"].shape[-1]
     dev = g["q"].device
@@ -400,20 +408,38 @@ def time_fwd_bwd(ga, torch, st, g, spec, lists, reps=10):
     dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
     ws = torch.empty(ga.attn_bwd_workspace_bytes(torch.bfloat16, B, H, S, S, Dqk, Dv), dtype=torch.uint8,
                      device=dev)
-    fwd = lambda: ga.attn_fwd(g["q"], g["k"], g["v"], 0.0, spec, lists, o=o, lse=lse, stream=st)  # noqa: E731
-    bwd = lambda: ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists,  # noqa: E731
-                              dq=dq, dk=dk, dv=dv, workspace=ws, stream=st)
-    out = []
-    for fn in (fwd, bwd):
-        for _ in range(3):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(reps):
-            fn()
-        e1.record(st)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cs = torch.cuda.Stream(dev)
+    fwd = lambda s: ga.attn_fwd(g["q"], g["k"], g["v"], 0.0, spec, lists, o=o, lse=lse, stream=s)  # noqa: E731
+    bwd = lambda s: ga.attn_bwd(g["q"], g["k"], g["v"], o, g["do"], lse, 0.0, spec, lists,  # noqa: E731
+                                dq=dq, dk=dk, dv=dv, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+
+    def graph_ms(fn):
+        with torch.cuda.stream(cs):
+            for _ in range(3):  # warm-up outside the capture
+                if fn is not None:
+                    fn(cs)
+                flush.zero_()
         torch.cuda.synchronize()
-        out.append(e0.elapsed_time(e1) / reps)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            for _ in range(reps):
+                if fn is not None:
+                    fn(cs)
+                flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):  # a replay runs on the current stream
+            graph.replay()
+            torch.cuda.synchronize()
+            e0.record(cs)
+            graph.replay()
+            e1.record(cs)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    base = graph_ms(None)
+    out = [max(graph_ms(fn) - base, 0.0) / reps for fn in (fwd, bwd)]
     rc = ga.load_library().gbattn_last_device_error(None)
     if rc != 0:
         raise RuntimeError(f"device error {rc} in the workload sweep")
@@ -452,10 +478,10 @@ def sweep_masks(ga, torch, dev, st, g):
                                     "note": "dK/dV on CTA pairs (cta_group::2); the default one-CTA kernel is "
                                             "the bench line's attn_bwd"}
     return dict(masks, config=f"B={B} H={H} Sq=Sk={S} Dqk={Dqk} Dv={Dv} bf16, sparse tiles "
-                              f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}")
+                              f"{P['sparse_m']}x{P['sparse_n']}, rel bias {P['slope']}", timing=SWEEP_TIMING)
 
 
-def sweep_dense(ga, torch, dev, st, rank, reps=10):
+def sweep_dense(ga, torch, dev, st, rank, reps=30):
     """The dense masked workload: B=2, H=8, S=2048, D=64, causal and causal
     sliding W=512, 128x128 lists. FLOPs count the allowed pairs."""
     from block_sparse_attention_tma_gb300.synth import make_inputs
@@ -472,10 +498,11 @@ def sweep_dense(ga, torch, dev, st, rank, reps=10):
                        "fwd_tflops": round(2 * n * 2 * Dd / (fms * 1e-3) / 1e12, 1),
                        "bwd_tflops": round(2 * n * 5 * Dd / (bms * 1e-3) / 1e12, 1)}
     dense["config"] = f"B={Bd} H={Hd} Sq=Sk={Sd} D={Dd} bf16, kernel tiles 128x128"
+    dense["timing"] = SWEEP_TIMING
     return dense
 
 
-def sweep_dynamic(ga, torch, dev, st, rank, dims=(32, 64), reps=10):
+def sweep_dynamic(ga, torch, dev, st, rank, dims=(32, 64), reps=20):
     """The dynamic top-k workload: B=1, H=16, S=8192, top-2048 keys per head by
     an N(0,1) key bias, with causal; kept keys streamed compacted."""
     from block_sparse_attention_tma_gb300.synth import make_inputs
@@ -496,6 +523,7 @@ def sweep_dynamic(ga, torch, dev, st, rank, dims=(32, 64), reps=10):
         del gd, dl
     dyn["config"] = (f"B={Bd} H={Hd} Sq=Sk={Sd} bf16, top-{topk} keys per head by an N(0,1) key bias, with causal; "
                      "kept keys streamed compacted")
+    dyn["timing"] = SWEEP_TIMING
     return dyn
 
 
@@ -721,10 +749,10 @@ def main():
         if args.only == "gqa":
             ext = run_extensions(ga, torch, dev, st, rank, Sk=args.gqa_sk)
         elif args.only == "dense2k":
-            ext = {"dense2k": sweep_dense(ga, torch, dev, st, rank, reps=args.steps)}
+            ext = {"dense2k": sweep_dense(ga, torch, dev, st, rank, reps=max(args.steps, 30))}
         else:
             ext = {"dynamic_topk": sweep_dynamic(ga, torch, dev, st, rank, dims=(args.dyn_d,) if args.dyn_d else (32, 64),
-                                                 reps=args.steps)}
+                                                 reps=max(args.steps, 20))}
         if rank == 0:
             print(json.dumps({"only": args.only, **ext}), flush=True)
     else:

@@ -47,6 +47,19 @@
 
 namespace gb {
 
+// 64 TMEM columns in one load (32 lanes x 64 x 32 bit); the softmax warps'
+// S tile half (the backward kernels keep two 32-column loads: with this one
+// their gathered / softcap variants spill and they measured no faster).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : GB_R16(r, 0), GB_R16(r, 16), GB_R16(r, 32), GB_R16(r, 48)
+      : "r"(taddr));
+}
+
 // Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads that
 // also returns the OR of their predicates. Every participant must reach it:
 // callers pass their failure flag through it and leave their loop together.
@@ -518,8 +531,8 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
       }
       tc_fence_after();
       float t[CWF];
-      tmem_ld32(tl + sb * 128 + cb, reinterpret_cast<uint32_t*>(t));
-      if constexpr (CWF == 64) tmem_ld32(tl + sb * 128 + cb + 32, reinterpret_cast<uint32_t*>(t) + 32);
+      if constexpr (CWF == 64) tmem_ld64(tl + sb * 128 + cb, reinterpret_cast<uint32_t*>(t));
+      else tmem_ld32(tl + sb * 128 + cb, reinterpret_cast<uint32_t*>(t));
       tmem_wait_ld32(reinterpret_cast<uint32_t*>(t));
       if constexpr (CWF == 64) reg_fence32(reinterpret_cast<uint32_t*>(t) + 32);
       {

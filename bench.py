@@ -255,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e and args.only == "all":
-        e2e = run_e2e(args, ga, torch, dev, x, dx, spec, lists, st)
+        e2e = run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=args.e2e_chunks)
     if args.only != "all":
         print(json.dumps({"only": args.only, "ms": {n: round(statistics.mean(v), 4) for n, v in ev.items()},
                           "total_ms": round(total_ms, 3)}), flush=True)
@@ -539,7 +539,7 @@ def run_workload_sweep(ga, torch, dev, st, g, rank):
     return {"dense2k": dense, "mla16k_mask_kinds": masks, "dynamic_topk": dyn}
 
 
-def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=4):
+def run_e2e(args, ga, torch, dev, x, dx, spec, lists, st, nch=8):
     """Same step through the C ABI with host buffers: every step copies its
     inputs in from pinned host memory and its results out, inside the timed
     region. The step is cut into `nch` independent chunks (heads for the
@@ -714,6 +714,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=8, choices=[1, 2, 4, 8, 16],
+                    help="independent chunks (and streams) of the end-to-end step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extensions", action="store_true", help="skip the informational lines (paged GQA decode, mask-kind and dynamic sweeps)")
     ap.add_argument("--quick-cpu", action="store_true", help="cpu_baseline on a 4096-token sample")

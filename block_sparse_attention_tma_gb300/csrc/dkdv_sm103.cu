@@ -14,9 +14,12 @@ namespace gb {
 //   S^T_n = K Q_n^T -> R;   P^T_n = exp2(...) -> X (bf16);
 //   dP^T_n = V dO_n^T -> R; dV += P^T_n dO_n (A = X);
 //   dS^T_n = P^T (dP^T - delta) -> X (bf16);  dK += dS^T_n Q_n (A = X).
-// dK of tile n is issued after S^T of tile n+1, so the tensor pipe runs
-// S^T_{n+1} / dK_n / dP^T_{n+1} / dV_{n+1} back to back while the dS warps
-// work. TMEM: R [0,128), X [128,192), dV [192,192+Dv), dK [192+Dv, +Dqk).
+// Two threads issue the products: one the score-side S^T_n and dP^T_n
+// (writing R), the other the gradient-side dV_n and dK_n (reading X). A
+// thread's tcgen05.mma issue keeps pace with the tensor pipe, so every gap
+// between its products (a barrier wait, the loop control) would leave the
+// pipe idle; with two issuers one thread's gaps are filled by the other's
+// products. TMEM: R [0,128), X [128,192), dV [192,192+Dv), dK [192+Dv, +Dqk).
 template <int DQK, int DV>
 struct DkdvCfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
@@ -27,7 +30,10 @@ struct DkdvCfg {
   // elementwise warps: NG per TMEM lane quarter, each thread one key row and
   // CW = 128 / NG of the tile's query columns
   static constexpr int NG = 2, CW = 128 / NG;
-  static constexpr int THREADS = 64 + 128 * NG;
+  // warp 0 producer, warp 1 score-side MMA issuer, warps 2 .. 1 + 4 NG
+  // elementwise, warp 2 + 4 NG gradient-side MMA issuer
+  static constexpr int THREADS = 64 + 128 * NG + 32;
+  static constexpr int WGRAD = 2 + 4 * NG;
   static constexpr int NEW = 128 * NG;  // elementwise threads
   static constexpr int GST = DQK >= 192 ? 1 : 2;
   static constexpr int T_R = 0, T_X = 128, T_DV = 192, T_DK = 192 + DV;
@@ -35,8 +41,10 @@ struct DkdvCfg {
   // B_RA / B_RB: the elementwise warps have copied S^T / dP^T out of R (R may
   // be overwritten); B_P / B_DS: P^T / dS^T written to X.
   // B_FIN: the second half's key-bias partial sums are in shared memory.
+  // B_GE (dO stage free) completes on two commits: dP^T (score side) and dV
+  // (gradient side) both read the stage.
   enum { B_KV, B_QF, B_QE = B_QF + QST, B_GF = B_QE + QST, B_GE = B_GF + GST, B_S = B_GE + GST, B_RA, B_P, B_DP, B_RB,
-         B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, B_FIN, NBAR };
+         B_DVD, B_DS, B_DKD, B_DONE, B_DRAIN, B_DRAIN2, B_FIN, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
       1024 + QTILE + VTILE + QST * QTILE + GST * VTILE + QST * 1024 + 512 * (NG - 1) + 4 * (kMaxGroup + 4) + TCAP * 2 +
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
     for (int b = 0; b < C::NBAR; ++b)
       mbar_init(bar + b, (b == C::B_P || b == C::B_DS || b == C::B_RA || b == C::B_RB) ? C::NEW
                          : b == C::B_FIN                                             ? C::NEW - 128
+                         : (b >= C::B_GE && b < C::B_GE + C::GST)                   ? 2
                                                                                      : 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -278,28 +287,14 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score-side MMA issuer
+    // per query tile n: S^T_n once dP^T_{n-1} has been copied out of R, then
+    // dP^T_n once S^T_n has been
     if (lane == 0) {
-      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));     // K, K-major
-      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));     // Q, K-major
-      const SDesc qm = make_sdesc(smem_u32(sQ), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // Q, MN-major
-      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));     // V, K-major
-      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));     // dO, K-major
-      const SDesc gm = make_sdesc(smem_u32(sG), C::VSLAB, 8 * C::SWV, swz_code(C::SWV));  // dO, MN-major
-      auto issue_dk = [&](int j) {
-        const int qs = j % C::QST;
-        const uint32_t blo = qm.lo + ((qs * C::QTILE) >> 4);
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::T_DK, tmem + C::T_X + kk * 8, blo + mnmajor_step(kk, C::SWQ), qm.hi, C::ID_DK,
-                 kk > 0 ? 1u : acc0);
-        umma_commit(bar + C::B_DKD);
-        umma_commit(bar + C::B_QE + qs);
-      };
-      // Issue order per query tile n: S^T_n, dK_{n-1}, dP^T_n, dV_n. R is
-      // reused as soon as the elementwise warps have copied it to registers,
-      // so dP^T_n runs while P^T_n is computed and S^T_{n+1} while dS^T_n is.
+      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));  // K, K-major
+      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));  // Q, K-major
+      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));  // V, K-major
+      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));  // dO, K-major
       int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -319,11 +314,6 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
-        if (n >= 1) {
-          if (!(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;  // dS^T_{n-1} in X
-          tc_fence_after();
-          issue_dk(n - 1);
-        }
         if (!(ok = mbar_wait(bar + C::B_RA, n & 1, abort_flag))) break;  // S^T_n read
         const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
@@ -336,11 +326,34 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
                    blo + kmajor_step(kk, C::SWV, C::VSLAB), gd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_DP);
+        umma_commit(bar + C::B_GE + gs);
+        ++n;
+      }
+      if (*abort_flag) {
+        umma_commit(bar + C::B_DRAIN);
+        mbar_drain(bar + C::B_DRAIN, 0, abort_flag);
+      }
+    }
+  } else if (warp == C::WGRAD) {
+    // ------------------------------------------------------------ gradient-side MMA issuer
+    // per query tile n: dV += P^T_n dO_n once P^T_n is in X, then
+    // dK += dS^T_n Q_n once dS^T_n is
+    if (lane == 0) {
+      const SDesc qm = make_sdesc(smem_u32(sQ), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // Q, MN-major
+      const SDesc gm = make_sdesc(smem_u32(sG), C::VSLAB, 8 * C::SWV, swz_code(C::SWV));  // dO, MN-major
+      int n = 0;
+      bool ok = true;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int q0;
+      bool masked;
+      while (ok && it.next(&q0, &masked)) {
+        const uint32_t acc0 = n > 0 ? 1u : 0u;
+        const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;  // P^T_n in X
+        if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
         tc_fence_after();
         {
           const uint32_t blo = gm.lo + ((gs * C::VTILE) >> 4);
-          const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + C::T_DV, tmem + C::T_X + kk * 8, blo + mnmajor_step(kk, C::SWV), gm.hi, C::ID_DV,
@@ -348,18 +361,25 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
         }
         umma_commit(bar + C::B_DVD);
         umma_commit(bar + C::B_GE + gs);
-        ++n;
-      }
-      if (ok && n >= 1) {
-        if ((ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) {
-          tc_fence_after();
-          issue_dk(n - 1);
+        const int qs = n % C::QST;
+        if (!(ok = mbar_wait(bar + C::B_DS, n & 1, abort_flag))) break;  // dS^T_n in X
+        if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
+        tc_fence_after();
+        {
+          const uint32_t blo = qm.lo + ((qs * C::QTILE) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::T_DK, tmem + C::T_X + kk * 8, blo + mnmajor_step(kk, C::SWQ), qm.hi, C::ID_DK,
+                   kk > 0 ? 1u : acc0);
         }
+        umma_commit(bar + C::B_DKD);
+        umma_commit(bar + C::B_QE + qs);
+        ++n;
       }
       umma_commit(bar + C::B_DONE);
       if (*abort_flag) {
-        umma_commit(bar + C::B_DRAIN);
-        mbar_drain(bar + C::B_DRAIN, 0, abort_flag);
+        umma_commit(bar + C::B_DRAIN2);
+        mbar_drain(bar + C::B_DRAIN2, 0, abort_flag);
       }
     }
   } else {

@@ -522,6 +522,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// bf16x2 of two softmax probabilities (finite, >= 0) on the integer pipe:
+// the high half of each bit pattern after adding half a bf16 ulp, i.e. round
+// to nearest with ties away from zero. The float-to-bf16x2 conversion
+// instruction issues to the same unit as ex2, which the softmax loops keep
+// busy. An input that is NaN need not stay NaN (0x7FFFFFFF becomes -0); the
+// dK/dV kernel, its user, carries the fp32 value on into dS, so a NaN still
+// reaches dK.
+__device__ __forceinline__ uint32_t pack_bf16_prob(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+}
 
 __device__ __forceinline__ int floor_div(int a, int b) {
   int q = a / b;

@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
           }
         }
 #pragma unroll
-        for (int c = 0; c < CW / 2; ++c) pk[c] = pack_bf16(pf[2 * c], pf[2 * c + 1]);
+        for (int c = 0; c < CW / 2; ++c) pk[c] = pack_bf16_prob(pf[2 * c], pf[2 * c + 1]);
       }
       // X still holds dS^T of the previous tile until its dK MMA completes
       if (n >= 1) {

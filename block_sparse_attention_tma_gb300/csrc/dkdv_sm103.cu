@@ -314,9 +314,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
-        if (!(ok = mbar_wait(bar + C::B_RA, n & 1, abort_flag))) break;  // S^T_n read
+        // the dO tile has landed long before S^T_n is read: its wait goes first
         const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar + C::B_RA, n & 1, abort_flag))) break;  // S^T_n read
         tc_fence_after();
         {
           const uint32_t blo = gd.lo + ((gs * C::VTILE) >> 4);
@@ -348,9 +349,13 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
       bool masked;
       while (ok && it.next(&q0, &masked)) {
         const uint32_t acc0 = n > 0 ? 1u : 0u;
-        const int gs = n % C::GST;
-        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;  // P^T_n in X
+        // the Q and dO tiles land long before P^T_n is written: their waits
+        // go first, off the path from the elementwise warps' arrivals to the
+        // products
+        const int gs = n % C::GST, qs = n % C::QST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(bar + C::B_P, n & 1, abort_flag))) break;  // P^T_n in X
         tc_fence_after();
         {
           const uint32_t blo = gm.lo + ((gs * C::VTILE) >> 4);
@@ -361,9 +366,7 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
         }
         umma_commit(bar + C::B_DVD);
         umma_commit(bar + C::B_GE + gs);
-        const int qs = n % C::QST;
         if (!(ok = mbar_wait(bar + C::B_DS, n & 1, abort_flag))) break;  // dS^T_n in X
-        if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
         tc_fence_after();
         {
           const uint32_t blo = qm.lo + ((qs * C::QTILE) >> 4);

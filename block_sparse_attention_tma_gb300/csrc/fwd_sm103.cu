@@ -403,10 +403,12 @@ float* colterm = reinterpret_cast<float*>(sV + C::VST * C::VTILE);  // [4 NG war
       const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));
       const SDesc vd = make_sdesc(smem_u32(sV), C::VSLAB, 8 * C::SWV, swz_code(C::SWV));
       auto issue_pv = [&](int j) -> bool {
+        // the V tile landed long before P_j is written: its wait goes first,
+        // so that P_j's arrival is followed directly by the product
         const int sb = j & 1;
-        if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
         const int vs = j % C::VST;
         if (!mbar_wait(v_full + vs, (j / C::VST) & 1, abort_flag)) return false;
+        if (!mbar_wait(p_full + sb, (j >> 1) & 1, abort_flag)) return false;
         if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         tc_fence_after();
         // B = V tile, MN-major: 16 key rows per step; LBO = slab stride, SBO = 8 rows

@@ -434,8 +434,10 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
         }
       }
       const int qs = n % C::QST;
-      ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
-      if (ok) ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag);  // lse2 / delta landed
+      // lse2 / delta landed with Q, before S^T_n was issued: that wait goes
+      // first, off the path from S^T_n's completion to the copy-out
+      ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag);
+      if (ok) ok = mbar_wait(bar + C::B_S, n & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;

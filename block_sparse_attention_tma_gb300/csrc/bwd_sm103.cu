@@ -100,8 +100,9 @@ __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_b
 // CTA = (b, h, 128-row query tile), walking the forward lists (thread = query
 // row). Per kv tile n: S_n = Q K_n^T -> [0,128), dP_n = dO V_n^T -> [128,256);
 // dS_n = P (dP - delta) -> [448,512) (bf16); dQ += dS_n K_n -> [256,256+Dqk).
-// dQ of tile n is issued after S of tile n+1, so the K stage of tile n is
-// free only once dQ_n is done; the V stage once dP_n is done.
+// Two threads issue the products (S_n and dP_n from one, dQ_n from the
+// other), so the gaps of one issuer are filled by the other's products. The K
+// stage of tile n is free once dQ_n is done; the V stage once dP_n is done.
 template <int DQK, int DV, bool GAT>
 struct DqCfg {
   static constexpr int SWQ = DQK >= 64 ? 128 : 64;
@@ -114,13 +115,14 @@ struct DqCfg {
   // cannot spare.
   static constexpr int KST = DQK <= 64 || (DQK == 128 && !GAT) ? 3 : 2;
   static constexpr int VST = DQK >= 192 || (DQK == 128 && !GAT) ? 1 : 2;
-  static constexpr bool DQ_FIRST = DQK > 32;  // dQ_{n-1} issued before dP_n
+  // warp 0 producer, warp 1 S / dP issuer, warps 2..9 elementwise, warp 10 dQ issuer
+  static constexpr int THREADS = 352, WDQ = 10;
   static constexpr int T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 448;
   static_assert(T_DQ + DQK <= T_DS, "TMEM budget");
   // B_RS / B_RP: the elementwise warps have copied S / dP out of TMEM;
   // B_DS: dS written to TMEM.
   enum { B_QG, B_KF, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST, B_S = B_VE + VST, B_DP, B_RS, B_RP, B_DS,
-         B_DQD, B_DONE, B_DRAIN, NBAR };
+         B_DQD, B_DONE, B_DRAIN, B_DRAIN2, NBAR };
   static constexpr int TCAP = 1024;  // visited-tile list entries (uint16)
   static constexpr int SMEM_USED =
       1024 + QTILE + VTILE + KST * QTILE + VST * VTILE + 8 * 2 * 64 * 4 + TCAP * 2 + NBAR * 8 + 32 + 2048;
@@ -130,7 +132,7 @@ struct DqCfg {
 };
 
 template <int DQK, int DV, bool CAP, bool GAT>
-__global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DqCfg<DQK, DV, GAT>::THREADS, 1) dq_kernel(const __grid_constant__ BwdParams p) {
   using C = DqCfg<DQK, DV, GAT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -286,29 +288,13 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
       if (lane == 0 && *abort_flag && n > 0) mbar_drain(bar + C::B_QG, 0, abort_flag);
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ S / dP issuer
+    // per kv tile n: S_n once S_{n-1} has been copied out, dP_n once dP_{n-1} has
     if (lane == 0) {
-      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));     // Q, K-major
-      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));     // dO, K-major
-      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));     // K, K-major
-      const SDesc km = make_sdesc(smem_u32(sK), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // K, MN-major
-      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));     // V, K-major
-      auto issue_dq = [&](int jt) {
-        const int ks = jt % C::KST;
-        const uint32_t blo = km.lo + ((ks * C::QTILE) >> 4);
-        const uint32_t acc0 = jt > 0 ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::T_DQ, tmem + C::T_DS + kk * 8, blo + mnmajor_step(kk, C::SWQ), km.hi, C::ID_DQ,
-                 kk > 0 ? 1u : acc0);
-        umma_commit(bar + C::B_DQD);
-        umma_commit(bar + C::B_KE + ks);
-      };
-      // Issue order per kv tile n: S_n, dQ_{n-1}, dP_n (Dqk = 32: S_n, dP_n,
-      // dQ_{n-1}). S and dP are reused as soon as the elementwise warps have
-      // copied them to registers. dQ_{n-1} ahead of dP_n frees the K stage of
-      // tile n-1 one MMA earlier, so the next K load overlaps dP_n (16K
-      // causal 192/128 bwd 4.15 -> 3.84 ms); at Dqk = 32 the early dP_n
-      // measured slightly better.
+      const SDesc qd = make_sdesc(smem_u32(sQ), 16, 8 * C::SWQ, swz_code(C::SWQ));  // Q, K-major
+      const SDesc gd = make_sdesc(smem_u32(sG), 16, 8 * C::SWV, swz_code(C::SWV));  // dO, K-major
+      const SDesc kd = make_sdesc(smem_u32(sK), 16, 8 * C::SWQ, swz_code(C::SWQ));  // K, K-major
+      const SDesc vd = make_sdesc(smem_u32(sV), 16, 8 * C::SWV, swz_code(C::SWV));  // V, K-major
       int n = 0;
       bool ok = true;
       auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
@@ -329,11 +315,6 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), kd.hi, C::ID_S, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
-        if (C::DQ_FIRST && n >= 1) {
-          if (!(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          issue_dq(n - 1);
-        }
         if (!(ok = mbar_wait(bar + C::B_VF + vs, (n / C::VST) & 1, abort_flag))) break;
         if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
         if (n >= 1 && !(ok = mbar_wait(bar + C::B_RP, (n - 1) & 1, abort_flag))) break;  // dP_{n-1} read
@@ -347,23 +328,48 @@ __global__ void __launch_bounds__(320, 1) dq_kernel(const __grid_constant__ BwdP
         }
         umma_commit(bar + C::B_DP);
         umma_commit(bar + C::B_VE + vs);
-        if (!C::DQ_FIRST && n >= 1) {
-          if (!(ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          issue_dq(n - 1);
-        }
         ++n;
       }
-      if (ok && n >= 1) {
-        if ((ok = mbar_wait(bar + C::B_DS, (n - 1) & 1, abort_flag))) {
-          tc_fence_after();
-          issue_dq(n - 1);
-        }
-      }
-      umma_commit(bar + C::B_DONE);
       if (*abort_flag) {
         umma_commit(bar + C::B_DRAIN);
         mbar_drain(bar + C::B_DRAIN, 0, abort_flag);
+      }
+    }
+  } else if (warp == C::WDQ) {
+    // ------------------------------------------------------------ dQ issuer
+    // per kv tile n: dQ += dS_n K_n once dS_n is in TMEM (S_n, which read the
+    // same K stage, completed before the elementwise warps wrote dS_n)
+    if (lane == 0) {
+      const SDesc km = make_sdesc(smem_u32(sK), C::QSLAB, 8 * C::SWQ, swz_code(C::SWQ));  // K, MN-major
+      int n = 0;
+      bool ok = true;
+      auto it = tile_seq(slot, tlist, ntiles, C::TCAP, nslots);
+      int kv0;
+      bool masked;
+      while (ok && it.next(&kv0, &masked)) {
+        const int ks = n % C::KST;
+        // the K tile landed before S_n was issued: its wait goes first, off
+        // the path from the elementwise warps' dS_n to the product
+        if (!(ok = mbar_wait(bar + C::B_KF + ks, (n / C::KST) & 1, abort_flag))) break;
+        if constexpr (GAT) fence_async_smem();  // rows copied with cp.async
+        if (!(ok = mbar_wait(bar + C::B_DS, n & 1, abort_flag))) break;
+        tc_fence_after();
+        {
+          const uint32_t blo = km.lo + ((ks * C::QTILE) >> 4);
+          const uint32_t acc0 = n > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::T_DQ, tmem + C::T_DS + kk * 8, blo + mnmajor_step(kk, C::SWQ), km.hi, C::ID_DQ,
+                   kk > 0 ? 1u : acc0);
+        }
+        umma_commit(bar + C::B_DQD);
+        umma_commit(bar + C::B_KE + ks);
+        ++n;
+      }
+      umma_commit(bar + C::B_DONE);
+      if (*abort_flag) {
+        umma_commit(bar + C::B_DRAIN2);
+        mbar_drain(bar + C::B_DRAIN2, 0, abort_flag);
       }
     }
   } else {
@@ -538,7 +544,8 @@ template <int DQK, int DV, bool CAP, bool GAT>
 static int launch_dq(const BwdParams& prm, const Shape& s, cudaStream_t st) {
   static std::atomic<unsigned long long> attr{0};
   if (ensure_smem(dq_kernel<DQK, DV, CAP, GAT>, DqCfg<DQK, DV, GAT>::SMEM, attr)) return GBATTN_ERR_CUDA;
-  dq_kernel<DQK, DV, CAP, GAT><<<((s.Sq + 127) / 128) * s.B * s.H, 320, DqCfg<DQK, DV, GAT>::SMEM, st>>>(prm);
+  dq_kernel<DQK, DV, CAP, GAT>
+      <<<((s.Sq + 127) / 128) * s.B * s.H, DqCfg<DQK, DV, GAT>::THREADS, DqCfg<DQK, DV, GAT>::SMEM, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 

@@ -87,24 +87,32 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The spin of mbar_wait after its first probe failed, out of line: a wait
+// site then adds only the probe and a call to the kernel's instruction stream
+// (the role loops are long, and their instruction fetch is on the per-tile path).
+static __device__ __noinline__ bool mbar_wait_spin(uint32_t a, uint32_t parity, volatile int* flag,
+                                                   uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(a, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*flag) return false;
+      if (global_ns() - t0 > limit_ns) {
+        raise_dev_error(GBATTN_ERR_TIMEOUT);
+        *flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Waits for the phase with the given parity to complete. Gives up (returns
 // false, raising GBATTN_ERR_TIMEOUT once) after abort.limit_ns, or as soon as
 // the abort flag is set by another role of the same CTA.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& abort) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try(a, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(a, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*abort) return false;
-      if (global_ns() - t0 > abort.limit_ns) {
-        raise_dev_error(GBATTN_ERR_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait_spin(a, parity, abort.flag, abort.limit_ns);
 }
 
 // Bounded wait used only on the way out of an aborted kernel (the same time

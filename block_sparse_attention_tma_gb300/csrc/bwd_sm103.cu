@@ -481,8 +481,10 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV, GAT>::THREADS, 1) dq_kernel(con
         mbar_arrive(bar + C::B_RP);
 #pragma unroll
         for (int c2 = 0; c2 < 32; ++c2) {
-          float d0 = pf[2 * c2] * (__uint_as_float(rp[2 * c2]) - dl);
-          float d1 = pf[2 * c2 + 1] * (__uint_as_float(rp[2 * c2 + 1]) - dl);
+          // two columns per instruction: (dP - delta), then times P
+          float d0, d1;
+          sub2(d0, d1, __uint_as_float(rp[2 * c2]), __uint_as_float(rp[2 * c2 + 1]), dl, dl);
+          mul2(d0, d1, d0, d1, pf[2 * c2], pf[2 * c2 + 1]);
           if constexpr (CAP) {
             d0 *= dd[2 * c2];
             d1 *= dd[2 * c2 + 1];

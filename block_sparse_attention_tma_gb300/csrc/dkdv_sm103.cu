@@ -543,10 +543,12 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
         for (int c4 = 0; c4 < CW / 4; ++c4) {
           const float4 d4 = sd4[c4];
           const uint32_t p01 = pk[2 * c4], p23 = pk[2 * c4 + 1];
-          float d0 = bf_lo(p01) * (__uint_as_float(r[4 * c4 + 0]) - d4.x);
-          float d1 = bf_hi(p01) * (__uint_as_float(r[4 * c4 + 1]) - d4.y);
-          float d2 = bf_lo(p23) * (__uint_as_float(r[4 * c4 + 2]) - d4.z);
-          float d3 = bf_hi(p23) * (__uint_as_float(r[4 * c4 + 3]) - d4.w);
+          // two columns per instruction: (dP^T - delta), then times P^T
+          float d0, d1, d2, d3;
+          sub2(d0, d1, __uint_as_float(r[4 * c4 + 0]), __uint_as_float(r[4 * c4 + 1]), d4.x, d4.y);
+          sub2(d2, d3, __uint_as_float(r[4 * c4 + 2]), __uint_as_float(r[4 * c4 + 3]), d4.z, d4.w);
+          mul2(d0, d1, d0, d1, bf_lo(p01), bf_hi(p01));
+          mul2(d2, d3, d2, d3, bf_lo(p23), bf_hi(p23));
           if constexpr (DB) dbs += (d0 + d1) + (d2 + d3);
           if constexpr (CAP) {
             d0 *= bf_lo(dc[2 * c4]);

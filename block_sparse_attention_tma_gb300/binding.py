@@ -79,6 +79,8 @@ _SIGS = [
     # include/gbattn_test.h: a test hook, not part of the attention API
     ("gbattn_test_fwd_stalled", ctypes.c_int, [ctypes.c_int] * 5 + [ctypes.c_void_p] * 5
      + [ctypes.c_ulonglong, ctypes.c_void_p]),
+    ("gbattn_test_bwd_stalled", ctypes.c_int, [ctypes.c_int] * 4 + [ctypes.c_void_p] * 10
+     + [ctypes.c_size_t, ctypes.c_ulonglong, ctypes.c_void_p]),
 ]
 
 EXPORTS = [s[0] for s in _SIGS]

@@ -463,6 +463,28 @@ int gbattn_test_fwd_stalled(int B, int H, int Sq, int Sk, int D, const void* q, 
   return fwd_bf16_launch(s, q, k, v, resolve_scale(0.f, D), hm, o, lse, static_cast<cudaStream_t>(stream), &hook);
 }
 
+int gbattn_test_bwd_stalled(int B, int H, int S, int D, const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, unsigned long long wait_ns, gbattn_stream stream) {
+  if (!dims_ok(B, H, S, S) || !q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return GBATTN_ERR_ARG;
+  if (wait_ns < 1 || wait_ns > 2000000000ull) return GBATTN_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return GBATTN_ERR_ALIGN;
+  if (D != 32 && D != 64 && D != 128) return GBATTN_ERR_UNSUPPORTED;
+  if (!bf16_seq_ok(S, S)) return GBATTN_ERR_UNSUPPORTED;
+  const Shape s{B, H, S, S, D, D, H};
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(s)) return GBATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return GBATTN_ERR_ALIGN;
+  const int rc = device_check();
+  if (rc) return rc;
+  HostMask hm;
+  check_mask(nullptr, &hm);
+  const BwdTestHook hook{wait_ns, 1};
+  return bwd_bf16_launch(s, q, k, v, o, dout, lse, resolve_scale(0.f, D), hm, dq, dk, dv, nullptr, workspace,
+                         static_cast<cudaStream_t>(stream), &hook);
+}
+
 int gbattn_set_dkdv_cta_pair(int mode, int* previous) {
   if (mode < -1 || mode > 1) return GBATTN_ERR_ARG;
   const int prev = g_dkdv_pair.exchange(mode);

@@ -30,6 +30,7 @@ struct BwdParams {
   const int32_t* kidx; // [BH][Sk] kept key indices (gathered keys)
   const __nv_bfloat16 *gk, *gv;  // K [B*H*Sk, Dqk], V [B*H*Sk, Dv] (gathered keys)
   unsigned long long wait_ns;     // time limit of every wait (0 = kWaitLimitNs)
+  int test_withhold;              // test hook: the first dO tile (dK/dV) / K tile (dQ) is never loaded
   int hgroup;                     // dQ grid order: query heads per group (head_group), 0 = none
   int hgroup_kv;                  // dK/dV grid order: key/value heads per group
 };

@@ -226,10 +226,13 @@ __global__ void __launch_bounds__(DqCfg<DQK, DV, GAT>::THREADS, 1) dq_kernel(con
           }
           const int ks = n % C::KST;
           if (n >= C::KST && !(ok = mbar_wait(bar + C::B_KE + ks, ((n / C::KST) + 1) & 1, abort_flag))) break;
-          mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
-          for (int j = 0; j < C::NQSLAB; ++j)
-            tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0, bkv);
-          ++nk;
+          if (!(p.test_withhold && n == 0)) {
+            mbar_expect_tx(bar + C::B_KF + ks, C::QTILE);
+            for (int j = 0; j < C::NQSLAB; ++j)
+              tma_load_3d(sK + ks * C::QTILE + j * C::QSLAB, &p.tm_k, bar + C::B_KF + ks, j * (C::SWQ / 2), kv0,
+                          bkv);
+          }
+          ++nk;  // a withheld tile counts too: its drain below gives up after the time limit
           const int vs = n % C::VST;
           if (n >= C::VST && !(ok = mbar_wait(bar + C::B_VE + vs, ((n / C::VST) + 1) & 1, abort_flag))) break;
           mbar_expect_tx(bar + C::B_VF + vs, C::VTILE);
@@ -592,9 +595,13 @@ static int launch_dq_cap(const BwdParams& prm, const Shape& s, bool cap, cudaStr
 
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, float scale, const HostMask& m, void* dq, void* dk, void* dv,
-                    float* dkey_bias, void* ws, cudaStream_t st) {
+                    float* dkey_bias, void* ws, cudaStream_t st, const BwdTestHook* hook) {
   BwdParams prm;
   memset(&prm, 0, sizeof(prm));
+  if (hook) {
+    prm.wait_ns = hook->wait_ns;
+    prm.test_withhold = hook->withhold_first_tiles;
+  }
   const int BH = s.B * s.H;
   const int swq = s.Dqk >= 64 ? 128 : 64, swv = s.Dv >= 64 ? 128 : 64;
   if (!make_tmap_bf16_3d(&prm.tm_q, q, s.Dqk, s.Sq, BH, swq)) return GBATTN_ERR_CUDA;

@@ -216,10 +216,12 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
           ++nq;
           const int gs = n % C::GST;
           if (n >= C::GST && !(ok = mbar_wait(bar + C::B_GE + gs, ((n / C::GST) + 1) & 1, abort_flag))) break;
-          mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
-          for (int j = 0; j < C::NVSLAB; ++j)
-            tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bq);
-          ++ng;
+          if (!(p.test_withhold && n == 0)) {
+            mbar_expect_tx(bar + C::B_GF + gs, C::VTILE);
+            for (int j = 0; j < C::NVSLAB; ++j)
+              tma_load_3d(sG + gs * C::VTILE + j * C::VSLAB, &p.tm_do, bar + C::B_GF + gs, j * (C::SWV / 2), q0, bq);
+          }
+          ++ng;  // a withheld tile counts too: its drain below gives up after the time limit
           ++n;
         }
         if (*abort_flag) {

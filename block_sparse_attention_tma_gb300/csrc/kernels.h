@@ -135,9 +135,16 @@ int fwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v,
                     const HostMask& m, void* o, float* lse, cudaStream_t st, const FwdTestHook* hook = nullptr);
 int fwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, float scale,
                     const HostMask& m, float* o, float* lse, cudaStream_t st);
+// Test hook of the bf16 backward: a shorter wait limit, and the dO tile of
+// each dK/dV CTA's first query tile and the K tile of each dQ CTA's first key
+// tile withheld, so that the MMA issuers' waits for them run out.
+struct BwdTestHook {
+  unsigned long long wait_ns;
+  int withhold_first_tiles;
+};
 int bwd_bf16_launch(const Shape& s, const void* q, const void* k, const void* v, const void* o,
                     const void* dout, const float* lse, float scale, const HostMask& m, void* dq, void* dk,
-                    void* dv, float* dkey_bias, void* ws, cudaStream_t st);
+                    void* dv, float* dkey_bias, void* ws, cudaStream_t st, const BwdTestHook* hook = nullptr);
 int bwd_fp32_launch(const Shape& s, const float* q, const float* k, const float* v, const float* o,
                     const float* dout, const float* lse, float scale, const HostMask& m, float* dq, float* dk,
                     float* dv, float* dkey_bias, void* ws, cudaStream_t st);

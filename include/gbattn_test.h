@@ -35,6 +35,26 @@ extern "C" {
 int gbattn_test_fwd_stalled(int B, int H, int Sq, int Sk, int D, const void* q, const void* k, const void* v,
                             void* o, float* lse, unsigned long long wait_ns, gbattn_stream stream);
 
+/*
+ * gbattn_test_bwd_stalled - the bf16 tensor-core backward of attn_bwd (no
+ * mask, B x H heads of S queries over S keys, Dqk = Dv = D, the one-CTA
+ * dK/dV kernel unless gbattn_set_dkdv_cta_pair selected the pair) launched
+ * with two changes: every mbarrier wait gives up after wait_ns nanoseconds,
+ * the producer of each dK/dV CTA never loads the dO tile of its first query
+ * tile, and the producer of each dQ CTA never loads the K tile of its first
+ * key tile, so both kernels' MMA issuers' waits run out.
+ *   q, k, v, o, dout [B, H, S, D] bf16, lse [B, H, S] fp32 (as attn_fwd wrote
+ *   it), dq / dk / dv [B, H, S, D] bf16, workspace of at least
+ *   attn_bwd_workspace_bytes(GBATTN_BF16, B, H, S, S, D, D) bytes: caller-owned
+ *   device memory, 16-byte aligned. D in {32, 64, 128}; 1 <= wait_ns <= 2e9.
+ * dQ, dK and dV are left undefined. Returns GBATTN_OK once the launches are
+ * queued (the timeout is read back with gbattn_last_device_error, which also
+ * clears it), or the argument codes of attn_bwd.
+ */
+int gbattn_test_bwd_stalled(int B, int H, int S, int D, const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, unsigned long long wait_ns, gbattn_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,6 +39,7 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, n), n
     assert set(bd.EXPORTS) >= set(declared_functions())
     assert "gbattn_test_fwd_stalled" in declared_functions()
+    assert "gbattn_test_bwd_stalled" in declared_functions()
     assert lib.gbattn_version() == 102
 
 
@@ -164,6 +165,19 @@ def test_stalled_forward_hook_rejects_bad_arguments_on_the_host():
     assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 64, f + 2, f, f, f, f, 10**6, None) == bd.ERR_ALIGN
     assert lib.gbattn_test_fwd_stalled(1, 1, 128, 128, 96, f, f, f, f, f, 10**6, None) == bd.ERR_UNSUPPORTED
     assert lib.gbattn_test_fwd_stalled(0, 1, 128, 128, 64, f, f, f, f, f, 10**6, None) == bd.ERR_ARG
+
+
+def test_stalled_backward_hook_rejects_bad_arguments_on_the_host():
+    lib = ga.load_library()
+    f = FAKE
+    ws = 1 << 30
+    args = lambda B=1, D=64, q=f, wsb=ws, wait=10**6: (B, 1, 128, D, q, f, f, f, f, f, f, f, f, f, wsb, wait, None)
+    assert lib.gbattn_test_bwd_stalled(*args(wait=0)) == bd.ERR_ARG
+    assert lib.gbattn_test_bwd_stalled(*args(wait=3 * 10**9)) == bd.ERR_ARG
+    assert lib.gbattn_test_bwd_stalled(*args(q=f + 2)) == bd.ERR_ALIGN
+    assert lib.gbattn_test_bwd_stalled(*args(D=96)) == bd.ERR_UNSUPPORTED
+    assert lib.gbattn_test_bwd_stalled(*args(B=0)) == bd.ERR_ARG
+    assert lib.gbattn_test_bwd_stalled(*args(wsb=16)) == bd.ERR_WORKSPACE
 
 
 def test_dkdv_cta_pair_selector_host_side():

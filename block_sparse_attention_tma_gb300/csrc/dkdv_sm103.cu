@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
                    blo + kmajor_step(kk, C::SWQ, C::QSLAB), qd.hi, C::ID_ST, kk > 0 ? 1u : 0u);
         }
         umma_commit(bar + C::B_S);
-        // the dO tile has landed long before S^T_n is read: its wait goes first
+        // the dO tile lands independently of the elementwise warps (usually
+        // before S^T_n has been read): its wait goes first
         const int gs = n % C::GST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
         if (!(ok = mbar_wait(bar + C::B_RA, n & 1, abort_flag))) break;  // S^T_n read
@@ -351,9 +352,9 @@ __global__ void __launch_bounds__(DkdvCfg<DQK, DV>::THREADS, 1) dkdv_kernel(cons
       bool masked;
       while (ok && it.next(&q0, &masked)) {
         const uint32_t acc0 = n > 0 ? 1u : 0u;
-        // the Q and dO tiles land long before P^T_n is written: their waits
-        // go first, off the path from the elementwise warps' arrivals to the
-        // products
+        // the Q and dO tiles land independently of the elementwise warps
+        // (usually before P^T_n is written): their waits go first, off the
+        // path from the elementwise warps' arrivals to the products
         const int gs = n % C::GST, qs = n % C::QST;
         if (!(ok = mbar_wait(bar + C::B_GF + gs, (n / C::GST) & 1, abort_flag))) break;
         if (!(ok = mbar_wait(bar + C::B_QF + qs, (n / C::QST) & 1, abort_flag))) break;
